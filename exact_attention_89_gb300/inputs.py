@@ -1,0 +1,75 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the oracle checks.
+
+This module only draws random numbers and names workload shapes; it holds none of the attention
+arithmetic.  Every tensor is drawn on the CPU with a seeded ``torch.Generator`` in the fixed
+order Q, K, V, dO, as iid N(0, 1) fp32, optionally multiplied (the long-sequence stress case
+multiplies Q by 4 to widen the score range), then cast to the working dtype with round-to-
+nearest-even.  The same host tensors feed both the CUDA path and the oracle.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    N: int
+    d: int
+    causal: bool
+    seed: int
+    dtype: torch.dtype
+    backward: bool
+    q_mult: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / (self.d ** 0.5)
+
+    def flops_fwd(self) -> float:
+        """4 B Hq N^2 d, halved for causal (the formula, not N(N+1)/2)."""
+        f = 4.0 * self.B * self.Hq * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+    def flops_bwd(self) -> float:
+        """2.5x the forward count (five contractions instead of two)."""
+        return 2.5 * self.flops_fwd()
+
+
+# The five workloads of the method's evaluation plan.
+WORKLOADS = {
+    "tiny_fp32": Workload("tiny_fp32", 1, 1, 1, 256, 64, False, 0, torch.float32, True),
+    "fwd_d64": Workload("fwd_d64", 4, 16, 16, 1024, 64, False, 1, torch.bfloat16, False),
+    "causal_n4096": Workload("causal_n4096", 2, 32, 32, 4096, 128, True, 2, torch.bfloat16, True),
+    "gqa_n8192": Workload("gqa_n8192", 1, 32, 8, 8192, 128, True, 3, torch.bfloat16, True),
+    "long_n32768": Workload("long_n32768", 1, 16, 16, 32768, 128, True, 4, torch.bfloat16, True,
+                            q_mult=4.0),
+}
+
+
+def make_inputs(B: int, Hq: int, Hkv: int, N: int, d: int, seed: int,
+                dtype: torch.dtype = torch.bfloat16, q_mult: float = 1.0,
+                with_dO: bool = True):
+    """Q [B,Hq,N,d], K, V [B,Hkv,N,d], dO [B,Hq,N,d] (or None) on the CPU, drawn in that order."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.randn(B, Hq, N, d, generator=g, dtype=torch.float32)
+    if q_mult != 1.0:
+        q = q * q_mult
+    k = torch.randn(B, Hkv, N, d, generator=g, dtype=torch.float32)
+    v = torch.randn(B, Hkv, N, d, generator=g, dtype=torch.float32)
+    do = torch.randn(B, Hq, N, d, generator=g, dtype=torch.float32) if with_dO else None
+    out = [t.to(dtype).contiguous() for t in (q, k, v)]
+    out.append(do.to(dtype).contiguous() if do is not None else None)
+    return tuple(out)
+
+
+def workload_inputs(w: Workload, seed_offset: int = 0):
+    """Inputs for a named workload (seed_offset gives independent replicas per rank)."""
+    return make_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed + seed_offset, w.dtype, w.q_mult,
+                       with_dO=w.backward)

@@ -1,0 +1,183 @@
+"""fp64 CPU oracle for exact attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import this package.  The CUDA library never calls it and shares no code with it; the two meet
+only through the seeded input generators, which hold none of the method's arithmetic.
+
+The arithmetic lives in ``attention_oracle.c`` (plain C, fp64, OpenMP over independent rows or
+key columns).  This module compiles it with gcc on first use (or through ``build()``) and wraps
+it with ctypes over numpy float64 arrays laid out [B, H, N, d].
+
+What the oracle computes (see the C file for the page citations):
+  P = softmax(scale * Q K^T, masked pairs weight 0), O = P V, LSE = m + ln l (natural log),
+  dS = P * (dO V^T - D), D = rowsum(dO * O), dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO,
+  with dK, dV summed over the query heads of a KV group (query head hq reads KV head hq // G).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attention_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_D = ctypes.POINTER(ctypes.c_double)
+_I = ctypes.POINTER(ctypes.c_int)
+_L = ctypes.POINTER(ctypes.c_int64)
+
+
+def build(force: bool = False) -> str:
+    """Compile attention_oracle.c into liboracle.so next to it (gcc -O2 -fopenmp). Returns path."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + ".%d.tmp" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            common = [ctypes.c_int] * 6 + [ctypes.c_double]
+            lib.oracle_attention_forward.argtypes = common + [_D, _D, _D, ctypes.c_int, _I, _D, _D, _D]
+            lib.oracle_attention_backward.argtypes = common + [_D, _D, _D, _D, ctypes.c_int, _I, _D, _D, _D]
+            lib.oracle_forward_rows.argtypes = common + [_D, _D, _D, ctypes.c_int, _L, _D, _D]
+            lib.oracle_backward_dq_rows.argtypes = common + [_D, _D, _D, _D, ctypes.c_int, _L, _D]
+            lib.oracle_backward_dkv_cols.argtypes = common + [_D, _D, _D, _D, ctypes.c_int, _L, _D, _D]
+            for name in ("oracle_attention_forward", "oracle_attention_backward",
+                         "oracle_forward_rows", "oracle_backward_dq_rows",
+                         "oracle_backward_dkv_cols", "oracle_num_threads"):
+                getattr(lib, name).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle uses (OMP_NUM_THREADS or all cores)."""
+    return int(_load().oracle_num_threads())
+
+
+def _f64(a) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    return a
+
+
+def _ptr(a: np.ndarray, typ=_D):
+    return a.ctypes.data_as(typ)
+
+
+def _shape(Q, K):
+    B, Hq, N, d = Q.shape
+    Bk, Hkv, Nk, dk = K.shape
+    if (Bk, Nk, dk) != (B, N, d) or Hq % Hkv:
+        raise ValueError("shape mismatch: Q %s K %s" % (Q.shape, K.shape))
+    return B, Hq, Hkv, N, d
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise RuntimeError("%s failed (code %d)" % (what, rc))
+
+
+def forward(Q, K, V, causal: bool, scale: float, heads=None, want_P: bool = False):
+    """Full forward for the listed heads (b*Hq + hq; default all).
+
+    Returns (O [nh, N, d], LSE [nh, N]) and P [nh, N, N] if want_P; with heads=None the outputs
+    are reshaped to [B, Hq, N, d] / [B, Hq, N] (/ [B, Hq, N, N]).
+    """
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, Hq, Hkv, N, d = _shape(Q, K)
+    full = heads is None
+    hs = np.arange(B * Hq, dtype=np.int32) if full else np.asarray(heads, dtype=np.int32)
+    hs = np.ascontiguousarray(hs)
+    nh = len(hs)
+    O = np.zeros((nh, N, d))
+    L = np.zeros((nh, N))
+    P = np.zeros((nh, N, N)) if want_P else None
+    rc = _load().oracle_attention_forward(B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                                          _ptr(Q), _ptr(K), _ptr(V), nh, _ptr(hs, _I),
+                                          _ptr(O), _ptr(L), _ptr(P) if want_P else None)
+    _check(rc, "oracle_attention_forward")
+    if full:
+        O, L = O.reshape(B, Hq, N, d), L.reshape(B, Hq, N)
+        if want_P:
+            P = P.reshape(B, Hq, N, N)
+    return (O, L, P) if want_P else (O, L)
+
+
+def backward(Q, K, V, dO, causal: bool, scale: float, groups=None):
+    """Full backward for the listed KV groups (b*Hkv + hk; default all).
+
+    Returns (dQ [ng, G, N, d], dK [ng, N, d], dV [ng, N, d]); with groups=None reshaped to
+    [B, Hq, N, d] and [B, Hkv, N, d].
+    """
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, Hq, Hkv, N, d = _shape(Q, K)
+    G = Hq // Hkv
+    full = groups is None
+    gs = np.arange(B * Hkv, dtype=np.int32) if full else np.asarray(groups, dtype=np.int32)
+    gs = np.ascontiguousarray(gs)
+    ng = len(gs)
+    dQ = np.zeros((ng, G, N, d))
+    dK = np.zeros((ng, N, d))
+    dV = np.zeros((ng, N, d))
+    rc = _load().oracle_attention_backward(B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                                           _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), ng, _ptr(gs, _I),
+                                           _ptr(dQ), _ptr(dK), _ptr(dV))
+    _check(rc, "oracle_attention_backward")
+    if full:
+        return dQ.reshape(B, Hq, N, d), dK.reshape(B, Hkv, N, d), dV.reshape(B, Hkv, N, d)
+    return dQ, dK, dV
+
+
+def forward_rows(Q, K, V, causal: bool, scale: float, rows):
+    """Sampled rows (flat index (b*Hq + hq)*N + i) -> (O_rows [n, d], LSE_rows [n])."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, Hq, Hkv, N, d = _shape(Q, K)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    O = np.zeros((len(rows), d))
+    L = np.zeros(len(rows))
+    rc = _load().oracle_forward_rows(B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                                     _ptr(Q), _ptr(K), _ptr(V), len(rows), _ptr(rows, _L),
+                                     _ptr(O), _ptr(L))
+    _check(rc, "oracle_forward_rows")
+    return O, L
+
+
+def backward_dq_rows(Q, K, V, dO, causal: bool, scale: float, rows):
+    """Sampled dQ rows (flat index (b*Hq + hq)*N + i) -> [n, d]."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, Hq, Hkv, N, d = _shape(Q, K)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    dQ = np.zeros((len(rows), d))
+    rc = _load().oracle_backward_dq_rows(B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                                         _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), len(rows),
+                                         _ptr(rows, _L), _ptr(dQ))
+    _check(rc, "oracle_backward_dq_rows")
+    return dQ
+
+
+def backward_dkv_cols(Q, K, V, dO, causal: bool, scale: float, cols):
+    """Sampled dK/dV rows (flat index (b*Hkv + hk)*N + j) -> (dK [n, d], dV [n, d])."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, Hq, Hkv, N, d = _shape(Q, K)
+    cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+    dK = np.zeros((len(cols), d))
+    dV = np.zeros((len(cols), d))
+    rc = _load().oracle_backward_dkv_cols(B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                                          _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), len(cols),
+                                          _ptr(cols, _L), _ptr(dK), _ptr(dV))
+    _check(rc, "oracle_backward_dkv_cols")
+    return dK, dV

@@ -1,0 +1,344 @@
+/*
+ * attention_oracle.c -- plain, slow, fp64 CPU reference for exact scaled-dot-product attention.
+ *
+ * TEST INFRASTRUCTURE ONLY. The CUDA library never links, loads or calls this file. Only the
+ * test suite, the smoke check and the benchmark's CPU-baseline leg use it. It shares no code,
+ * header, helper, table or constant with the CUDA kernels.
+ *
+ * What it computes is the plain definition of attention, written out term by term:
+ *
+ *   s_ij  = scale * <q_i, k_j>                     for allowed pairs (i, j)
+ *   m_i   = max_j s_ij,   l_i = sum_j exp(s_ij - m_i)
+ *   P_ij  = exp(s_ij - m_i) / l_i                  (0 for masked pairs)
+ *   O_i   = sum_j P_ij v_j,   LSE_i = m_i + ln l_i  (natural log)
+ *   dP_ij = <dO_i, v_j>,  D_i = <dO_i, O_i>,  dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = scale * sum_j dS_ij k_j
+ *   dK_j  = scale * sum_{query heads of the group} sum_i dS_ij q_i
+ *   dV_j  = sum_{query heads of the group} sum_i P_ij dO_i
+ *
+ * Sources (page title, section, formula):
+ *  - Forward: "Attention's hidden recurrence: an introduction to Flash Attention" (mzeromiko blog),
+ *    section "standard attention / forward": O = Diag((exp(QK^T) (.) M) 1)^-1 (exp(QK^T) (.) M) V.
+ *    Subtracting the row maximum before exp (the stability shift) is from the same page, section
+ *    "blocked form with online-softmax rescaling", and from the FlashAttention note
+ *    (paweldubiel.com), section "averaging block results is not enough" (state m, l, u; result u/l).
+ *  - Mask: FlashAttention DAC'24 reading note (paper.adslab.icu), section "other operators": the
+ *    mask acts on each block of QK^T; mzeromiko blog, "blocked recurrence": M is causal or none.
+ *    Masked pairs carry weight exactly 0 (M multiplies exp(S) by 0), i.e. -inf before softmax.
+ *  - Backward: mzeromiko blog, section "standard attention / backward":
+ *    d(exp(QK^T) (.) M) = Diag(E 1)^-1 (dO V^T - diag(dO O^T) 1^T),  dV = E^T Diag(E 1)^-1 dO,
+ *    dQ = (dE (.) E) K,  dK = (dE (.) E)^T Q  with E = exp(QK^T) (.) M.  Since dE (.) E equals
+ *    P (.) (dP - D 1^T), that is dS above; diag(dO O^T) is D.  The factor `scale` on dQ and dK is
+ *    the chain rule through s = scale * q.k (the pages use scale = 1).
+ *  - GQA: FlashAttention note (paweldubiel.com), last section: grouped-query attention combines
+ *    with the method.  Query head hq reads key/value head hq / (Hq / Hkv) (consecutive groups).
+ *
+ * Layout: every tensor is contiguous [B, H, N, d] fp64 (d fastest); K, V, dK, dV use H = Hkv.
+ * LSE is [B, Hq, N].  Causal means key j <= query i (top-left aligned, Nq = Nk = N).
+ * A row with no allowed key (impossible with these masks) would get O = 0 and LSE = -inf.
+ *
+ * Parallelism: OpenMP over independent rows (or key columns); no blocking or reordering of the
+ * sums beyond what the definition states.  Every function returns 0 on success, nonzero on
+ * invalid arguments or allocation failure.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef int64_t i64;
+
+static int is_allowed(int causal, i64 i, i64 j) { return !causal || j <= i; }
+
+static double dot(const double *a, const double *b, int d) {
+    double acc = 0.0;
+    for (int k = 0; k < d; ++k) acc += a[k] * b[k];
+    return acc;
+}
+
+static int check_shape(int B, int Hq, int Hkv, int N, int d) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || d < 1) return 1;
+    if (Hq % Hkv != 0) return 1;
+    return 0;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * One query row of one head: fills s_row[0..N) with the scores (-INFINITY where masked), turns it
+ * into the probability row in place, writes o_row[0..d) and returns LSE_i.
+ */
+static double softmax_row(const double *qi, const double *k, const double *v, i64 i, int N, int d,
+                          int causal, double scale, double *p_row, double *o_row) {
+    double m = -INFINITY;
+    for (i64 j = 0; j < N; ++j) {
+        if (is_allowed(causal, i, j)) {
+            p_row[j] = scale * dot(qi, k + j * d, d);
+            if (p_row[j] > m) m = p_row[j];
+        } else {
+            p_row[j] = -INFINITY;
+        }
+    }
+    for (int c = 0; c < d; ++c) o_row[c] = 0.0;
+    if (m == -INFINITY) {               /* no allowed key: O = 0, LSE = -inf */
+        for (i64 j = 0; j < N; ++j) p_row[j] = 0.0;
+        return -INFINITY;
+    }
+    double l = 0.0;
+    for (i64 j = 0; j < N; ++j) {
+        double e = is_allowed(causal, i, j) ? exp(p_row[j] - m) : 0.0;
+        p_row[j] = e;
+        l += e;
+    }
+    for (i64 j = 0; j < N; ++j) {
+        p_row[j] /= l;
+        if (p_row[j] != 0.0) {
+            const double *vj = v + j * d;
+            for (int c = 0; c < d; ++c) o_row[c] += p_row[j] * vj[c];
+        }
+    }
+    return m + log(l);
+}
+
+/*
+ * Forward over a list of heads, materialising S and P (N x N) for each head.
+ *   heads[h] = b * Hq + hq.  O_out is [nheads, N, d], LSE_out is [nheads, N].
+ *   P_out (optional, may be NULL) receives the probability matrices [nheads, N, N].
+ */
+int oracle_attention_forward(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
+                             const double *Q, const double *K, const double *V, int nheads,
+                             const int *heads, double *O_out, double *LSE_out, double *P_out) {
+    if (check_shape(B, Hq, Hkv, N, d) || nheads < 0) return 1;
+    const int G = Hq / Hkv;
+    const i64 nn = (i64)N * N, nd = (i64)N * d;
+    double *P = P_out ? NULL : (double *)malloc(sizeof(double) * nn);
+    if (!P_out && !P) return 2;
+    for (int h = 0; h < nheads; ++h) {
+        const int bh = heads[h];
+        if (bh < 0 || bh >= B * Hq) { free(P); return 1; }
+        const int b = bh / Hq, hq = bh % Hq, hk = hq / G;
+        const double *q = Q + (i64)bh * nd;
+        const double *k = K + ((i64)b * Hkv + hk) * nd;
+        const double *v = V + ((i64)b * Hkv + hk) * nd;
+        double *Ph = P_out ? P_out + (i64)h * nn : P;
+#pragma omp parallel for schedule(dynamic, 16)
+        for (i64 i = 0; i < N; ++i)
+            LSE_out[(i64)h * N + i] = softmax_row(q + i * d, k, v, i, N, d, causal, scale,
+                                                  Ph + i * N, O_out + (i64)h * nd + i * d);
+    }
+    free(P);
+    return 0;
+}
+
+/*
+ * Backward over a list of KV groups, materialising P and dS (N x N) for each query head.
+ *   groups[g] = b * Hkv + hk.  dQ_out is [ngroups, G, N, d] (the group's query heads in order),
+ *   dK_out and dV_out are [ngroups, N, d].  O and D come from the oracle's own fp64 forward.
+ */
+int oracle_attention_backward(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
+                              const double *Q, const double *K, const double *V, const double *dO,
+                              int ngroups, const int *groups, double *dQ_out, double *dK_out,
+                              double *dV_out) {
+    if (check_shape(B, Hq, Hkv, N, d) || ngroups < 0) return 1;
+    const int G = Hq / Hkv;
+    const i64 nn = (i64)N * N, nd = (i64)N * d;
+    double *P = (double *)malloc(sizeof(double) * nn);
+    double *O = (double *)malloc(sizeof(double) * nd);
+    double *D = (double *)malloc(sizeof(double) * N);
+    if (!P || !O || !D) { free(P); free(O); free(D); return 2; }
+    for (int g = 0; g < ngroups; ++g) {
+        const int bk = groups[g];
+        if (bk < 0 || bk >= B * Hkv) { free(P); free(O); free(D); return 1; }
+        const int b = bk / Hkv, hk = bk % Hkv;
+        const double *k = K + (i64)bk * nd, *v = V + (i64)bk * nd;
+        double *dk = dK_out + (i64)g * nd, *dv = dV_out + (i64)g * nd;
+        memset(dk, 0, sizeof(double) * nd);
+        memset(dv, 0, sizeof(double) * nd);
+        for (int r = 0; r < G; ++r) {
+            const int hq = hk * G + r;
+            const double *q = Q + ((i64)b * Hq + hq) * nd;
+            const double *dor = dO + ((i64)b * Hq + hq) * nd;
+            double *dq = dQ_out + ((i64)g * G + r) * nd;
+            /* forward: P, O, then D_i = <dO_i, O_i> */
+#pragma omp parallel for schedule(dynamic, 16)
+            for (i64 i = 0; i < N; ++i) {
+                softmax_row(q + i * d, k, v, i, N, d, causal, scale, P + i * N, O + i * d);
+                D[i] = dot(dor + i * d, O + i * d, d);
+            }
+            /* dV_j += sum_i P_ij dO_i  (parallel over key columns j) */
+#pragma omp parallel for schedule(dynamic, 16)
+            for (i64 j = 0; j < N; ++j)
+                for (i64 i = 0; i < N; ++i) {
+                    const double p = P[i * N + j];
+                    if (p != 0.0)
+                        for (int c = 0; c < d; ++c) dv[j * d + c] += p * dor[i * d + c];
+                }
+            /* dS_ij = P_ij (<dO_i, v_j> - D_i), in place over P; dQ_i = scale sum_j dS_ij k_j */
+#pragma omp parallel for schedule(dynamic, 16)
+            for (i64 i = 0; i < N; ++i) {
+                double *row = P + i * N;
+                for (int c = 0; c < d; ++c) dq[i * d + c] = 0.0;
+                for (i64 j = 0; j < N; ++j) {
+                    if (row[j] == 0.0) continue;
+                    row[j] = row[j] * (dot(dor + i * d, v + j * d, d) - D[i]);
+                    for (int c = 0; c < d; ++c) dq[i * d + c] += row[j] * k[j * d + c];
+                }
+                for (int c = 0; c < d; ++c) dq[i * d + c] *= scale;
+            }
+            /* dK_j += scale sum_i dS_ij q_i  (parallel over key columns j) */
+#pragma omp parallel for schedule(dynamic, 16)
+            for (i64 j = 0; j < N; ++j) {
+                for (i64 i = 0; i < N; ++i) {
+                    const double ds = P[i * N + j];
+                    if (ds != 0.0)
+                        for (int c = 0; c < d; ++c) dk[j * d + c] += scale * ds * q[i * d + c];
+                }
+            }
+        }
+    }
+    free(P); free(O); free(D);
+    return 0;
+}
+
+/*
+ * Sampled forward rows: rows[r] = (b * Hq + hq) * N + i.  O_rows is [nrows, d], LSE_rows [nrows].
+ * Each row materialises its own score/probability row; cost O(N d) per row.
+ */
+int oracle_forward_rows(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
+                        const double *Q, const double *K, const double *V, int nrows,
+                        const i64 *rows, double *O_rows, double *LSE_rows) {
+    if (check_shape(B, Hq, Hkv, N, d) || nrows < 0) return 1;
+    const int G = Hq / Hkv;
+    const i64 nd = (i64)N * d;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * N);
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < nrows; ++r) {
+            const i64 idx = rows[r];
+            if (!p || idx < 0 || idx >= (i64)B * Hq * N) { bad = 1; continue; }
+            const i64 bh = idx / N, i = idx % N;
+            const i64 b = bh / Hq, hq = bh % Hq, hk = hq / G;
+            const double *k = K + (b * Hkv + hk) * nd, *v = V + (b * Hkv + hk) * nd;
+            LSE_rows[r] = softmax_row(Q + bh * nd + i * d, k, v, i, N, d, causal, scale, p,
+                                      O_rows + (i64)r * d);
+        }
+        free(p);
+    }
+    return bad;
+}
+
+/* Sampled dQ rows (same row encoding as oracle_forward_rows). dQ_rows is [nrows, d]. */
+int oracle_backward_dq_rows(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
+                            const double *Q, const double *K, const double *V, const double *dO,
+                            int nrows, const i64 *rows, double *dQ_rows) {
+    if (check_shape(B, Hq, Hkv, N, d) || nrows < 0) return 1;
+    const int G = Hq / Hkv;
+    const i64 nd = (i64)N * d;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * N);
+        double *o = (double *)malloc(sizeof(double) * d);
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < nrows; ++r) {
+            const i64 idx = rows[r];
+            if (!p || !o || idx < 0 || idx >= (i64)B * Hq * N) { bad = 1; continue; }
+            const i64 bh = idx / N, i = idx % N;
+            const i64 b = bh / Hq, hq = bh % Hq, hk = hq / G;
+            const double *k = K + (b * Hkv + hk) * nd, *v = V + (b * Hkv + hk) * nd;
+            const double *doi = dO + bh * nd + i * d;
+            softmax_row(Q + bh * nd + i * d, k, v, i, N, d, causal, scale, p, o);
+            const double Di = dot(doi, o, d);
+            double *dq = dQ_rows + (i64)r * d;
+            for (int c = 0; c < d; ++c) dq[c] = 0.0;
+            for (i64 j = 0; j < N; ++j) {
+                if (p[j] == 0.0) continue;
+                const double ds = p[j] * (dot(doi, v + j * d, d) - Di);
+                for (int c = 0; c < d; ++c) dq[c] += ds * k[j * d + c];
+            }
+            for (int c = 0; c < d; ++c) dq[c] *= scale;
+        }
+        free(p); free(o);
+    }
+    return bad;
+}
+
+/*
+ * Sampled dK / dV rows: cols[r] = (b * Hkv + hk) * N + j.  dK_rows and dV_rows are [ncols, d].
+ * First a row pass computes LSE_i and D_i for every query row of each touched KV group (one
+ * group at a time), then each key column recomputes P_ij = exp(s_ij - LSE_i) and dS_ij.
+ */
+int oracle_backward_dkv_cols(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
+                             const double *Q, const double *K, const double *V, const double *dO,
+                             int ncols, const i64 *cols, double *dK_rows, double *dV_rows) {
+    if (check_shape(B, Hq, Hkv, N, d) || ncols < 0) return 1;
+    const int G = Hq / Hkv;
+    const i64 nd = (i64)N * d;
+    for (int r = 0; r < ncols; ++r)
+        if (cols[r] < 0 || cols[r] >= (i64)B * Hkv * N) return 1;
+    double *LSE = (double *)malloc(sizeof(double) * (i64)G * N);
+    double *D = (double *)malloc(sizeof(double) * (i64)G * N);
+    char *done = (char *)calloc(ncols > 0 ? ncols : 1, 1);
+    if (!LSE || !D || !done) { free(LSE); free(D); free(done); return 2; }
+    int bad = 0;
+    for (int r0 = 0; r0 < ncols; ++r0) {
+        if (done[r0]) continue;
+        const i64 bk = cols[r0] / N, b = bk / Hkv, hk = bk % Hkv;
+        const double *k = K + bk * nd, *v = V + bk * nd;
+        /* row pass over the group's query heads: LSE_i and D_i */
+        for (int g = 0; g < G; ++g) {
+            const i64 bh = b * Hq + hk * G + g;
+#pragma omp parallel
+            {
+                double *p = (double *)malloc(sizeof(double) * N);
+                double *o = (double *)malloc(sizeof(double) * d);
+#pragma omp for schedule(dynamic, 16)
+                for (i64 i = 0; i < N; ++i) {
+                    if (!p || !o) { bad = 2; continue; }
+                    LSE[(i64)g * N + i] = softmax_row(Q + bh * nd + i * d, k, v, i, N, d, causal,
+                                                      scale, p, o);
+                    D[(i64)g * N + i] = dot(dO + bh * nd + i * d, o, d);
+                }
+                free(p); free(o);
+            }
+        }
+        /* column pass for every requested key of this group */
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int r = r0; r < ncols; ++r) {
+            if (cols[r] / N != bk) continue;
+            done[r] = 1;
+            const i64 j = cols[r] % N;
+            double *dk = dK_rows + (i64)r * d, *dv = dV_rows + (i64)r * d;
+            for (int c = 0; c < d; ++c) { dk[c] = 0.0; dv[c] = 0.0; }
+            for (int g = 0; g < G; ++g) {
+                const i64 bh = b * Hq + hk * G + g;
+                const double *q = Q + bh * nd, *dor = dO + bh * nd;
+                for (i64 i = 0; i < N; ++i) {
+                    if (!is_allowed(causal, i, j)) continue;
+                    const double lse = LSE[(i64)g * N + i];
+                    if (lse == -INFINITY) continue;
+                    const double pij = exp(scale * dot(q + i * d, k + j * d, d) - lse);
+                    const double dsij = pij * (dot(dor + i * d, v + j * d, d) - D[(i64)g * N + i]);
+                    for (int c = 0; c < d; ++c) {
+                        dv[c] += pij * dor[i * d + c];
+                        dk[c] += scale * dsij * q[i * d + c];
+                    }
+                }
+            }
+        }
+    }
+    free(LSE); free(D); free(done);
+    return bad;
+}
