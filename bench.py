@@ -1,0 +1,375 @@
+"""Benchmark: exact attention forward + backward, bf16 d=128 causal, on GB300.
+
+One step = one pass of the whole path over one batch: fa_fwd (O, LSE) then fa_bwd (dQ, dK, dV)
+on the causal B2 H32 N4096 d128 workload (seed 2).  Inputs (Q, K, V, dO, O: 5 x 67 MB) are
+larger than the 129 MB L2, so no flush is needed between steps.
+
+Printed JSON line (rank 0):
+  value     attention TFLOP/s of fwd+bwd, whole job (all ranks), device-timed with CUDA events,
+            inputs resident in HBM; FLOPs = 4 B Hq N^2 d (x2.5 for the backward, /2 for causal).
+  e2e       the same metric through the public API with pinned host buffers: every step copies
+            Q, K, V, dO host->device and O, LSE, dQ, dK, dV device->host inside the timed region.
+  roofline  the dominant launch sequence (fa_bwd) against the measured dense bf16 peak.
+  cpu_baseline  the fp64 oracle on a bounded sample (whole heads) of the same workload.
+--impl reference times the oracle itself (the reference arm) on the same metric.
+Multi-GPU (torchrun): every rank runs its own replica (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "causal_n4096"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch of the dominant launch sequence from one ncu capture, keyed by the
+# sha256 of the kernel sources it was taken on; reported as null once the sources change.
+NCU_TRAFFIC = {}
+
+
+def kernel_sources_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_89_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        rows = [[c.strip() for c in ln.split(",")] for ln in self.lines if ln]
+        buses = sorted({r[1].lower() for r in rows if len(r) > 1})
+        if self.bus_id:
+            mine = [r for r in rows if len(r) >= 10 and self.bus_id[-12:] in r[1].lower()]
+        else:
+            mine = []
+        if not mine and len(buses) == 1:
+            mine = [r for r in rows if len(r) >= 10]
+        if not mine:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "gpu not matched"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in mine if num(r[2]) is not None]
+        mx = [num(r[3]) for r in mine if num(r[3]) is not None]
+        under = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in mine for n, v in zip(names, r[6:10]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(under) if under else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(mine)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_oracle_sample(w, budget_s: float, max_heads: int, inputs=None, first_group: int = 0):
+    """Times the fp64 oracle (forward + backward of whole KV groups) on the host cores."""
+    import torch
+
+    import oracle
+    from exact_attention_89_gb300.inputs import workload_inputs
+    Q, K, V, dO = inputs if inputs is not None else workload_inputs(w)
+    G = w.Hq // w.Hkv
+    heads_done, t_total = 0, 0.0
+    while heads_done < max_heads and (t_total < budget_s or heads_done == 0):
+        b, hk = divmod((first_group + heads_done // G) % (w.B * w.Hkv), w.Hkv)
+        sl = slice(hk * G, (hk + 1) * G)
+        q = Q[b:b + 1, sl].to(torch.float64).numpy()
+        k = K[b:b + 1, hk:hk + 1].to(torch.float64).numpy()
+        v = V[b:b + 1, hk:hk + 1].to(torch.float64).numpy()
+        do = dO[b:b + 1, sl].to(torch.float64).numpy()
+        t0 = time.perf_counter()
+        oracle.forward(q, k, v, w.causal, w.scale)
+        oracle.backward(q, k, v, do, w.causal, w.scale)
+        t_total += time.perf_counter() - t0
+        heads_done += G
+    per_head = (w.flops_fwd() + w.flops_bwd()) / (w.B * w.Hq)
+    return {"value": per_head * heads_done / t_total / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d whole query head(s) of %s (B%d Hq%d Hkv%d N%d d%d causal), fp64 "
+                      "forward+backward, %.1f s" % (heads_done, w.name, w.B, w.Hq, w.Hkv, w.N,
+                                                     w.d, t_total),
+            "seconds": t_total, "heads": heads_done}
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle as it stands, on the host cores, same metric."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from exact_attention_89_gb300.inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS[WORKLOAD]
+    inputs = workload_inputs(w)
+    # one whole KV group (fwd + bwd) per step: a bounded sample of the workload
+    for i in range(args.warmup):
+        cpu_oracle_sample(w, 0.0, 1, inputs, first_group=i)
+    t = 0.0
+    heads = 0
+    for i in range(args.steps):
+        r = cpu_oracle_sample(w, 0.0, 1, inputs, first_group=i)
+        t += r["seconds"]
+        heads += r["heads"]
+    per_head = (w.flops_fwd() + w.flops_bwd()) / (w.B * w.Hq)
+    value = per_head * heads / t / 1e12
+    import oracle
+    line = {"impl": "reference", "metric": "attention TFLOP/s fwd+bwd, bf16 d=128 causal",
+            "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N,
+                       "d": w.d, "causal": w.causal, "seed": w.seed,
+                       "step": "one whole query head, forward + backward (bounded sample)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": "%d step(s) of one whole head each" % args.steps},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for cpu_baseline (0 disables)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import torch
+    import torch.distributed as dist
+
+    from exact_attention_89_gb300 import build as fbuild
+    from exact_attention_89_gb300 import flashattn as fa
+    from exact_attention_89_gb300.inputs import WORKLOADS, workload_inputs
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if not os.path.exists(fa.LIB_PATH):
+        if rank == 0:
+            fbuild.build()
+        if ws > 1:
+            dist.barrier()
+    fa.lib()
+
+    w = WORKLOADS[args.workload]
+    Qh, Kh, Vh, dOh = workload_inputs(w, seed_offset=rank)
+    q, k, v, do = (t.to(dev) for t in (Qh, Kh, Vh, dOh))
+    B, Hq, Hkv, N, d = w.B, w.Hq, w.Hkv, w.N, w.d
+    O = torch.empty_like(q)
+    LSE = torch.empty(B, Hq, N, dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsp = torch.empty(fa.fa_bwd_workspace_bytes(B, Hq, N, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
+        if w.backward:
+            fa.fa_bwd(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsp)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = fa.fa_get_device_status()
+    if st != fa.FA_OK:
+        raise RuntimeError("device status after warm-up: " + fa.fa_status_string(st))
+
+    # ---------------------------------------------------------------- device-timed region
+    bus = None
+    try:
+        bus = getattr(torch.cuda.get_device_properties(dev), "pci_bus_id", None)
+    except Exception:
+        bus = None
+    sampler = ClockSampler(str(bus) if bus is not None else None)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
+        e1.record(stream)
+        if w.backward:
+            fa.fa_bwd(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsp)
+        e2.record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    st = fa.fa_get_device_status()
+    if st != fa.FA_OK:
+        raise RuntimeError("device status after timed region: " + fa.fa_status_string(st))
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / args.steps
+    bwd_ms = sum(b.elapsed_time(c) for _, b, c in ev) / args.steps
+    t_max = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    total_ms = float(t_max.item())
+
+    flops_step = w.flops_fwd() + (w.flops_bwd() if w.backward else 0.0)
+    value = ws * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---------------------------------------------------------------- end to end (host buffers)
+    pin = [t.pin_memory() for t in (Qh, Kh, Vh, dOh)]
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (O, LSE, dQ, dK, dV)]
+    h2d = sum(t.numel() * t.element_size() for t in pin)
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+
+    def e2e_step():
+        qd, kd, vd, dod = (t.to(dev, non_blocking=True) for t in pin)
+        Od, Ld = fa.attention_forward(qd, kd, vd, w.causal, w.scale)
+        gq, gk, gv = fa.attention_backward(qd, kd, vd, Od, dod, Ld, w.causal, w.scale, workspace=wsp)
+        for hbuf, dbuf in zip(outs_h, (Od, Ld, gq, gk, gv)):
+            hbuf.copy_(dbuf, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e_s = torch.cuda.Event(enable_timing=True)
+    e_e = torch.cuda.Event(enable_timing=True)
+    e_s.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_e.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_s.elapsed_time(e_e)
+    t2 = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(t2, op=dist.ReduceOp.MAX)
+    e2e_ms = float(t2.item())
+    e2e_value = ws * flops_step * args.steps / (e2e_ms * 1e-3) / 1e12
+
+    # ---------------------------------------------------------------- roofline + cpu baseline
+    peaks, peaks_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    src_hash = kernel_sources_hash()
+    bwd_achieved = w.flops_bwd() / (bwd_ms * 1e-3) / 1e12 if w.backward else None
+    fwd_achieved = w.flops_fwd() / (fwd_ms * 1e-3) / 1e12
+    traffic = NCU_TRAFFIC.get(src_hash)
+    roofline = {"bound": "tensor", "kernel": "fa_bwd (bwd_main + preprocess + dq_convert)",
+                "achieved": bwd_achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": bwd_achieved / peak if bwd_achieved else None,
+                "traffic": traffic, "peak_source": "%s burst bf16 (MEASURED_PEAKS.json)" % peaks_src
+                if peaks_src == "measured" else "fallback 1.9 PFLOP/s bf16",
+                "flops_per_launch": w.flops_bwd(),
+                "fwd": {"kernel": "fa_fwd", "achieved": fwd_achieved,
+                        "frac": fwd_achieved / peak, "ms": fwd_ms,
+                        "flops_per_launch": w.flops_fwd()},
+                "bwd_ms": bwd_ms, "sources": src_hash}
+    cpu = None
+    if rank == 0 and ws == 1 and args.cpu_budget > 0:
+        r = cpu_oracle_sample(w, args.cpu_budget, 8)
+        cpu = {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank == 0:
+        line = {"metric": "attention TFLOP/s fwd+bwd, bf16 d=128 causal", "value": value,
+                "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
+                           "causal": w.causal, "seed": w.seed, "scale": w.scale,
+                           "l2": "inputs larger than L2 (Q,K,V,dO,O = 5 x %.0f MB), no flush"
+                                 % (q.numel() * 2 / 1e6),
+                           "parallelism": "replicas x%d" % ws},
+                "fwd_tflops": w.flops_fwd() / (fwd_ms * 1e-3) / 1e12,
+                "fwd_frac_of_peak": fwd_achieved / peak,
+                "fwd_bwd_frac_of_peak": value / ws / peak,
+                "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+                "gpu_launches": args.steps * (1 + (3 if w.backward else 0)),
+                "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks}
+        print(json.dumps(line))
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,231 @@
+// fa_api.cu -- the C ABI of libflashattn (declared in include/flashattn.h).
+//
+// Host-side validation, TMA tensor-map encoding, the per-device status word and the launch
+// sequence of each entry point.  No device memory is allocated here: the status word is a
+// static __device__ variable, every tensor and the backward workspace belong to the caller.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "flashattn.h"
+
+namespace fa {
+
+__device__ unsigned g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool probed = false;
+    bool sm103 = false;
+    unsigned *status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Current device's entry, probed once.  Returns FA_OK or the reason it cannot run.
+fa_status current_device(DeviceInfo **out, bool need_sm103) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &di = g_dev[dev];
+    if (!di.probed) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return FA_ERR_CUDA;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return FA_ERR_CUDA;
+        di.status = static_cast<unsigned *>(p);
+        di.sm103 = (major == 10 && minor == 3);
+        di.probed = true;
+    }
+    if (need_sm103 && !di.sm103) return FA_ERR_UNSUPPORTED;
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return FA_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    *out = &di;
+    return FA_OK;
+}
+
+bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    // index arithmetic is 64-bit; keep the TMA coordinate ranges (int32) and grid sizes sane
+    if (static_cast<long long>(B) * Hq > (1LL << 31) - 1) return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// 3-D bf16 view [d, N, BH] of a contiguous [BH, N, d] tensor, box [64, rows, 1], 128B swizzle.
+bool encode_bf16(CUtensorMap *m, const void *base, int d, int N, long long BH, int box_rows) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace fa
+
+using fa::Problem;
+
+extern "C" {
+
+const char *fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+        case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+        case FA_ERR_DEVICE_BOUNDS: return "FA_ERR_DEVICE_BOUNDS";
+    }
+    return "FA_ERR_UNKNOWN";
+}
+
+size_t fa_bwd_workspace_bytes(int B, int Hq, int N, int d) {
+    if (B < 1 || Hq < 1 || N < 1 || d < 1) return 0;
+    const size_t rows = static_cast<size_t>(B) * Hq * N;
+    return fa::align256(rows * sizeof(float)) + rows * d * sizeof(float);
+}
+
+fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int Hq,
+                 int Hkv, int N, int d, int causal, float scale, cudaStream_t stream) {
+    fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!fa::aligned16(Q) || !fa::aligned16(K) || !fa::aligned16(V) || !fa::aligned16(O) ||
+        !fa::aligned16(LSE))
+        return FA_ERR_MISALIGNED;
+    fa::DeviceInfo *di = nullptr;
+    if ((st = fa::current_device(&di, true)) != FA_OK) return st;
+    const Problem p{B, Hq, Hkv, N, d, causal ? 1 : 0, scale};
+    CUtensorMap tq, tk, tv, to;
+    if (!fa::encode_bf16(&tq, Q, d, N, 1LL * B * Hq, 128) ||
+        !fa::encode_bf16(&tk, K, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tv, V, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&to, O, d, N, 1LL * B * Hq, 128))
+        return FA_ERR_CUDA;
+    return fa::from_cuda(fa::launch_fwd_bf16(p, tq, tk, tv, to, LSE, di->status, stream));
+}
+
+fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                 const float *LSE, void *dQ, void *dK, void *dV, int B, int Hq, int Hkv, int N,
+                 int d, int causal, float scale, void *workspace, size_t workspace_bytes,
+                 cudaStream_t stream) {
+    fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (!fa::aligned16(Q) || !fa::aligned16(K) || !fa::aligned16(V) || !fa::aligned16(O) ||
+        !fa::aligned16(dO) || !fa::aligned16(LSE) || !fa::aligned16(dQ) || !fa::aligned16(dK) ||
+        !fa::aligned16(dV))
+        return FA_ERR_MISALIGNED;
+    if (!fa::aligned16(workspace) || workspace_bytes < fa_bwd_workspace_bytes(B, Hq, N, d))
+        return FA_ERR_WORKSPACE;
+    fa::DeviceInfo *di = nullptr;
+    if ((st = fa::current_device(&di, true)) != FA_OK) return st;
+    const Problem p{B, Hq, Hkv, N, d, causal ? 1 : 0, scale};
+    const size_t rows = static_cast<size_t>(B) * Hq * N;
+    float *Dvec = static_cast<float *>(workspace);
+    float *dQacc = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                             fa::align256(rows * sizeof(float)));
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+    if (!fa::encode_bf16(&tq, Q, d, N, 1LL * B * Hq, 64) ||
+        !fa::encode_bf16(&tk, K, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tv, V, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tdo, dO, d, N, 1LL * B * Hq, 64) ||
+        !fa::encode_bf16(&tdk, dK, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tdv, dV, d, N, 1LL * B * Hkv, 128))
+        return FA_ERR_CUDA;
+    cudaError_t e = fa::launch_bwd_preprocess_bf16(p, O, dO, Dvec, dQacc, stream);
+    if (e == cudaSuccess)
+        e = fa::launch_bwd_main_bf16(p, tq, tk, tv, tdo, tdk, tdv, LSE, Dvec, dQacc, di->status, stream);
+    if (e == cudaSuccess) e = fa::launch_bwd_dq_convert_bf16(p, dQacc, dQ, stream);
+    return fa::from_cuda(e);
+}
+
+fa_status fa_fwd_fp32(const float *Q, const float *K, const float *V, float *O, float *LSE, int B,
+                      int Hq, int Hkv, int N, int d, int causal, float scale, cudaStream_t stream) {
+    fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (d > 128) return FA_ERR_UNSUPPORTED;
+    if (!fa::aligned16(Q) || !fa::aligned16(K) || !fa::aligned16(V) || !fa::aligned16(O) ||
+        !fa::aligned16(LSE))
+        return FA_ERR_MISALIGNED;
+    fa::DeviceInfo *di = nullptr;
+    if ((st = fa::current_device(&di, true)) != FA_OK) return st;
+    const Problem p{B, Hq, Hkv, N, d, causal ? 1 : 0, scale};
+    return fa::from_cuda(fa::launch_fwd_fp32(p, Q, K, V, O, LSE, stream));
+}
+
+fa_status fa_bwd_fp32(const float *Q, const float *K, const float *V, const float *O,
+                      const float *dO, const float *LSE, float *dQ, float *dK, float *dV, int B,
+                      int Hq, int Hkv, int N, int d, int causal, float scale, void *workspace,
+                      size_t workspace_bytes, cudaStream_t stream) {
+    fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (d > 128) return FA_ERR_UNSUPPORTED;
+    if (!fa::aligned16(Q) || !fa::aligned16(K) || !fa::aligned16(V) || !fa::aligned16(O) ||
+        !fa::aligned16(dO) || !fa::aligned16(LSE) || !fa::aligned16(dQ) || !fa::aligned16(dK) ||
+        !fa::aligned16(dV))
+        return FA_ERR_MISALIGNED;
+    if (!fa::aligned16(workspace) || workspace_bytes < fa_bwd_workspace_bytes(B, Hq, N, d))
+        return FA_ERR_WORKSPACE;
+    fa::DeviceInfo *di = nullptr;
+    if ((st = fa::current_device(&di, true)) != FA_OK) return st;
+    const Problem p{B, Hq, Hkv, N, d, causal ? 1 : 0, scale};
+    return fa::from_cuda(fa::launch_bwd_fp32(p, Q, K, V, O, dO, LSE, dQ, dK, dV,
+                                             static_cast<float *>(workspace), stream));
+}
+
+fa_status fa_get_device_status(cudaStream_t stream) {
+    fa::DeviceInfo *di = nullptr;
+    fa_status st = fa::current_device(&di, false);
+    if (st != FA_OK) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpyFromSymbol(&word, fa::g_status_word, sizeof(word)) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (word != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(fa::g_status_word, &zero, sizeof(zero)) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    return static_cast<fa_status>(word);
+}
+
+}  // extern "C"

@@ -1,0 +1,474 @@
+// fa_bwd_sm103a.cu -- K2 / K3 / K4: exact attention backward, bf16 in / fp32 accumulate, sm_103a.
+//
+// Method ("Attention's hidden recurrence" blog by mzeromiko, sections "standard attention /
+// backward" and "Flash Attention backward"): nothing of P is stored by the forward pass; P is
+// recomputed per tile from the stored statistics (here LSE = m + ln l, so P = exp(s - LSE)), and
+//   D_i = diag(dO O^T)_i = sum_k dO_ik O_ik,   dS = P * (dP - D),  dP = dO V^T,
+//   dV = P^T dO,   dK = scale dS^T Q,   dQ = scale dS K.
+// (The blog's d(exp(QK^T) (.) M) (.) exp(QK^T) equals dS; scale enters by the chain rule.)
+//
+// K2 forms D and clears the fp32 dQ accumulator.  K3 gives each CTA one 128-key block of one
+// (batch, KV head); it loops over the G query heads of the group and over 64-row query tiles
+// (under causal masking only tiles at or below the block's diagonal), so dK and dV of the block
+// accumulate in TMEM across the whole group and need no atomics.  Per query tile:
+//   S^T = K Q^T and dP^T = V dO^T        (SS MMAs, M = 128 keys, N = 64 queries, K = d)
+//   P^T = exp2(S^T c - LSE log2 e), dS^T = P^T (dP^T - D)   (thread = key row = TMEM lane)
+//   dV += P^T dO,  dK += dS^T Q          (TS MMAs: P^T / dS^T as bf16 in TMEM, over S^T / dP^T)
+//   dQ^T = K^T dS^T                      (SS MMA, M = d = 128, dS^T staged in smem)
+// and a second warpgroup reduces scale * dQ^T into the fp32 accumulator with coalesced
+// fp32 reductions (thread = one column d of dQ).  K4 rounds the accumulator to bf16.
+// dQ strategy: recomputing S and dP in a separate dQ kernel would cost 7 products per tile
+// instead of 5 (+40% tensor work); the reduction costs L2 bandwidth instead.
+//
+// Roles (320 threads): warps 0-3 softmax-gradient, warps 4-7 dQ drain, warp 8 TMA, warp 9 MMA.
+// TMEM (512 columns): dK [0,128), dV [128,256), S^T/P^T [256,320), dP^T/dS^T [320,384),
+// dQ^T [384,448).
+#include <cmath>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace bwd {
+
+constexpr int BKV = 128;          // keys per CTA (= TMEM lanes)
+constexpr int BQ = 64;            // query rows per step
+constexpr int NSQ = 2;            // Q / dO ring stages
+constexpr int NUM_THREADS = 320;
+constexpr int WARP_TMA = 8;
+constexpr int WARP_MMA = 9;
+constexpr float LOG2E = 1.4426950408889634f;
+
+template <int D>
+struct Layout {
+    static constexpr int KV_BYTES = BKV * D * 2;          // K or V block
+    static constexpr int KV_CHUNK = BKV * 128;            // 128 rows x 64 bf16
+    static constexpr int Q_BYTES = BQ * D * 2;            // Q or dO tile
+    static constexpr int Q_CHUNK = BQ * 128;              // 64 rows x 64 bf16
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = K_OFF + KV_BYTES;
+    static constexpr int QR_OFF = V_OFF + KV_BYTES;        // ring: [stage][Q | dO]
+    static constexpr int DS_OFF = QR_OFF + NSQ * 2 * Q_BYTES;  // dS^T: 128 rows x 64 bf16
+    static constexpr int STAT_OFF = DS_OFF + BKV * 128;     // [2 buffers][lse2 64 | D 64] fp32
+    static constexpr int BAR_OFF = STAT_OFF + 2 * 2 * BQ * 4;
+    // kv_full, q_full[NSQ], q_empty[NSQ], s_full, p_full, dq_full, dq_empty, acc_full, epi, mma_done
+    static constexpr int NBARS = 1 + 2 * NSQ + 7;
+    static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int ABORT_OFF = TMEM_OFF + 8;
+    static constexpr int BYTES = ABORT_OFF + 8 + 1024;
+};
+
+constexpr uint32_t T_DK = 0, T_DV = 128, T_ST = 256, T_DPT = 320, T_DQT = 384;
+
+template <bool CAUSAL>
+__device__ __forceinline__ int first_q_tile(int jb) {
+    return CAUSAL ? (jb * BKV) / BQ : 0;
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                    const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                    const float *__restrict__ LSE, const float *__restrict__ Dvec,
+                    float *__restrict__ dQacc, int Hq, int Hkv, int N, int BHkv, float scale,
+                    float scale_log2, unsigned *status) {
+    static_assert(D == 128, "the bf16 backward main loop is laid out for d = 128");
+    using L = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
+    uint64_t *kv_full = bars;
+    uint64_t *q_full = bars + 1;
+    uint64_t *q_empty = q_full + NSQ;
+    uint64_t *s_full = q_empty + NSQ;
+    uint64_t *p_full = s_full + 1;
+    uint64_t *dq_full = p_full + 1;
+    uint64_t *dq_empty = dq_full + 1;
+    uint64_t *acc_full = dq_empty + 1;
+    uint64_t *epi = acc_full + 1;
+    uint64_t *mma_done = epi + 1;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::TMEM_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ABORT_OFF);
+    float *stat = reinterpret_cast<float *>(smem + L::STAT_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = Hq / Hkv;
+    const int bkv = blockIdx.x % BHkv;          // b * Hkv + hk
+    const int jb = blockIdx.x / BHkv;           // key block; small jb (most work) first
+    const int b = bkv / Hkv, hk = bkv % Hkv;
+    const int nq = (N + BQ - 1) / BQ;
+    const int i0 = first_q_tile<CAUSAL>(jb);
+    const int tiles_per_head = nq - i0;
+    const int T = G * tiles_per_head;           // steps of this CTA
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        for (int s = 0; s < NSQ; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&q_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 128);
+        mbar_init(dq_full, 1);
+        mbar_init(dq_empty, 128);
+        mbar_init(acc_full, 1);
+        mbar_init(epi, 128);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == WARP_MMA) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == WARP_TMA) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(kv_full, 2 * L::KV_BYTES);
+            for (int ch = 0; ch < D / 64; ++ch) {
+                tma_load_3d(smem + L::K_OFF + ch * L::KV_CHUNK, &tmK, ch * 64, jb * BKV, bkv, kv_full);
+                tma_load_3d(smem + L::V_OFF + ch * L::KV_CHUNK, &tmV, ch * 64, jb * BKV, bkv, kv_full);
+            }
+            int issued = 0;
+            for (int s = 0; s < T; ++s) {
+                const int st = s % NSQ, rnd = s / NSQ;
+                if (!mbar_wait(&q_empty[st], (rnd & 1) ^ 1, abort_flag, status)) break;
+                const int g = s / tiles_per_head, i = i0 + s % tiles_per_head;
+                const int bhq = b * Hq + hk * G + g;
+                mbar_arrive_expect_tx(&q_full[st], 2 * L::Q_BYTES);
+                uint8_t *qdst = smem + L::QR_OFF + st * 2 * L::Q_BYTES;
+                for (int ch = 0; ch < D / 64; ++ch) {
+                    tma_load_3d(qdst + ch * L::Q_CHUNK, &tmQ, ch * 64, i * BQ, bhq, &q_full[st]);
+                    tma_load_3d(qdst + L::Q_BYTES + ch * L::Q_CHUNK, &tmdO, ch * 64, i * BQ, bhq,
+                                &q_full[st]);
+                }
+                ++issued;
+            }
+            if (*abort_flag) {
+                for (int s = max(0, issued - NSQ); s < issued; ++s)
+                    mbar_drain(&q_full[s % NSQ], (s / NSQ) & 1);
+                mbar_drain(kv_full, 0);
+            }
+        }
+    } else if (warp == WARP_MMA) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_SP = idesc_bf16(BKV, BQ, false, false);   // S^T, dP^T
+            constexpr uint32_t IDESC_KV = idesc_bf16(BKV, D, false, true);     // dV, dK
+            constexpr uint32_t IDESC_DQ = idesc_bf16(D, BQ, true, true);       // dQ^T
+            const uint32_t k_base = smem_u32(smem + L::K_OFF);
+            const uint32_t v_base = smem_u32(smem + L::V_OFF);
+            const uint32_t ds_base = smem_u32(smem + L::DS_OFF);
+            bool ok = mbar_wait(kv_full, 0, abort_flag, status);
+            tc_fence_after();
+            for (int s = 0; s < T && ok; ++s) {
+                const int st = s % NSQ;
+                const uint32_t q_base = smem_u32(smem + L::QR_OFF + st * 2 * L::Q_BYTES);
+                const uint32_t do_base = q_base + L::Q_BYTES;
+                if (!mbar_wait(&q_full[st], (s / NSQ) & 1, abort_flag, status)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
+                    const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
+                    mma_ss(tmem + T_ST, sdesc_sw128(k_base + oa, 16, 1024),
+                           sdesc_sw128(q_base + ob, 16, 1024), IDESC_SP, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
+                    const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
+                    mma_ss(tmem + T_DPT, sdesc_sw128(v_base + oa, 16, 1024),
+                           sdesc_sw128(do_base + ob, 16, 1024), IDESC_SP, kk > 0);
+                }
+                mma_commit(s_full);
+                if (!mbar_wait(p_full, s & 1, abort_flag, status)) break;
+                tc_fence_after();
+                // dV += P^T dO ; dK += dS^T Q   (B operands MN-major: d contiguous)
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk)
+                    mma_ts(tmem + T_DV, tmem + T_ST + kk * 8,
+                           sdesc_sw128(do_base + kk * 2048, L::Q_CHUNK, 1024), IDESC_KV,
+                           (s > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk)
+                    mma_ts(tmem + T_DK, tmem + T_DPT + kk * 8,
+                           sdesc_sw128(q_base + kk * 2048, L::Q_CHUNK, 1024), IDESC_KV,
+                           (s > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&q_empty[st]);
+                // dQ^T = K^T dS^T  (A = K MN-major, B = dS^T MN-major, K dim = 128 keys)
+                if (!mbar_wait(dq_empty, (s & 1) ^ 1, abort_flag, status)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BKV / 16; ++kk)
+                    mma_ss(tmem + T_DQT, sdesc_sw128(k_base + kk * 2048, L::KV_CHUNK, 1024),
+                           sdesc_sw128(ds_base + kk * 2048, BKV * 128, 1024), IDESC_DQ, kk > 0);
+                mma_commit(dq_full);
+            }
+            mma_commit(acc_full);
+            mma_commit(mma_done);
+            mbar_drain(mma_done, 0);
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------------------------ P^T / dS^T warps
+        const int krow = warp * 32 + lane;          // key row within the block = TMEM lane
+        const int key = jb * BKV + krow;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        uint8_t *ds_row = smem + L::DS_OFF + krow * 128;
+        bool ok = true;
+        for (int s = 0; s < T; ++s) {
+            const int g = s / tiles_per_head, i = i0 + s % tiles_per_head;
+            const int bhq = b * Hq + hk * G + g;
+            const int q0 = i * BQ;
+            float *buf = stat + (s & 1) * 2 * BQ;
+            // statistics of this query tile: thread t < 64 loads LSE_t, t >= 64 loads D_{t-64};
+            // the global loads are in flight while the thread waits for the MMAs.
+            float v;
+            {
+                const int q = q0 + (krow & (BQ - 1));
+                if (krow < BQ)
+                    v = (q < N) ? LSE[static_cast<size_t>(bhq) * N + q] * LOG2E : INFINITY;
+                else
+                    v = (q < N) ? Dvec[static_cast<size_t>(bhq) * N + q] : 0.f;
+            }
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full, s & 1, abort_flag, status));
+            buf[krow] = v;
+            // executed by all four warps every step (even after a failed wait) so the counts match
+            named_barrier_sync(1, 128);
+            if (ok) {
+                tc_fence_after();
+                uint32_t sr[64], dr[64];
+                tmem_ld_x64(tmem + lane_off + T_ST, sr);
+                tmem_ld_x64(tmem + lane_off + T_DPT, dr);
+                const bool need_mask = (CAUSAL && q0 < jb * BKV + BKV) || (q0 + BQ > N) ||
+                                       (jb * BKV + BKV > N);
+                uint32_t pp[32], dd[32];
+#pragma unroll
+                for (int c = 0; c < BQ; c += 2) {
+                    float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, -buf[c]));
+                    float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), scale_log2, -buf[c + 1]));
+                    if (need_mask) {
+                        const int q = q0 + c;
+                        if ((CAUSAL && key > q) || q >= N || key >= N) p0 = 0.f;
+                        if ((CAUSAL && key > q + 1) || q + 1 >= N || key >= N) p1 = 0.f;
+                    }
+                    const float d0 = p0 * (__uint_as_float(dr[c]) - buf[BQ + c]);
+                    const float d1 = p1 * (__uint_as_float(dr[c + 1]) - buf[BQ + c + 1]);
+                    pp[c >> 1] = pack_bf16x2(p0, p1);
+                    dd[c >> 1] = pack_bf16x2(d0, d1);
+                }
+                tmem_st_x32(tmem + lane_off + T_ST, pp);
+                tmem_st_x32(tmem + lane_off + T_DPT, dd);
+                // dS^T row -> smem (128B-swizzled, MN-major B operand of the dQ^T product)
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    uint4 v = make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+                    *reinterpret_cast<uint4 *>(ds_row + ((u ^ (krow & 7)) << 4)) = v;
+                }
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(p_full);
+            }
+        }
+        // epilogue: dK (scaled) and dV rows -> bf16 -> smem (over K / V) -> TMA store
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, status));
+        if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t tcol = which ? T_DV : T_DK;
+                const float mul = which ? 1.f : scale;
+                uint8_t *dst = smem + (which ? L::V_OFF : L::K_OFF);
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t a[32];
+                    tmem_ld_x32(tmem + lane_off + tcol + c0, a);
+                    uint8_t *rowp = dst + (c0 / 64) * L::KV_CHUNK + krow * 128;
+                    const int u0 = (c0 % 64) / 8;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(a[8 * u + 0]) * mul, __uint_as_float(a[8 * u + 1]) * mul);
+                        v.y = pack_bf16x2(__uint_as_float(a[8 * u + 2]) * mul, __uint_as_float(a[8 * u + 3]) * mul);
+                        v.z = pack_bf16x2(__uint_as_float(a[8 * u + 4]) * mul, __uint_as_float(a[8 * u + 5]) * mul);
+                        v.w = pack_bf16x2(__uint_as_float(a[8 * u + 6]) * mul, __uint_as_float(a[8 * u + 7]) * mul);
+                        *reinterpret_cast<uint4 *>(rowp + (((u0 + u) ^ (krow & 7)) << 4)) = v;
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(epi);
+            if (krow == 0 && mbar_wait(epi, 0, abort_flag, status)) {
+                for (int ch = 0; ch < D / 64; ++ch) {
+                    tma_store_3d(&tmdK, smem + L::K_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
+                    tma_store_3d(&tmdV, smem + L::V_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
+                }
+                tma_store_commit_and_wait_read();
+            }
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------------------ dQ drain warps
+        const int wq = warp - 4;
+        const int dcol = wq * 32 + lane;            // column of dQ = TMEM lane of dQ^T
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        for (int s = 0; s < T; ++s) {
+            const int g = s / tiles_per_head, i = i0 + s % tiles_per_head;
+            const int bhq = b * Hq + hk * G + g;
+            const int q0 = i * BQ;
+            if (!__all_sync(0xffffffffu, mbar_wait(dq_full, s & 1, abort_flag, status))) break;
+            tc_fence_after();
+            uint32_t a[64];
+            tmem_ld_x64(tmem + lane_off + T_DQT, a);
+            tc_fence_before();
+            mbar_arrive(dq_empty);
+            float *dst = dQacc + (static_cast<size_t>(bhq) * N + q0) * D + dcol;
+            const int nvalid = min(BQ, N - q0);
+#pragma unroll
+            for (int c = 0; c < BQ; ++c)
+                if (c < nvalid) atomicAdd(dst + static_cast<size_t>(c) * D, __uint_as_float(a[c]) * scale);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// K2: D[row] = sum_k dO[row,k] O[row,k] (fp32) and dQacc = 0.  HBM-bound: one 16-byte vector
+// per lane per tensor, 8 bf16 each.
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16 *__restrict__ O,
+                                                             const __nv_bfloat16 *__restrict__ dO,
+                                                             float *__restrict__ Dvec,
+                                                             float4 *__restrict__ dQacc,
+                                                             long long rows, int d,
+                                                             long long acc_vec4) {
+    const int lanes_per_row = d / 8;                 // 16 (d = 128) or 8 (d = 64)
+    const int rows_per_warp = 32 / lanes_per_row;
+    const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+    const int lane = threadIdx.x & 31, sub = lane % lanes_per_row;
+    const long long warp_id = tid >> 5, nwarps = nthreads >> 5;
+    // each group of lanes_per_row lanes owns one row; the loop is uniform across the warp
+    for (long long wb = warp_id * rows_per_warp; wb < rows; wb += nwarps * rows_per_warp) {
+        const long long row = wb + lane / lanes_per_row;
+        float acc = 0.f;
+        if (row < rows) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(O + row * d + sub * 8);
+            const uint4 c = *reinterpret_cast<const uint4 *>(dO + row * d + sub * 8);
+            const __nv_bfloat162 *ah = reinterpret_cast<const __nv_bfloat162 *>(&a);
+            const __nv_bfloat162 *ch = reinterpret_cast<const __nv_bfloat162 *>(&c);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 x = __bfloat1622float2(ah[k]);
+                const float2 y = __bfloat1622float2(ch[k]);
+                acc = fmaf(x.x, y.x, acc);
+                acc = fmaf(x.y, y.y, acc);
+            }
+        }
+        for (int off = lanes_per_row / 2; off > 0; off >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, off, lanes_per_row);
+        if (sub == 0 && row < rows) Dvec[row] = acc;
+    }
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long k = tid; k < acc_vec4; k += nthreads) dQacc[k] = z;
+}
+
+// K4: dQ = bf16(dQacc), 8 elements per thread per step.
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4 *__restrict__ acc,
+                                                             uint4 *__restrict__ out,
+                                                             long long n8) {
+    const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long k = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; k < n8;
+         k += nthreads) {
+        const float4 a = acc[2 * k], c = acc[2 * k + 1];
+        uint4 v;
+        v.x = pack_bf16x2(a.x, a.y);
+        v.y = pack_bf16x2(a.z, a.w);
+        v.z = pack_bf16x2(c.x, c.y);
+        v.w = pack_bf16x2(c.z, c.w);
+        out[k] = v;
+    }
+}
+
+static int grid_for(long long work, int per_block, int num_sms) {
+    long long g = (work + per_block - 1) / per_block;
+    const long long cap = static_cast<long long>(num_sms) * 8;
+    if (g > cap) g = cap;
+    if (g < 1) g = 1;
+    return static_cast<int>(g);
+}
+
+static int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+    return n;
+}
+
+}  // namespace bwd
+
+cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const void *dO, float *D,
+                                       float *dQacc, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(p.B) * p.Hq * p.N;
+    const long long acc4 = rows * p.d / 4;
+    const int sms = bwd::sm_count();
+    const int grid = bwd::grid_for(rows * (p.d / 8), 256, sms);
+    bwd::bwd_preprocess_kernel<<<grid, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), D,
+        reinterpret_cast<float4 *>(dQacc), rows, p.d, acc4);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                                 const CUtensorMap &tmV, const CUtensorMap &tmdO,
+                                 const CUtensorMap &tmdK, const CUtensorMap &tmdV,
+                                 const float *LSE, const float *D, float *dQacc, unsigned *status,
+                                 cudaStream_t stream) {
+    if (p.d != 128) return cudaErrorInvalidValue;
+    const int BHkv = p.B * p.Hkv;
+    const long long nkb = (p.N + bwd::BKV - 1) / bwd::BKV;
+    const long long grid = nkb * BHkv;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int smem = bwd::Layout<128>::BYTES;
+    const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+    cudaError_t e;
+    if (p.causal) {
+        auto kern = bwd::bwd_main_kernel<128, true>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        kern<<<static_cast<unsigned>(grid), bwd::NUM_THREADS, smem, stream>>>(
+            tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, p.scale,
+            scale_log2, status);
+    } else {
+        auto kern = bwd::bwd_main_kernel<128, false>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        kern<<<static_cast<unsigned>(grid), bwd::NUM_THREADS, smem, stream>>>(
+            tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, p.scale,
+            scale_log2, status);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_convert_bf16(const Problem &p, const float *dQacc, void *dQ,
+                                       cudaStream_t stream) {
+    const long long n8 = static_cast<long long>(p.B) * p.Hq * p.N * p.d / 8;
+    const int grid = bwd::grid_for(n8, 256, bwd::sm_count());
+    bwd::bwd_dq_convert_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4 *>(dQacc),
+                                                         static_cast<uint4 *>(dQ), n8);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,373 @@
+// fa_fwd_sm103a.cu -- K1: exact attention forward, bf16 in / fp32 accumulate, sm_103a.
+//
+// Method (FlashAttention DAC'24 reading note, paper.adslab.icu, Methods): a query tile stays in
+// on-chip memory while key/value blocks stream past it; per block the running row max m and
+// running sum l are rescaled, l' = e^{m-m'} l + e^{m~-m'} l~, and the output accumulator is
+// rescaled the same way.  Normalisation is deferred to the end (FlashAttention note,
+// paweldubiel.com: keep u = sum e^{s-m} v and return u / l), which equals the per-step form of
+// the reading note's O update in exact arithmetic.  The mask acts on each block's scores
+// (reading note, "other operators"), here only on blocks that cross the diagonal or the end of
+// the sequence.  LSE = m + ln l is stored for the backward pass (mzeromiko blog, end of the
+// "blocked form with online-softmax rescaling" section: logsumexp placement).
+//
+// GB300 mapping (one CTA = two 128-row query tiles of one (batch, head), 320 threads):
+//   warps 0-3 : softmax for query tile 0  (thread = query row = TMEM lane)
+//   warps 4-7 : softmax for query tile 1
+//   warp 8    : TMA producer (Q tiles once, then K_j / V_j through a 4-stage ring)
+//   warp 9    : TMEM allocator and single-thread tcgen05.mma issuer
+// TMEM (512 columns): S/P of tile t at columns 128 t, O of tile t at 256 + 128 t.
+// S = Q K_j^T runs as SS MMAs (both operands K-major in 128B-swizzled smem); P is written back
+// over S as packed bf16 and O += P V_j runs as a TS MMA (P from TMEM, V MN-major in smem).
+// The MMA order S0(j+1) after PV0(j) lets softmax of one tile overlap the other tile's MMAs.
+// Rescaling of O is lazy: the stale max is kept until the block max exceeds it by 8 (log2
+// units), so p <= 2^8; the shift cancels in O = u / l, so the result is unchanged.
+#include <cmath>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace fwd {
+
+constexpr int BM = 128;           // query rows per tile (= TMEM lanes)
+constexpr int BN = 128;           // keys per block
+constexpr int NS = 4;             // K/V ring stages
+constexpr int NUM_THREADS = 320;
+constexpr int WARP_TMA = 8;
+constexpr int WARP_MMA = 9;
+constexpr float RESCALE_THRESHOLD = 8.0f;
+constexpr float LN2 = 0.693147180559945309f;
+
+template <int D>
+struct Layout {
+    static constexpr int TILE_BYTES = 128 * D * 2;   // one Q tile or one K/V block, bf16
+    static constexpr int CHUNK_BYTES = 128 * 128;    // 128 rows x 64 bf16 (one swizzle column)
+    static constexpr int Q_OFF = 0;
+    static constexpr int KV_OFF = 2 * TILE_BYTES;
+    static constexpr int BAR_OFF = KV_OFF + NS * TILE_BYTES;
+    // q_full, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_full[2], epi[2], mma_done
+    static constexpr int NBARS = 1 + 2 * NS + 2 + 2 + 2 + 2 + 1;
+    static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int ABORT_OFF = TMEM_OFF + 8;
+    static constexpr int BYTES = ABORT_OFF + 8 + 1024;   // + slack for 1024-byte alignment
+};
+
+template <int D>
+__device__ __forceinline__ void rescale_o_row(uint32_t tO, float alpha) {
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld_x32(tO + c0, o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st_x32(tO + c0, o);
+    }
+    tmem_wait_st();
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+               float *__restrict__ LSE, int Hq, int Hkv, int N, int BH, float scale_log2,
+               unsigned *status) {
+    using L = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
+    uint64_t *q_full = bars;
+    uint64_t *kv_full = bars + 1;
+    uint64_t *kv_empty = kv_full + NS;
+    uint64_t *s_full = kv_empty + NS;
+    uint64_t *p_full = s_full + 2;
+    uint64_t *o_full = p_full + 2;
+    uint64_t *epi = o_full + 2;
+    uint64_t *mma_done = epi + 2;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::TMEM_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ABORT_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // Work item: (query-tile pair, batch*head).  Under causal masking the late (heavy) pairs go
+    // first so the tail of the grid holds the short ones.
+    const int n_pairs = (N + 2 * BM - 1) / (2 * BM);
+    const int bh = blockIdx.x % BH;
+    int pair = blockIdx.x / BH;
+    if (CAUSAL) pair = n_pairs - 1 - pair;
+    const int hq = bh % Hq, b = bh / Hq;
+    const int bkv = b * Hkv + hq / (Hq / Hkv);
+    const int nkb = (N + BN - 1) / BN;
+    int q0[2], nblk[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        q0[t] = pair * 2 * BM + t * BM;
+        if (q0[t] >= N)
+            nblk[t] = 0;
+        else if (CAUSAL)
+            nblk[t] = min(nkb, (min(q0[t] + BM, N) - 1) / BN + 1);
+        else
+            nblk[t] = nkb;
+    }
+    const int nmax = max(nblk[0], nblk[1]);
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], BM);
+            mbar_init(&o_full[t], 1);
+            mbar_init(&epi[t], BM);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == WARP_MMA) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == WARP_TMA) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            const int ntiles = nblk[1] > 0 ? 2 : 1;
+            mbar_arrive_expect_tx(q_full, ntiles * L::TILE_BYTES);
+            for (int t = 0; t < ntiles; ++t)
+                for (int ch = 0; ch < D / 64; ++ch)
+                    tma_load_3d(smem + L::Q_OFF + t * L::TILE_BYTES + ch * L::CHUNK_BYTES, &tmQ,
+                                ch * 64, q0[t], bh, q_full);
+            int issued = 0;
+            bool ok = true;
+            for (int idx = 0; idx < 2 * nmax && ok; ++idx) {
+                const int j = idx >> 1, st = idx % NS, rnd = idx / NS;
+                if (!mbar_wait(&kv_empty[st], (rnd & 1) ^ 1, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&kv_full[st], L::TILE_BYTES);
+                uint8_t *dst = smem + L::KV_OFF + st * L::TILE_BYTES;
+                const CUtensorMap *tm = (idx & 1) ? &tmV : &tmK;
+                for (int ch = 0; ch < D / 64; ++ch)
+                    tma_load_3d(dst + ch * L::CHUNK_BYTES, tm, ch * 64, j * BN, bkv, &kv_full[st]);
+                ++issued;
+            }
+            if (!ok || *abort_flag) {
+                // Unwinding: let copies still in flight land before the CTA's smem goes away.
+                for (int idx = max(0, issued - NS); idx < issued; ++idx)
+                    mbar_drain(&kv_full[idx % NS], (idx / NS) & 1);
+                mbar_drain(q_full, 0);
+            }
+        }
+    } else if (warp == WARP_MMA) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false, false);
+            constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, false, true);
+            const uint32_t q_base = smem_u32(smem + L::Q_OFF);
+            const uint32_t kv_base = smem_u32(smem + L::KV_OFF);
+            auto issue_s = [&](int t, int st) {
+                const uint32_t qa = q_base + t * L::TILE_BYTES;
+                const uint32_t ka = kv_base + st * L::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * L::CHUNK_BYTES + (kk & 3) * 32;
+                    mma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024),
+                           sdesc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
+                }
+                mma_commit(&s_full[t]);
+            };
+            auto issue_pv = [&](int t, int st, int j) {
+                const uint32_t va = kv_base + st * L::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                           sdesc_sw128(va + kk * 2048, L::CHUNK_BYTES, 1024), IDESC_PV,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                if (j == nblk[t] - 1) mma_commit(&o_full[t]);
+            };
+            bool ok = mbar_wait(q_full, 0, abort_flag, status) &&
+                      mbar_wait(&kv_full[0], 0, abort_flag, status);
+            tc_fence_after();
+            if (ok) {
+                for (int t = 0; t < 2; ++t)
+                    if (nblk[t] > 0) issue_s(t, 0);
+                mma_commit(&kv_empty[0]);
+            }
+            for (int j = 0; j < nmax && ok; ++j) {
+                const int vidx = 2 * j + 1, kidx = 2 * j + 2;
+                const int vst = vidx % NS, kst = kidx % NS;
+                const bool next = j + 1 < nmax;
+                if (!mbar_wait(&kv_full[vst], (vidx / NS) & 1, abort_flag, status)) break;
+                if (j < nblk[0]) {
+                    if (!mbar_wait(&p_full[0], j & 1, abort_flag, status)) break;
+                    tc_fence_after();
+                    issue_pv(0, vst, j);
+                }
+                if (next) {
+                    if (!mbar_wait(&kv_full[kst], (kidx / NS) & 1, abort_flag, status)) break;
+                    tc_fence_after();
+                    if (j + 1 < nblk[0]) issue_s(0, kst);
+                }
+                if (j < nblk[1]) {
+                    if (!mbar_wait(&p_full[1], j & 1, abort_flag, status)) break;
+                    tc_fence_after();
+                    issue_pv(1, vst, j);
+                }
+                mma_commit(&kv_empty[vst]);
+                if (next) {
+                    if (j + 1 < nblk[1]) issue_s(1, kst);
+                    mma_commit(&kv_empty[kst]);
+                }
+            }
+            // Nothing issued may still be running when TMEM is released.
+            mma_commit(mma_done);
+            mbar_drain(mma_done, 0);
+        }
+    } else {
+        // ------------------------------------------------------------------ softmax warps
+        const int t = warp >> 2, wq = warp & 3;
+        const int row = wq * 32 + lane;             // row within the tile = TMEM lane
+        const int r = q0[t] + row;                  // query index
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + t * 128;
+        const uint32_t tO = tmem + lane_off + 256 + t * 128;
+        const int nb = nblk[t];
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nb; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_flag, status));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sraw[128];
+            tmem_ld_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(&sraw[0]));
+            tmem_ld_x64(tS + 64, *reinterpret_cast<uint32_t(*)[64]>(&sraw[64]));
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sraw[c]);
+            const int kbase = j * BN;
+            const bool need_mask = (CAUSAL && kbase + BN - 1 > q0[t]) || (kbase + BN > N);
+            if (need_mask) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const int key = kbase + c;
+                    if ((CAUSAL && key > r) || key >= N) s[c] = -INFINITY;
+                }
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+            const float m_blk = mx * scale_log2;
+            const bool need = m_blk > m + RESCALE_THRESHOLD;
+            if (__any_sync(0xffffffffu, need)) {
+                const float alpha = need ? ex2_approx(m - m_blk) : 1.f;
+                if (need) {
+                    l *= alpha;
+                    m = m_blk;
+                }
+                if (j > 0) rescale_o_row<D>(tO, alpha);
+            }
+            const float m_sub = (m == -INFINITY) ? 0.f : m;
+            float sum = 0.f;
+            uint32_t p[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float p0 = ex2_approx(fmaf(s[2 * c], scale_log2, -m_sub));
+                const float p1 = ex2_approx(fmaf(s[2 * c + 1], scale_log2, -m_sub));
+                sum += p0 + p1;
+                p[c] = pack_bf16x2(p0, p1);
+            }
+            l += sum;
+            tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+            tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_full[t]);
+        }
+        if (ok && nb > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[t], 0, abort_flag, status));
+        if (ok && nb > 0) {
+            tc_fence_after();
+            // Every MMA reading Q tile t has completed, so its smem becomes the O staging tile,
+            // in the same 128B-swizzled layout the TMA store expects.
+            uint8_t *stage = smem + L::Q_OFF + t * L::TILE_BYTES;
+            const float inv_l = 1.f / l;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld_x32(tO + c0, o);
+                uint8_t *rowp = stage + (c0 / 64) * L::CHUNK_BYTES + row * 128;
+                const int u0 = (c0 % 64) / 8;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint4 v;
+                    v.x = pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv_l, __uint_as_float(o[8 * u + 1]) * inv_l);
+                    v.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv_l, __uint_as_float(o[8 * u + 3]) * inv_l);
+                    v.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv_l, __uint_as_float(o[8 * u + 5]) * inv_l);
+                    v.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv_l, __uint_as_float(o[8 * u + 7]) * inv_l);
+                    *reinterpret_cast<uint4 *>(rowp + (((u0 + u) ^ (row & 7)) << 4)) = v;
+                }
+            }
+            if (r < N) LSE[static_cast<size_t>(bh) * N + r] = (m + log2f(l)) * LN2;
+            fence_proxy_async_smem();
+            mbar_arrive(&epi[t]);
+            if (row == 0 && mbar_wait(&epi[t], 0, abort_flag, status)) {
+                for (int ch = 0; ch < D / 64; ++ch)
+                    tma_store_3d(&tmO, stage + ch * L::CHUNK_BYTES, ch * 64, q0[t], bh);
+                tma_store_commit_and_wait_read();
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                   const CUtensorMap &tmV, const CUtensorMap &tmO, float *LSE, unsigned *status,
+                   cudaStream_t stream) {
+    auto kern = fwd_kernel<D, CAUSAL>;
+    const int smem = Layout<D>::BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int BH = p.B * p.Hq;
+    const long long n_pairs = (p.N + 2 * BM - 1) / (2 * BM);
+    const long long grid = n_pairs * BH;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+    kern<<<static_cast<unsigned>(grid), NUM_THREADS, smem, stream>>>(
+        tmQ, tmK, tmV, tmO, LSE, p.Hq, p.Hkv, p.N, BH, scale_log2, status);
+    return cudaGetLastError();
+}
+
+}  // namespace fwd
+
+cudaError_t launch_fwd_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                            const CUtensorMap &tmV, const CUtensorMap &tmO, float *LSE,
+                            unsigned *status, cudaStream_t stream) {
+    if (p.d == 128)
+        return p.causal ? fwd::launch<128, true>(p, tmQ, tmK, tmV, tmO, LSE, status, stream)
+                        : fwd::launch<128, false>(p, tmQ, tmK, tmV, tmO, LSE, status, stream);
+    if (p.d == 64)
+        return p.causal ? fwd::launch<64, true>(p, tmQ, tmK, tmV, tmO, LSE, status, stream)
+                        : fwd::launch<64, false>(p, tmQ, tmK, tmV, tmO, LSE, status, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -1,0 +1,45 @@
+// fa_internal.h -- host-side launchers shared between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "flashattn.h"
+
+namespace fa {
+
+// Problem description after host validation.
+struct Problem {
+    int B, Hq, Hkv, N, d, causal;
+    float scale;
+};
+
+// K1: bf16 forward on tcgen05. Maps are 3-D [d, N, B*H] bf16, box [64, 128, 1], 128B swizzle.
+cudaError_t launch_fwd_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                            const CUtensorMap &tmV, const CUtensorMap &tmO, float *LSE,
+                            unsigned *status, cudaStream_t stream);
+
+// K2: D = rowsum(dO * O) in fp32 and zeroing of the fp32 dQ accumulator.
+cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const void *dO, float *D,
+                                       float *dQacc, cudaStream_t stream);
+
+// K3: bf16 backward main loop on tcgen05.  tmQ / tmdO use a [64, 64, 1] box; tmK, tmV, tmdK,
+// tmdV a [64, 128, 1] box.  Accumulates scale * dS K into dQacc with fp32 reductions.
+cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                                 const CUtensorMap &tmV, const CUtensorMap &tmdO,
+                                 const CUtensorMap &tmdK, const CUtensorMap &tmdV,
+                                 const float *LSE, const float *D, float *dQacc, unsigned *status,
+                                 cudaStream_t stream);
+
+// K4: dQ = bf16(dQacc).
+cudaError_t launch_bwd_dq_convert_bf16(const Problem &p, const float *dQacc, void *dQ,
+                                       cudaStream_t stream);
+
+// K5: fp32 SIMT forward / backward.
+cudaError_t launch_fwd_fp32(const Problem &p, const float *Q, const float *K, const float *V,
+                            float *O, float *LSE, cudaStream_t stream);
+cudaError_t launch_bwd_fp32(const Problem &p, const float *Q, const float *K, const float *V,
+                            const float *O, const float *dO, const float *LSE, float *dQ,
+                            float *dK, float *dV, float *D, cudaStream_t stream);
+
+}  // namespace fa

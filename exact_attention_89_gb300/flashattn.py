@@ -1,0 +1,172 @@
+"""ctypes binding of libflashattn with the C ABI's names (argument marshalling only).
+
+Every computation runs in the CUDA library; this module only turns torch tensors into device
+pointers and sizes, picks the current CUDA stream and raises on a non-OK status.  There is no
+fallback: if ``libflashattn.so`` is missing or the GPU is not sm_103, calls fail loudly.
+
+Low-level functions (same names and argument order as ``include/flashattn.h``):
+    fa_fwd, fa_bwd, fa_bwd_workspace_bytes, fa_fwd_fp32, fa_bwd_fp32,
+    fa_get_device_status, fa_status_string
+Convenience wrappers that allocate outputs with torch:
+    attention_forward, attention_backward
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libflashattn.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_WORKSPACE = 4
+FA_ERR_CUDA = 5
+FA_ERR_DEVICE_TIMEOUT = 6
+FA_ERR_DEVICE_BOUNDS = 7
+
+# Every symbol include/flashattn.h declares.
+EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_fp32", "fa_bwd_fp32",
+            "fa_get_device_status", "fa_status_string")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FlashAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__("%s failed: %s" % (where, fa_status_string(status)))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library with argument types set (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libflashattn.so not found at %s; build it with "
+                                   "exact_attention_89_gb300.build.build()" % LIB_PATH)
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            dims = [i, i, i, i, i, i, f]
+            L.fa_fwd.argtypes = [vp] * 5 + dims + [vp]
+            L.fa_fwd.restype = i
+            L.fa_bwd.argtypes = [vp] * 9 + dims + [vp, sz, vp]
+            L.fa_bwd.restype = i
+            L.fa_fwd_fp32.argtypes = [vp] * 5 + dims + [vp]
+            L.fa_fwd_fp32.restype = i
+            L.fa_bwd_fp32.argtypes = [vp] * 9 + dims + [vp, sz, vp]
+            L.fa_bwd_fp32.restype = i
+            L.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
+            L.fa_bwd_workspace_bytes.restype = sz
+            L.fa_get_device_status.argtypes = [vp]
+            L.fa_get_device_status.restype = i
+            L.fa_status_string.argtypes = [i]
+            L.fa_status_string.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def fa_status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _dims(Q, K):
+    B, Hq, N, d = Q.shape
+    return B, Hq, K.shape[1], N, d
+
+
+def _check(status: int, where: str, check: bool):
+    if check and status != FA_OK:
+        raise FlashAttnError(status, where)
+    return status
+
+
+def fa_fwd(Q, K, V, O, LSE, causal: bool, scale: float, stream=None, check: bool = True) -> int:
+    """O, LSE <- attention(Q, K, V); bf16 [B,H,N,d] tensors, LSE fp32 [B,Hq,N]."""
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    st = lib().fa_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d,
+                      int(bool(causal)), float(scale), _stream(stream))
+    return _check(st, "fa_fwd", check)
+
+
+def fa_bwd_workspace_bytes(B: int, Hq: int, N: int, d: int) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, Hq, N, d))
+
+
+def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, causal: bool, scale: float, workspace,
+           stream=None, check: bool = True) -> int:
+    """dQ, dK, dV <- gradients of attention; workspace is a byte tensor on the device."""
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().fa_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ),
+                      _ptr(dK), _ptr(dV), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                      _ptr(workspace), wbytes, _stream(stream))
+    return _check(st, "fa_bwd", check)
+
+
+def fa_fwd_fp32(Q, K, V, O, LSE, causal: bool, scale: float, stream=None, check: bool = True):
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    st = lib().fa_fwd_fp32(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d,
+                           int(bool(causal)), float(scale), _stream(stream))
+    return _check(st, "fa_fwd_fp32", check)
+
+
+def fa_bwd_fp32(Q, K, V, O, dO, LSE, dQ, dK, dV, causal: bool, scale: float, workspace,
+                stream=None, check: bool = True):
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().fa_bwd_fp32(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ),
+                           _ptr(dK), _ptr(dV), B, Hq, Hkv, N, d, int(bool(causal)),
+                           float(scale), _ptr(workspace), wbytes, _stream(stream))
+    return _check(st, "fa_bwd_fp32", check)
+
+
+def fa_get_device_status(stream=None) -> int:
+    return int(lib().fa_get_device_status(_stream(stream)))
+
+
+# ----------------------------------------------------------------------------- convenience
+def attention_forward(Q, K, V, causal: bool, scale: float | None = None, stream=None):
+    """Allocates O and LSE and runs the forward (bf16 or fp32 by Q's dtype)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(Q.shape[-1])
+    B, Hq, N, d = Q.shape
+    O = torch.empty_like(Q)
+    LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=Q.device)
+    f = fa_fwd_fp32 if Q.dtype == torch.float32 else fa_fwd
+    f(Q, K, V, O, LSE, causal, scale, stream)
+    return O, LSE
+
+
+def attention_backward(Q, K, V, O, dO, LSE, causal: bool, scale: float | None = None,
+                       workspace=None, stream=None):
+    """Allocates dQ, dK, dV (and the workspace unless given) and runs the backward."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(Q.shape[-1])
+    B, Hq, N, d = Q.shape
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_bytes(B, Hq, N, d), dtype=torch.uint8,
+                                device=Q.device)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    f = fa_bwd_fp32 if Q.dtype == torch.float32 else fa_bwd
+    f(Q, K, V, O, dO, LSE, dQ, dK, dV, causal, scale, workspace, stream)
+    return dQ, dK, dV

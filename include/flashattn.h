@@ -1,0 +1,119 @@
+/*
+ * flashattn.h -- C ABI of libflashattn: exact scaled-dot-product attention on GB300 (sm_103a).
+ *
+ * What it computes. For every batch b and query head hq (key/value head hk = hq / (Hq / Hkv)):
+ *     S = scale * Q K^T  (masked pairs excluded),  P = softmax_rows(S),  O = P V,
+ *     LSE_i = ln sum_j exp(S_ij)  (natural log, over the allowed keys j).
+ * The result is exact attention up to floating-point reordering: the method only reorganises
+ * the computation (FlashAttention note (paweldubiel.com), section "mechanism and details").
+ * The forward pass keeps one query tile on chip and streams key/value tiles past it with the
+ * running row max m, running sum l and rescaled accumulator (FlashAttention DAC'24 reading note,
+ * paper.adslab.icu, Methods, the l and O update equations), normalising once at the end
+ * (paweldubiel.com note: result u / l).  The N x N matrices S and P never reach device memory.
+ * The backward pass stores nothing but LSE from the forward and recomputes P tile by tile
+ * ("Attention's hidden recurrence" blog by mzeromiko, section "Flash Attention backward"), with
+ *     D_i = sum_k dO_ik O_ik,   dS = P * (dO V^T - D),
+ *     dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO
+ * (same blog, section "standard attention / backward"; dK and dV are summed over the query
+ * heads that share a key/value head).
+ *
+ * Conventions shared by every entry point.
+ *  - Layout: contiguous [B, H, N, d] with d fastest; Q, O, dO, dQ use H = Hq; K, V, dK, dV use
+ *    H = Hkv; LSE is [B, Hq, N] fp32.  N need not be a multiple of any tile size.
+ *  - causal != 0 keeps key j <= query i (top-left aligned, one N for queries and keys);
+ *    causal == 0 keeps every key.
+ *  - Ownership: every tensor pointer is a DEVICE pointer owned by the caller; the library keeps
+ *    no reference after the call is enqueued.  The library allocates no device memory.
+ *  - Execution: all work is enqueued on `stream` (0 = legacy default stream) and is
+ *    asynchronous; nothing synchronises except fa_get_device_status.
+ *  - Errors: arguments are validated on the host before anything is enqueued; a failed check
+ *    returns its status and enqueues nothing.  A failed launch returns FA_ERR_CUDA.  Failures
+ *    detected on the device (a bounded wait that ran out) are recorded in a per-device status
+ *    word read by fa_get_device_status.  The library never prints, traps or exits.
+ *  - Precision of the bf16 entry points: bf16 inputs and outputs, fp32 accumulation, fp32 LSE,
+ *    probabilities rounded to bf16 (round-to-nearest-even) before the second product.
+ */
+#ifndef FLASHATTN_H
+#define FLASHATTN_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,    /* a size < 1, Hq % Hkv != 0, non-finite or non-positive scale */
+    FA_ERR_UNSUPPORTED = 2,    /* head dim not supported, or the device is not sm_103 */
+    FA_ERR_MISALIGNED = 3,     /* a null pointer or one not aligned to 16 bytes */
+    FA_ERR_WORKSPACE = 4,      /* workspace null or smaller than fa_bwd_workspace_bytes */
+    FA_ERR_CUDA = 5,           /* a CUDA runtime/driver call or a launch failed */
+    FA_ERR_DEVICE_TIMEOUT = 6, /* a kernel's bounded wait ran out (reported by the status word) */
+    FA_ERR_DEVICE_BOUNDS = 7   /* a kernel's own bounds check failed (reported likewise) */
+} fa_status;
+
+/*
+ * Forward, bf16 on tcgen05 tensor cores.
+ *   Q [B,Hq,N,d], K [B,Hkv,N,d], V [B,Hkv,N,d]: bf16 inputs.
+ *   O [B,Hq,N,d] bf16 output; LSE [B,Hq,N] fp32 output (natural log, scale included).
+ *   d must be 64 or 128.  scale is usually 1/sqrt(d).
+ */
+fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                 int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                 cudaStream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd and fa_bwd_fp32 need: D [B,Hq,N] fp32 followed (at a
+ * 256-byte boundary) by the fp32 dQ accumulator [B,Hq,N,d].  Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int Hq, int N, int d);
+
+/*
+ * Backward, bf16 on tcgen05 tensor cores, recomputing P from LSE.
+ *   Q, K, V, O, dO: bf16 inputs as in fa_fwd (O is the forward output; D is formed from it).
+ *   LSE: the fp32 LSE fa_fwd wrote for these inputs.
+ *   dQ [B,Hq,N,d], dK [B,Hkv,N,d], dV [B,Hkv,N,d]: bf16 outputs (dK, dV summed over the group).
+ *   d must be 128 (other head dims return FA_ERR_UNSUPPORTED).
+ *   workspace: caller-owned device scratch of at least fa_bwd_workspace_bytes(B,Hq,N,d) bytes,
+ *   16-byte aligned; its contents on entry do not matter and are clobbered.
+ *   Calls that share one workspace must not overlap on the GPU.
+ */
+fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                 const float *LSE, void *dQ, void *dK, void *dV,
+                 int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                 void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Forward in fp32 on the CUDA cores (no tensor cores), for checks that need fp32 accuracy.
+ * Same shapes and semantics as fa_fwd with every tensor fp32; 1 <= d <= 128.
+ */
+fa_status fa_fwd_fp32(const float *Q, const float *K, const float *V, float *O, float *LSE,
+                      int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                      cudaStream_t stream);
+
+/*
+ * Backward in fp32 on the CUDA cores.  Same shapes and semantics as fa_bwd with every tensor
+ * fp32; 1 <= d <= 128; workspace as for fa_bwd (only its D part is used).
+ */
+fa_status fa_bwd_fp32(const float *Q, const float *K, const float *V, const float *O,
+                      const float *dO, const float *LSE, float *dQ, float *dK, float *dV,
+                      int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                      void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status word.
+ * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_DEVICE_BOUNDS (first failure recorded since the
+ * last read), or FA_ERR_CUDA if the synchronisation itself failed.
+ */
+fa_status fa_get_device_status(cudaStream_t stream);
+
+/* Static, human-readable name of a status code ("FA_OK", ...); never NULL. */
+const char *fa_status_string(fa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLASHATTN_H */

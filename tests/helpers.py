@@ -1,0 +1,55 @@
+"""Shared helpers for the parity tests: moving tensors to the oracle, slicing independent
+(batch, KV-group) sub-problems, and the error measures the tolerances are stated in."""
+import numpy as np
+import torch
+
+
+def f64(t):
+    """Exact fp64 copy of a (bf16 / fp32) tensor as a numpy array."""
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def group_slice(Q, K, V, dO, b, hk):
+    """The sub-problem of batch b and KV head hk: its G query heads and its one KV head.
+    Attention of different (batch, KV head) pairs is independent, so the oracle on the slice
+    gives exactly the slice of the full result."""
+    G = Q.shape[1] // K.shape[1]
+    sl = slice(hk * G, (hk + 1) * G)
+    out = [Q[b:b + 1, sl], K[b:b + 1, hk:hk + 1], V[b:b + 1, hk:hk + 1]]
+    out.append(dO[b:b + 1, sl] if dO is not None else None)
+    return out
+
+
+def max_abs(a, b):
+    return float(np.max(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64))))
+
+
+def mean_abs(a, b):
+    return float(np.mean(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64))))
+
+
+def rel_fro(a, ref):
+    a = np.asarray(a, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.linalg.norm(a - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+# Tolerances of the method's evaluation plan.
+FP32_MAX_ABS = 1e-5
+BF16_O_MAX_ABS = 1e-2
+BF16_O_MEAN_ABS = 1e-3
+BF16_LSE_MAX_ABS = 1e-3
+BF16_GRAD_REL_FRO = 2e-2
+
+
+def sample_rows(B, H, N, n, seed):
+    """Flat row indices (b*H + h)*N + i: first / last rows of every tile edge plus random ones."""
+    rng = np.random.default_rng(seed)
+    edges = [0, 1, 63, 64, 127, 128, 129, 255, 256, N // 2, N - 129, N - 128, N - 2, N - 1]
+    rows = []
+    for bh in rng.choice(B * H, size=min(B * H, 4), replace=False):
+        for i in edges:
+            if 0 <= i < N:
+                rows.append(int(bh) * N + i)
+    rows += rng.integers(0, B * H * N, size=n).tolist()
+    return np.unique(np.asarray(rows, dtype=np.int64))

@@ -1,0 +1,120 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every symbol the
+header declares, and rejects every invalid argument before any CUDA call."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flashattn.h")
+
+A = 0x10000        # a 16-byte aligned fake device address (never dereferenced: checks fail first)
+MIS = 0x10008      # 8-byte aligned only
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names(built_lib):
+    assert declared_functions() == sorted(built_lib.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(built_lib):
+    L = built_lib.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(built_lib):
+    names = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
+             "FA_ERR_WORKSPACE", "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT", "FA_ERR_DEVICE_BOUNDS"]
+    for code, name in enumerate(names):
+        assert built_lib.fa_status_string(code) == name
+    assert built_lib.fa_status_string(99) == "FA_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(built_lib):
+    f = built_lib.fa_bwd_workspace_bytes
+    rows = 2 * 32 * 4096
+    assert f(2, 32, 4096, 128) == ((rows * 4 + 255) // 256) * 256 + rows * 128 * 4
+    assert f(1, 1, 1, 1) == 256 + 4
+    assert f(0, 1, 1, 1) == 0 and f(1, 1, -1, 64) == 0
+
+
+def fwd(L, Q=A, K=A, V=A, O=A, LSE=A, B=1, Hq=2, Hkv=1, N=64, d=128, causal=1, scale=0.1, fp32=False):
+    fn = L.fa_fwd_fp32 if fp32 else L.fa_fwd
+    return fn(Q, K, V, O, LSE, B, Hq, Hkv, N, d, causal, scale, None)
+
+
+def bwd(L, ptrs=None, B=1, Hq=2, Hkv=1, N=64, d=128, causal=1, scale=0.1, ws=A, wbytes=None,
+        fp32=False):
+    ptrs = ptrs or [A] * 9
+    if wbytes is None:
+        wbytes = L.fa_bwd_workspace_bytes(B, Hq, N, d)
+    fn = L.fa_bwd_fp32 if fp32 else L.fa_bwd
+    return fn(*ptrs, B, Hq, Hkv, N, d, causal, scale, ws, wbytes, None)
+
+
+@pytest.mark.parametrize("fp32", [False, True])
+def test_forward_rejects_invalid_arguments(built_lib, fp32):
+    L = built_lib.lib()
+    E = built_lib
+    assert fwd(L, B=0, fp32=fp32) == E.FA_ERR_INVALID_ARG
+    assert fwd(L, Hq=0, fp32=fp32) == E.FA_ERR_INVALID_ARG
+    assert fwd(L, Hkv=0, fp32=fp32) == E.FA_ERR_INVALID_ARG
+    assert fwd(L, N=0, fp32=fp32) == E.FA_ERR_INVALID_ARG
+    assert fwd(L, N=-5, fp32=fp32) == E.FA_ERR_INVALID_ARG
+    assert fwd(L, Hq=3, Hkv=2, fp32=fp32) == E.FA_ERR_INVALID_ARG
+    for s in (0.0, -0.5, math.nan, math.inf):
+        assert fwd(L, scale=s, fp32=fp32) == E.FA_ERR_INVALID_ARG
+    assert fwd(L, d=0, fp32=fp32) == E.FA_ERR_INVALID_ARG
+    assert fwd(L, d=129 if fp32 else 96, fp32=fp32) == E.FA_ERR_UNSUPPORTED
+    for k in ("Q", "K", "V", "O", "LSE"):
+        assert fwd(L, **{k: None}, fp32=fp32) == E.FA_ERR_MISALIGNED
+        assert fwd(L, **{k: MIS}, fp32=fp32) == E.FA_ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("fp32", [False, True])
+def test_backward_rejects_invalid_arguments(built_lib, fp32):
+    L = built_lib.lib()
+    E = built_lib
+    assert bwd(L, B=0, fp32=fp32) == E.FA_ERR_INVALID_ARG
+    assert bwd(L, Hq=4, Hkv=3, fp32=fp32) == E.FA_ERR_INVALID_ARG
+    assert bwd(L, scale=math.nan, fp32=fp32) == E.FA_ERR_INVALID_ARG
+    if not fp32:
+        assert bwd(L, d=64, fp32=fp32) == E.FA_ERR_UNSUPPORTED
+    assert bwd(L, d=200, fp32=fp32) == E.FA_ERR_UNSUPPORTED
+    for k in range(9):
+        ptrs = [A] * 9
+        ptrs[k] = None
+        assert bwd(L, ptrs, fp32=fp32) == E.FA_ERR_MISALIGNED
+        ptrs[k] = MIS
+        assert bwd(L, ptrs, fp32=fp32) == E.FA_ERR_MISALIGNED
+    need = L.fa_bwd_workspace_bytes(1, 2, 64, 128)
+    assert bwd(L, wbytes=need - 1, fp32=fp32) == E.FA_ERR_WORKSPACE
+    assert bwd(L, ws=None, fp32=fp32) == E.FA_ERR_WORKSPACE
+    assert bwd(L, ws=MIS, fp32=fp32) == E.FA_ERR_WORKSPACE
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    """The binding never falls back: a missing library is an error, not a CPU path."""
+    from exact_attention_89_gb300 import flashattn
+    monkeypatch.setattr(flashattn, "_lib", None)
+    monkeypatch.setattr(flashattn, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        flashattn.lib()
+
+
+def test_product_path_does_not_reference_the_oracle():
+    """Nothing in the package or the CUDA sources imports, loads or names the oracle module."""
+    pkg = os.path.join(ROOT, "exact_attention_89_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"\bimport\s+oracle\b|\bfrom\s+oracle\b|liboracle", text), fn
