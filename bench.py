@@ -203,6 +203,9 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for cpu_baseline (0 disables)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="only warm-up and timed steps (no clock load, e2e or cpu baseline); "
+                         "for profiler runs")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -262,7 +265,18 @@ def main():
         bus = None
     sampler = ClockSampler(str(bus) if bus is not None else None)
     sampler.start()
-    time.sleep(0.3)
+
+    def load_for(seconds):
+        # the same steps, untimed, so the clock samples around the short timed region are
+        # taken under the same load
+        t_end_load = time.perf_counter() + seconds
+        while time.perf_counter() < t_end_load:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
+
+    if not args.no_extras:
+        load_for(0.8)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
@@ -280,6 +294,8 @@ def main():
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
+    if not args.no_extras:
+        load_for(0.6)
     clocks = sampler.stop()
     st = fa.fa_get_device_status()
     if st != fa.FA_OK:
@@ -308,18 +324,20 @@ def main():
         for hbuf, dbuf in zip(outs_h, (Od, Ld, gq, gk, gv)):
             hbuf.copy_(dbuf, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier()
-    e_s = torch.cuda.Event(enable_timing=True)
-    e_e = torch.cuda.Event(enable_timing=True)
-    e_s.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e_e.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e_s.elapsed_time(e_e)
+    e2e_ms = float("nan")
+    if not args.no_extras:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e_s = torch.cuda.Event(enable_timing=True)
+        e_e = torch.cuda.Event(enable_timing=True)
+        e_s.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e_e.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e_s.elapsed_time(e_e)
     t2 = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
     if ws > 1:
         dist.all_reduce(t2, op=dist.ReduceOp.MAX)
@@ -344,7 +362,7 @@ def main():
                         "flops_per_launch": w.flops_fwd()},
                 "bwd_ms": bwd_ms, "sources": src_hash}
     cpu = None
-    if rank == 0 and ws == 1 and args.cpu_budget > 0:
+    if rank == 0 and ws == 1 and args.cpu_budget > 0 and not args.no_extras:
         r = cpu_oracle_sample(w, args.cpu_budget, 8)
         cpu = {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")}
 

@@ -21,6 +21,8 @@
 // The MMA order S0(j+1) after PV0(j) lets softmax of one tile overlap the other tile's MMAs.
 // Rescaling of O is lazy: the stale max is kept until the block max exceeds it by 8 (log2
 // units), so p <= 2^8; the shift cancels in O = u / l, so the result is unchanged.
+// O is divided by the sum of the bf16-rounded weights that entered P V (so the applied weights
+// sum to one); LSE uses the sum of the unrounded fp32 weights.
 #include <cmath>
 
 #include "fa_internal.h"
@@ -244,7 +246,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t tS = tmem + lane_off + t * 128;
         const uint32_t tO = tmem + lane_off + 256 + t * 128;
         const int nb = nblk[t];
-        float m = -INFINITY, l = 0.f;
+        // l: sum of the fp32 weights (gives LSE); lr: sum of the bf16-rounded weights that the
+        // P V product actually uses (normalises O, so the weights applied sum to one).
+        float m = -INFINITY, l = 0.f, lr = 0.f;
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_flag, status));
@@ -274,21 +278,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float alpha = need ? ex2_approx(m - m_blk) : 1.f;
                 if (need) {
                     l *= alpha;
+                    lr *= alpha;
                     m = m_blk;
                 }
                 if (j > 0) rescale_o_row<D>(tO, alpha);
             }
             const float m_sub = (m == -INFINITY) ? 0.f : m;
-            float sum = 0.f;
+            float sum = 0.f, sum_r = 0.f;
             uint32_t p[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
                 const float p0 = ex2_approx(fmaf(s[2 * c], scale_log2, -m_sub));
                 const float p1 = ex2_approx(fmaf(s[2 * c + 1], scale_log2, -m_sub));
                 sum += p0 + p1;
-                p[c] = pack_bf16x2(p0, p1);
+                const uint32_t pk = pack_bf16x2(p0, p1);
+                p[c] = pk;
+                sum_r += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xffff0000u);
             }
             l += sum;
+            lr += sum_r;
             tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
             tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
             tmem_wait_st();
@@ -301,7 +309,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // Every MMA reading Q tile t has completed, so its smem becomes the O staging tile,
             // in the same 128B-swizzled layout the TMA store expects.
             uint8_t *stage = smem + L::Q_OFF + t * L::TILE_BYTES;
-            const float inv_l = 1.f / l;
+            const float inv_l = 1.f / lr;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];

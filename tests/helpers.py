@@ -3,6 +3,15 @@
 import numpy as np
 import torch
 
+# Device the parity tests run the CUDA path on.
+DEVICE = torch.device("cuda:0")
+
+
+def _np(x):
+    if isinstance(x, torch.Tensor):
+        return x.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(x, np.float64)
+
 
 def f64(t):
     """Exact fp64 copy of a (bf16 / fp32) tensor as a numpy array."""
@@ -21,16 +30,16 @@ def group_slice(Q, K, V, dO, b, hk):
 
 
 def max_abs(a, b):
-    return float(np.max(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64))))
+    return float(np.max(np.abs(_np(a) - _np(b))))
 
 
 def mean_abs(a, b):
-    return float(np.mean(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64))))
+    return float(np.mean(np.abs(_np(a) - _np(b))))
 
 
 def rel_fro(a, ref):
-    a = np.asarray(a, np.float64)
-    ref = np.asarray(ref, np.float64)
+    a = _np(a)
+    ref = _np(ref)
     return float(np.linalg.norm(a - ref) / max(np.linalg.norm(ref), 1e-300))
 
 

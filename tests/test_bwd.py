@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 import torch
 
+import helpers
 from exact_attention_89_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
 from helpers import BF16_GRAD_REL_FRO, f64, group_slice, rel_fro, sample_rows
 
@@ -15,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 
 def gpu_fwd_bwd(flash, Q, K, V, dO, causal, scale):
-    dev = torch.device("cuda:0")
+    dev = helpers.DEVICE
     q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
     O, LSE = flash.attention_forward(q, k, v, causal, scale)
     dQ, dK, dV = flash.attention_backward(q, k, v, O, do, LSE, causal, scale)

@@ -4,6 +4,7 @@ import numpy as np
 import pytest
 import torch
 
+import helpers
 from exact_attention_89_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
 from helpers import FP32_MAX_ABS, f64, max_abs
 
@@ -11,7 +12,7 @@ pytestmark = pytest.mark.gpu
 
 
 def run_fp32(flash, Q, K, V, dO, causal, scale):
-    dev = torch.device("cuda:0")
+    dev = helpers.DEVICE
     q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
     O, LSE = flash.attention_forward(q, k, v, causal, scale)
     dQ, dK, dV = flash.attention_backward(q, k, v, O, do, LSE, causal, scale)

@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 import torch
 
+import helpers
 from exact_attention_89_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
 from helpers import (BF16_LSE_MAX_ABS, BF16_O_MAX_ABS, BF16_O_MEAN_ABS, f64, group_slice,
                      max_abs, mean_abs, sample_rows)
@@ -15,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 
 def gpu_forward(flash, Q, K, V, causal, scale):
-    dev = torch.device("cuda:0")
+    dev = helpers.DEVICE
     q, k, v = (t.to(dev) for t in (Q, K, V))
     O, LSE = flash.attention_forward(q, k, v, causal, scale)
     assert flash.fa_get_device_status() == flash.FA_OK
