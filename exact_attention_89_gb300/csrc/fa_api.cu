@@ -80,6 +80,8 @@ fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+int g_sms[kMaxDevices] = {0};
+
 // 3-D bf16 view [d, N, BH] of a contiguous [BH, N, d] tensor, box [64, rows, 1], 128B swizzle.
 bool encode_bf16(CUtensorMap *m, const void *base, int d, int N, long long BH, int box_rows) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
@@ -97,6 +99,19 @@ bool encode_bf16(CUtensorMap *m, const void *base, int d, int N, long long BH, i
 fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 }  // namespace
+
+int num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    if (g_sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            n = 148;
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
 }  // namespace fa
 
 using fa::Problem;

@@ -10,19 +10,25 @@
 // K2 forms D and clears the fp32 dQ accumulator.  K3 gives each CTA one 128-key block of one
 // (batch, KV head); it loops over the G query heads of the group and over 64-row query tiles
 // (under causal masking only tiles at or below the block's diagonal), so dK and dV of the block
-// accumulate in TMEM across the whole group and need no atomics.  Per query tile:
+// accumulate in TMEM across the whole group and need no atomics.  Per query tile (step s):
 //   S^T = K Q^T and dP^T = V dO^T        (SS MMAs, M = 128 keys, N = 64 queries, K = d)
 //   P^T = exp2(S^T c - LSE log2 e), dS^T = P^T (dP^T - D)   (thread = key row = TMEM lane)
-//   dV += P^T dO,  dK += dS^T Q          (TS MMAs: P^T / dS^T as bf16 in TMEM, over S^T / dP^T)
+//   dV += P^T dO,  dK += dS^T Q          (TS MMAs: P^T / dS^T as bf16 in TMEM)
 //   dQ^T = K^T dS^T                      (SS MMA, M = d = 128, dS^T staged in smem)
 // and a second warpgroup reduces scale * dQ^T into the fp32 accumulator with coalesced
 // fp32 reductions (thread = one column d of dQ).  K4 rounds the accumulator to bf16.
 // dQ strategy: recomputing S and dP in a separate dQ kernel would cost 7 products per tile
 // instead of 5 (+40% tensor work); the reduction costs L2 bandwidth instead.
 //
+// Software pipeline: S^T / dP^T are double-buffered in TMEM, so the products of step s+1 are
+// issued before those that consume step s, and the softmax-gradient warps of one step overlap
+// the tensor core's work on the other.  Inside a buffer, P^T and dS^T (bf16) are both written over
+// the S^T half, which frees the dP^T half for the dQ^T product of the same step.
+//
 // Roles (320 threads): warps 0-3 softmax-gradient, warps 4-7 dQ drain, warp 8 TMA, warp 9 MMA.
-// TMEM (512 columns): dK [0,128), dV [128,256), S^T/P^T [256,320), dP^T/dS^T [320,384),
-// dQ^T [384,448).
+// TMEM (512 columns): dK [0,128), dV [128,256), buffer b at 256 + 128 b:
+//   [+0,+64) S^T -> P^T [+0,+32) and dS^T [+32,+64);  [+64,+128) dP^T -> dQ^T.
+#include <algorithm>
 #include <cmath>
 
 #include "fa_internal.h"
@@ -33,7 +39,7 @@ namespace bwd {
 
 constexpr int BKV = 128;          // keys per CTA (= TMEM lanes)
 constexpr int BQ = 64;            // query rows per step
-constexpr int NSQ = 2;            // Q / dO ring stages
+constexpr int NSQ = 3;            // Q / dO ring stages
 constexpr int NUM_THREADS = 320;
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
@@ -45,20 +51,23 @@ struct Layout {
     static constexpr int KV_CHUNK = BKV * 128;            // 128 rows x 64 bf16
     static constexpr int Q_BYTES = BQ * D * 2;            // Q or dO tile
     static constexpr int Q_CHUNK = BQ * 128;              // 64 rows x 64 bf16
+    static constexpr int DS_BYTES = BKV * BQ * 2;         // dS^T: 128 rows x 64 bf16
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = K_OFF + KV_BYTES;
     static constexpr int QR_OFF = V_OFF + KV_BYTES;        // ring: [stage][Q | dO]
-    static constexpr int DS_OFF = QR_OFF + NSQ * 2 * Q_BYTES;  // dS^T: 128 rows x 64 bf16
-    static constexpr int STAT_OFF = DS_OFF + BKV * 128;     // [2 buffers][lse2 64 | D 64] fp32
+    static constexpr int DS_OFF = QR_OFF + NSQ * 2 * Q_BYTES;  // [2][dS^T]
+    static constexpr int STAT_OFF = DS_OFF + 2 * DS_BYTES;     // [2][lse2 64 | D 64] fp32
     static constexpr int BAR_OFF = STAT_OFF + 2 * 2 * BQ * 4;
-    // kv_full, q_full[NSQ], q_empty[NSQ], s_full, p_full, dq_full, dq_empty, acc_full, epi, mma_done
-    static constexpr int NBARS = 1 + 2 * NSQ + 7;
+    // kv_full, q_full[NSQ], q_empty[NSQ], s_full[2], p_full[2], dq_full[2], dq_empty[2],
+    // acc_full, epi, mma_done
+    static constexpr int NBARS = 1 + 2 * NSQ + 8 + 3;
     static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
     static constexpr int ABORT_OFF = TMEM_OFF + 8;
     static constexpr int BYTES = ABORT_OFF + 8 + 1024;
 };
 
-constexpr uint32_t T_DK = 0, T_DV = 128, T_ST = 256, T_DPT = 320, T_DQT = 384;
+constexpr uint32_t T_DK = 0, T_DV = 128, T_BUF = 256;
+constexpr uint32_t B_ST = 0, B_PT = 0, B_DST = 32, B_DPT = 64, B_DQT = 64;
 
 template <bool CAUSAL>
 __device__ __forceinline__ int first_q_tile(int jb) {
@@ -71,8 +80,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                     const float *__restrict__ LSE, const float *__restrict__ Dvec,
-                    float *__restrict__ dQacc, int Hq, int Hkv, int N, int BHkv, float scale,
-                    float scale_log2, unsigned *status) {
+                    float *__restrict__ dQacc, int Hq, int Hkv, int N, int BHkv, int HC,
+                    float scale, float scale_log2, unsigned *status) {
     static_assert(D == 128, "the bf16 backward main loop is laid out for d = 128");
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -82,11 +91,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t *kv_full = bars;
     uint64_t *q_full = bars + 1;
     uint64_t *q_empty = q_full + NSQ;
-    uint64_t *s_full = q_empty + NSQ;
-    uint64_t *p_full = s_full + 1;
-    uint64_t *dq_full = p_full + 1;
-    uint64_t *dq_empty = dq_full + 1;
-    uint64_t *acc_full = dq_empty + 1;
+    uint64_t *s_full = q_empty + NSQ;      // [2]
+    uint64_t *p_full = s_full + 2;         // [2]
+    uint64_t *dq_full = p_full + 2;        // [2]
+    uint64_t *dq_empty = dq_full + 2;      // [2]
+    uint64_t *acc_full = dq_empty + 2;
     uint64_t *epi = acc_full + 1;
     uint64_t *mma_done = epi + 1;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::TMEM_OFF);
@@ -95,13 +104,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = Hq / Hkv;
-    const int bkv = blockIdx.x % BHkv;          // b * Hkv + hk
-    const int jb = blockIdx.x / BHkv;           // key block; small jb (most work) first
+    const int nkb = (N + BKV - 1) / BKV;
+    // Work item: (key block jb, batch * KV head).  KV heads go in chunks of HC (about one wave),
+    // so the Q / dO / dQ accumulator rows of the heads in flight stay in L2; inside a chunk the
+    // small jb (most query tiles under causal masking) go first.
+    const int chunk = blockIdx.x / (HC * nkb);
+    const int in_chunk = blockIdx.x - chunk * HC * nkb;
+    const int hc = min(HC, BHkv - chunk * HC);
+    const int bkv = chunk * HC + in_chunk % hc;          // b * Hkv + hk
+    const int jb = in_chunk / hc;
     const int b = bkv / Hkv, hk = bkv % Hkv;
     const int nq = (N + BQ - 1) / BQ;
     const int i0 = first_q_tile<CAUSAL>(jb);
     const int tiles_per_head = nq - i0;
-    const int T = G * tiles_per_head;           // steps of this CTA
+    const int T = G * tiles_per_head;           // steps of this CTA (>= 1)
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
@@ -109,10 +125,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&q_full[s], 1);
             mbar_init(&q_empty[s], 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(p_full, 128);
-        mbar_init(dq_full, 1);
-        mbar_init(dq_empty, 128);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&s_full[k], 1);
+            mbar_init(&p_full[k], 128);
+            mbar_init(&dq_full[k], 1);
+            mbar_init(&dq_empty[k], 128);
+        }
         mbar_init(acc_full, 1);
         mbar_init(epi, 128);
         mbar_init(mma_done, 1);
@@ -131,6 +149,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_TMA) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmdO);
             mbar_arrive_expect_tx(kv_full, 2 * L::KV_BYTES);
             for (int ch = 0; ch < D / 64; ++ch) {
                 tma_load_3d(smem + L::K_OFF + ch * L::KV_CHUNK, &tmK, ch * 64, jb * BKV, bkv, kv_full);
@@ -166,51 +186,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t k_base = smem_u32(smem + L::K_OFF);
             const uint32_t v_base = smem_u32(smem + L::V_OFF);
             const uint32_t ds_base = smem_u32(smem + L::DS_OFF);
-            bool ok = mbar_wait(kv_full, 0, abort_flag, status);
-            tc_fence_after();
-            for (int s = 0; s < T && ok; ++s) {
-                const int st = s % NSQ;
-                const uint32_t q_base = smem_u32(smem + L::QR_OFF + st * 2 * L::Q_BYTES);
-                const uint32_t do_base = q_base + L::Q_BYTES;
-                if (!mbar_wait(&q_full[st], (s / NSQ) & 1, abort_flag, status)) break;
-                tc_fence_after();
+            auto qring = [&](int s) { return smem_u32(smem + L::QR_OFF + (s % NSQ) * 2 * L::Q_BYTES); };
+            // S^T(s) and dP^T(s) into buffer s & 1
+            auto issue_sp = [&](int s) {
+                const uint32_t q_base = qring(s), do_base = q_base + L::Q_BYTES;
+                const uint32_t buf = tmem + T_BUF + (s & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
-                    mma_ss(tmem + T_ST, sdesc_sw128(k_base + oa, 16, 1024),
+                    mma_ss(buf + B_ST, sdesc_sw128(k_base + oa, 16, 1024),
                            sdesc_sw128(q_base + ob, 16, 1024), IDESC_SP, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
-                    mma_ss(tmem + T_DPT, sdesc_sw128(v_base + oa, 16, 1024),
+                    mma_ss(buf + B_DPT, sdesc_sw128(v_base + oa, 16, 1024),
                            sdesc_sw128(do_base + ob, 16, 1024), IDESC_SP, kk > 0);
                 }
-                mma_commit(s_full);
-                if (!mbar_wait(p_full, s & 1, abort_flag, status)) break;
+                mma_commit(&s_full[s & 1]);
+            };
+            bool ok = mbar_wait(kv_full, 0, abort_flag, status) &&
+                      mbar_wait(&q_full[0], 0, abort_flag, status);
+            tc_fence_after();
+            if (ok) issue_sp(0);
+            for (int s = 0; s < T && ok; ++s) {
+                const int bsel = s & 1;
+                const uint32_t buf = tmem + T_BUF + bsel * 128;
+                if (s + 1 < T) {
+                    if (!mbar_wait(&q_full[(s + 1) % NSQ], ((s + 1) / NSQ) & 1, abort_flag, status)) break;
+                    // buffer (s+1)&1 last held dQ^T(s-1): wait until the drain warps read it
+                    if (s >= 1 && !mbar_wait(&dq_empty[bsel ^ 1], ((s - 1) >> 1) & 1, abort_flag, status)) break;
+                    tc_fence_after();
+                    issue_sp(s + 1);
+                }
+                if (!mbar_wait(&p_full[bsel], (s >> 1) & 1, abort_flag, status)) break;
                 tc_fence_after();
+                const uint32_t q_base = qring(s), do_base = q_base + L::Q_BYTES;
                 // dV += P^T dO ; dK += dS^T Q   (B operands MN-major: d contiguous)
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + T_DV, tmem + T_ST + kk * 8,
+                    mma_ts(tmem + T_DV, buf + B_PT + kk * 8,
                            sdesc_sw128(do_base + kk * 2048, L::Q_CHUNK, 1024), IDESC_KV,
                            (s > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + T_DK, tmem + T_DPT + kk * 8,
+                    mma_ts(tmem + T_DK, buf + B_DST + kk * 8,
                            sdesc_sw128(q_base + kk * 2048, L::Q_CHUNK, 1024), IDESC_KV,
                            (s > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&q_empty[st]);
+                mma_commit(&q_empty[s % NSQ]);
                 // dQ^T = K^T dS^T  (A = K MN-major, B = dS^T MN-major, K dim = 128 keys)
-                if (!mbar_wait(dq_empty, (s & 1) ^ 1, abort_flag, status)) break;
-                tc_fence_after();
+                const uint32_t dsb = ds_base + bsel * L::DS_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BKV / 16; ++kk)
-                    mma_ss(tmem + T_DQT, sdesc_sw128(k_base + kk * 2048, L::KV_CHUNK, 1024),
-                           sdesc_sw128(ds_base + kk * 2048, BKV * 128, 1024), IDESC_DQ, kk > 0);
-                mma_commit(dq_full);
+                    mma_ss(buf + B_DQT, sdesc_sw128(k_base + kk * 2048, L::KV_CHUNK, 1024),
+                           sdesc_sw128(dsb + kk * 2048, L::DS_BYTES, 1024), IDESC_DQ, kk > 0);
+                mma_commit(&dq_full[bsel]);
             }
             mma_commit(acc_full);
             mma_commit(mma_done);
@@ -221,13 +253,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int krow = warp * 32 + lane;          // key row within the block = TMEM lane
         const int key = jb * BKV + krow;
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        uint8_t *ds_row = smem + L::DS_OFF + krow * 128;
+        const uint64_t c2 = f2_pack(scale_log2, scale_log2);
         bool ok = true;
         for (int s = 0; s < T; ++s) {
             const int g = s / tiles_per_head, i = i0 + s % tiles_per_head;
             const int bhq = b * Hq + hk * G + g;
             const int q0 = i * BQ;
-            float *buf = stat + (s & 1) * 2 * BQ;
+            const int bsel = s & 1;
+            const uint32_t buf = tmem + lane_off + T_BUF + bsel * 128;
+            float *sbuf = stat + bsel * 2 * BQ;
             // statistics of this query tile: thread t < 64 loads LSE_t, t >= 64 loads D_{t-64};
             // the global loads are in flight while the thread waits for the MMAs.
             float v;
@@ -238,44 +272,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 else
                     v = (q < N) ? Dvec[static_cast<size_t>(bhq) * N + q] : 0.f;
             }
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full, s & 1, abort_flag, status));
-            buf[krow] = v;
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[bsel], (s >> 1) & 1, abort_flag, status));
+            sbuf[krow] = v;
             // executed by all four warps every step (even after a failed wait) so the counts match
             named_barrier_sync(1, 128);
             if (ok) {
                 tc_fence_after();
                 uint32_t sr[64], dr[64];
-                tmem_ld_x64(tmem + lane_off + T_ST, sr);
-                tmem_ld_x64(tmem + lane_off + T_DPT, dr);
+                tmem_ld_x64(buf + B_ST, sr);
+                tmem_ld_x64(buf + B_DPT, dr);
                 const bool need_mask = (CAUSAL && q0 < jb * BKV + BKV) || (q0 + BQ > N) ||
                                        (jb * BKV + BKV > N);
+                const float4 *l4 = reinterpret_cast<const float4 *>(sbuf);
+                const float4 *d4 = reinterpret_cast<const float4 *>(sbuf + BQ);
                 uint32_t pp[32], dd[32];
 #pragma unroll
-                for (int c = 0; c < BQ; c += 2) {
-                    float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, -buf[c]));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), scale_log2, -buf[c + 1]));
+                for (int c = 0; c < BQ; c += 4) {
+                    const float4 lse = l4[c >> 2];
+                    const float4 dv = d4[c >> 2];
+                    float2 pa = f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                                                 c2, f2_pack(-lse.x, -lse.y)));
+                    float2 pb = f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])),
+                                                 c2, f2_pack(-lse.z, -lse.w)));
+                    pa.x = ex2_approx(pa.x);
+                    pa.y = ex2_approx(pa.y);
+                    pb.x = ex2_approx(pb.x);
+                    pb.y = ex2_approx(pb.y);
                     if (need_mask) {
                         const int q = q0 + c;
-                        if ((CAUSAL && key > q) || q >= N || key >= N) p0 = 0.f;
-                        if ((CAUSAL && key > q + 1) || q + 1 >= N || key >= N) p1 = 0.f;
+                        if ((CAUSAL && key > q) || q >= N || key >= N) pa.x = 0.f;
+                        if ((CAUSAL && key > q + 1) || q + 1 >= N || key >= N) pa.y = 0.f;
+                        if ((CAUSAL && key > q + 2) || q + 2 >= N || key >= N) pb.x = 0.f;
+                        if ((CAUSAL && key > q + 3) || q + 3 >= N || key >= N) pb.y = 0.f;
                     }
-                    const float d0 = p0 * (__uint_as_float(dr[c]) - buf[BQ + c]);
-                    const float d1 = p1 * (__uint_as_float(dr[c + 1]) - buf[BQ + c + 1]);
-                    pp[c >> 1] = pack_bf16x2(p0, p1);
-                    dd[c >> 1] = pack_bf16x2(d0, d1);
+                    const uint64_t pa2 = f2_pack(pa.x, pa.y), pb2 = f2_pack(pb.x, pb.y);
+                    const float2 da = f2_unpack(f2_mul(pa2, f2_add(
+                        f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), f2_pack(-dv.x, -dv.y))));
+                    const float2 db = f2_unpack(f2_mul(pb2, f2_add(
+                        f2_pack(__uint_as_float(dr[c + 2]), __uint_as_float(dr[c + 3])), f2_pack(-dv.z, -dv.w))));
+                    pp[c >> 1] = pack_bf16x2(pa.x, pa.y);
+                    pp[(c >> 1) + 1] = pack_bf16x2(pb.x, pb.y);
+                    dd[c >> 1] = pack_bf16x2(da.x, da.y);
+                    dd[(c >> 1) + 1] = pack_bf16x2(db.x, db.y);
                 }
-                tmem_st_x32(tmem + lane_off + T_ST, pp);
-                tmem_st_x32(tmem + lane_off + T_DPT, dd);
-                // dS^T row -> smem (128B-swizzled, MN-major B operand of the dQ^T product)
+                tmem_st_x32(buf + B_PT, pp);
+                tmem_st_x32(buf + B_DST, dd);
+                // dS^T row -> smem buffer (128B-swizzled, MN-major B operand of the dQ^T product)
+                uint8_t *ds_row = smem + L::DS_OFF + bsel * L::DS_BYTES + krow * 128;
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    uint4 v = make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
-                    *reinterpret_cast<uint4 *>(ds_row + ((u ^ (krow & 7)) << 4)) = v;
+                    uint4 w4 = make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+                    *reinterpret_cast<uint4 *>(ds_row + ((u ^ (krow & 7)) << 4)) = w4;
                 }
                 tmem_wait_st();
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(p_full);
+                mbar_arrive(&p_full[bsel]);
             }
         }
         // epilogue: dK (scaled) and dV rows -> bf16 -> smem (over K / V) -> TMA store
@@ -295,12 +347,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int u0 = (c0 % 64) / 8;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(a[8 * u + 0]) * mul, __uint_as_float(a[8 * u + 1]) * mul);
-                        v.y = pack_bf16x2(__uint_as_float(a[8 * u + 2]) * mul, __uint_as_float(a[8 * u + 3]) * mul);
-                        v.z = pack_bf16x2(__uint_as_float(a[8 * u + 4]) * mul, __uint_as_float(a[8 * u + 5]) * mul);
-                        v.w = pack_bf16x2(__uint_as_float(a[8 * u + 6]) * mul, __uint_as_float(a[8 * u + 7]) * mul);
-                        *reinterpret_cast<uint4 *>(rowp + (((u0 + u) ^ (krow & 7)) << 4)) = v;
+                        uint4 w4;
+                        w4.x = pack_bf16x2(__uint_as_float(a[8 * u + 0]) * mul, __uint_as_float(a[8 * u + 1]) * mul);
+                        w4.y = pack_bf16x2(__uint_as_float(a[8 * u + 2]) * mul, __uint_as_float(a[8 * u + 3]) * mul);
+                        w4.z = pack_bf16x2(__uint_as_float(a[8 * u + 4]) * mul, __uint_as_float(a[8 * u + 5]) * mul);
+                        w4.w = pack_bf16x2(__uint_as_float(a[8 * u + 6]) * mul, __uint_as_float(a[8 * u + 7]) * mul);
+                        *reinterpret_cast<uint4 *>(rowp + (((u0 + u) ^ (krow & 7)) << 4)) = w4;
                     }
                 }
             }
@@ -323,12 +375,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int g = s / tiles_per_head, i = i0 + s % tiles_per_head;
             const int bhq = b * Hq + hk * G + g;
             const int q0 = i * BQ;
-            if (!__all_sync(0xffffffffu, mbar_wait(dq_full, s & 1, abort_flag, status))) break;
+            const int bsel = s & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&dq_full[bsel], (s >> 1) & 1, abort_flag, status))) break;
             tc_fence_after();
             uint32_t a[64];
-            tmem_ld_x64(tmem + lane_off + T_DQT, a);
+            tmem_ld_x64(tmem + lane_off + T_BUF + bsel * 128 + B_DQT, a);
             tc_fence_before();
-            mbar_arrive(dq_empty);
+            mbar_arrive(&dq_empty[bsel]);
             float *dst = dQacc + (static_cast<size_t>(bhq) * N + q0) * D + dcol;
             const int nvalid = min(BQ, N - q0);
 #pragma unroll
@@ -410,12 +463,6 @@ static int grid_for(long long work, int per_block, int num_sms) {
     return static_cast<int>(g);
 }
 
-static int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
-    return n;
-}
 
 }  // namespace bwd
 
@@ -423,7 +470,7 @@ cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const vo
                                        float *dQacc, cudaStream_t stream) {
     const long long rows = static_cast<long long>(p.B) * p.Hq * p.N;
     const long long acc4 = rows * p.d / 4;
-    const int sms = bwd::sm_count();
+    const int sms = num_sms();
     const int grid = bwd::grid_for(rows * (p.d / 8), 256, sms);
     bwd::bwd_preprocess_kernel<<<grid, 256, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), D,
@@ -439,6 +486,7 @@ cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const
     if (p.d != 128) return cudaErrorInvalidValue;
     const int BHkv = p.B * p.Hkv;
     const long long nkb = (p.N + bwd::BKV - 1) / bwd::BKV;
+    const int HC = static_cast<int>(std::max<long long>(1, std::min<long long>(BHkv, num_sms() / nkb)));
     const long long grid = nkb * BHkv;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int smem = bwd::Layout<128>::BYTES;
@@ -449,14 +497,14 @@ cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         kern<<<static_cast<unsigned>(grid), bwd::NUM_THREADS, smem, stream>>>(
-            tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, p.scale,
+            tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, HC, p.scale,
             scale_log2, status);
     } else {
         auto kern = bwd::bwd_main_kernel<128, false>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         kern<<<static_cast<unsigned>(grid), bwd::NUM_THREADS, smem, stream>>>(
-            tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, p.scale,
+            tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, HC, p.scale,
             scale_log2, status);
     }
     return cudaGetLastError();
@@ -465,7 +513,7 @@ cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const
 cudaError_t launch_bwd_dq_convert_bf16(const Problem &p, const float *dQacc, void *dQ,
                                        cudaStream_t stream) {
     const long long n8 = static_cast<long long>(p.B) * p.Hq * p.N * p.d / 8;
-    const int grid = bwd::grid_for(n8, 256, bwd::sm_count());
+    const int grid = bwd::grid_for(n8, 256, num_sms());
     bwd::bwd_dq_convert_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4 *>(dQacc),
                                                          static_cast<uint4 *>(dQ), n8);
     return cudaGetLastError();

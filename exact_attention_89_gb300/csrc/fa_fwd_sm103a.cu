@@ -23,6 +23,7 @@
 // units), so p <= 2^8; the shift cancels in O = u / l, so the result is unchanged.
 // O is divided by the sum of the bf16-rounded weights that entered P V (so the applied weights
 // sum to one); LSE uses the sum of the unrounded fp32 weights.
+#include <algorithm>
 #include <cmath>
 
 #include "fa_internal.h"
@@ -71,8 +72,8 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-               float *__restrict__ LSE, int Hq, int Hkv, int N, int BH, float scale_log2,
-               unsigned *status) {
+               float *__restrict__ LSE, int Hq, int Hkv, int N, int BH, int HC,
+               float scale_log2, unsigned *status) {
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -91,11 +92,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // Work item: (query-tile pair, batch*head).  Under causal masking the late (heavy) pairs go
-    // first so the tail of the grid holds the short ones.
+    // Work item: (query-tile pair, batch*head).  Heads go in chunks of HC (about one wave of
+    // CTAs), so the K/V of the heads in flight stay in L2; inside a chunk the late (heavy under
+    // causal masking) pairs go first.
     const int n_pairs = (N + 2 * BM - 1) / (2 * BM);
-    const int bh = blockIdx.x % BH;
-    int pair = blockIdx.x / BH;
+    const int chunk = blockIdx.x / (HC * n_pairs);
+    const int in_chunk = blockIdx.x - chunk * HC * n_pairs;
+    const int hc = min(HC, BH - chunk * HC);
+    const int bh = chunk * HC + in_chunk % hc;
+    int pair = in_chunk / hc;
     if (CAUSAL) pair = n_pairs - 1 - pair;
     const int hq = bh % Hq, b = bh / Hq;
     const int bkv = b * Hkv + hq / (Hq / Hkv);
@@ -269,9 +274,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if ((CAUSAL && key > r) || key >= N) s[c] = -INFINITY;
                 }
             }
-            float mx = s[0];
+            // row max as a shallow tree of 3-input maxes (8 independent chains)
+            float m8[8];
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+            for (int k = 0; k < 8; ++k) m8[k] = fmax3(s[k], s[k + 8], s[k + 16]);
+#pragma unroll
+            for (int i = 24; i < 120; i += 16)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m8[k] = fmax3(m8[k], s[i + k], s[i + 8 + k]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], s[120 + k]);
+            const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                                   fmaxf(m8[6], m8[7]));
             const float m_blk = mx * scale_log2;
             const bool need = m_blk > m + RESCALE_THRESHOLD;
             if (__any_sync(0xffffffffu, need)) {
@@ -284,19 +298,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (j > 0) rescale_o_row<D>(tO, alpha);
             }
             const float m_sub = (m == -INFINITY) ? 0.f : m;
-            float sum = 0.f, sum_r = 0.f;
+            // p = 2^(s c - m) on pairs: one packed FMA, two ex2, packed sums in 4 chains
+            const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+            const uint64_t nm2 = f2_pack(-m_sub, -m_sub);
+            uint64_t acc[4], accr[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[k] = accr[k] = 0ull;
             uint32_t p[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                const float p0 = ex2_approx(fmaf(s[2 * c], scale_log2, -m_sub));
-                const float p1 = ex2_approx(fmaf(s[2 * c + 1], scale_log2, -m_sub));
-                sum += p0 + p1;
+                const float2 x = f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), c2, nm2));
+                const float p0 = ex2_approx(x.x);
+                const float p1 = ex2_approx(x.y);
+                acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
                 const uint32_t pk = pack_bf16x2(p0, p1);
                 p[c] = pk;
-                sum_r += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xffff0000u);
+                accr[c & 3] = f2_add(accr[c & 3], f2_pack(__uint_as_float(pk << 16),
+                                                          __uint_as_float(pk & 0xffff0000u)));
             }
-            l += sum;
-            lr += sum_r;
+            {
+                const float2 a = f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])));
+                const float2 r2 = f2_unpack(f2_add(f2_add(accr[0], accr[1]), f2_add(accr[2], accr[3])));
+                l += a.x + a.y;
+                lr += r2.x + r2.y;
+            }
             tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
             tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
             tmem_wait_st();
@@ -359,8 +384,9 @@ cudaError_t launch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &
     const long long grid = n_pairs * BH;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
+    const int HC = static_cast<int>(std::max<long long>(1, std::min<long long>(BH, num_sms() / n_pairs)));
     kern<<<static_cast<unsigned>(grid), NUM_THREADS, smem, stream>>>(
-        tmQ, tmK, tmV, tmO, LSE, p.Hq, p.Hkv, p.N, BH, scale_log2, status);
+        tmQ, tmK, tmV, tmO, LSE, p.Hq, p.Hkv, p.N, BH, HC, scale_log2, status);
     return cudaGetLastError();
 }
 

@@ -8,6 +8,9 @@
 
 namespace fa {
 
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
 // Problem description after host validation.
 struct Problem {
     int B, Hq, Hkv, N, d, causal;
