@@ -25,7 +25,8 @@
 // the tensor core's work on the other.  Inside a buffer, P^T and dS^T (bf16) are both written over
 // the S^T half, which frees the dP^T half for the dQ^T product of the same step.
 //
-// Roles (320 threads): warps 0-3 softmax-gradient, warps 4-7 dQ drain, warp 8 TMA, warp 9 MMA.
+// Roles (384 threads): warps 0-3 softmax-gradient, warps 4-7 dQ drain, warp 8 TMA, warp 9 MMA,
+// warps 10-11 idle (they complete the third warpgroup for the register split).
 // TMEM (512 columns): dK [0,128), dV [128,256), buffer b at 256 + 128 b:
 //   [+0,+64) S^T -> P^T [+0,+32) and dS^T [+32,+64);  [+64,+128) dP^T -> dQ^T.
 #include <algorithm>
@@ -40,9 +41,12 @@ namespace bwd {
 constexpr int BKV = 128;          // keys per CTA (= TMEM lanes)
 constexpr int BQ = 64;            // query rows per step
 constexpr int NSQ = 3;            // Q / dO ring stages
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 384;   // three warpgroups
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
+// Register split: softmax-gradient warpgroup grows; dQ drain and TMA/MMA warpgroups shrink.
+constexpr uint32_t REGS_GRAD = 256, REGS_DRAIN = 104, REGS_OTHER = 40;
+constexpr int REGS_NEEDED = 128 * (REGS_GRAD + REGS_DRAIN + REGS_OTHER);
 constexpr float LOG2E = 1.4426950408889634f;
 
 template <int D>
@@ -146,7 +150,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == WARP_TMA) {
+    // Each role branch starts with its register budget and ends with its own copy of the final
+    // barrier, so no code is shared between budgets.
+    if (warp >= 8) {
+        regs_dec<REGS_OTHER>();
+      if (warp == WARP_TMA) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
@@ -223,6 +231,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (!mbar_wait(&p_full[bsel], (s >> 1) & 1, abort_flag, status)) break;
                 tc_fence_after();
+                // dQ^T = K^T dS^T first (A = K MN-major, B = dS^T MN-major, K dim = 128 keys), so
+                // the drain warps read it out while dV / dK run and buffer s&1 frees up early.
+                const uint32_t dsb = ds_base + bsel * L::DS_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BKV / 16; ++kk)
+                    mma_ss(buf + B_DQT, sdesc_sw128(k_base + kk * 2048, L::KV_CHUNK, 1024),
+                           sdesc_sw128(dsb + kk * 2048, L::DS_BYTES, 1024), IDESC_DQ, kk > 0);
+                mma_commit(&dq_full[bsel]);
                 const uint32_t q_base = qring(s), do_base = q_base + L::Q_BYTES;
                 // dV += P^T dO ; dK += dS^T Q   (B operands MN-major: d contiguous)
 #pragma unroll
@@ -236,19 +252,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                            sdesc_sw128(q_base + kk * 2048, L::Q_CHUNK, 1024), IDESC_KV,
                            (s > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&q_empty[s % NSQ]);
-                // dQ^T = K^T dS^T  (A = K MN-major, B = dS^T MN-major, K dim = 128 keys)
-                const uint32_t dsb = ds_base + bsel * L::DS_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < BKV / 16; ++kk)
-                    mma_ss(buf + B_DQT, sdesc_sw128(k_base + kk * 2048, L::KV_CHUNK, 1024),
-                           sdesc_sw128(dsb + kk * 2048, L::DS_BYTES, 1024), IDESC_DQ, kk > 0);
-                mma_commit(&dq_full[bsel]);
             }
             mma_commit(acc_full);
             mma_commit(mma_done);
             mbar_drain(mma_done, 0);
         }
+      }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == WARP_MMA) {
+            __syncwarp();
+            tc_fence_after();
+            tmem_dealloc(tmem, 512);
+        }
     } else if (warp < 4) {
+        regs_inc<REGS_GRAD>();
         // ------------------------------------------------------------------ P^T / dS^T warps
         const int krow = warp * 32 + lane;          // key row within the block = TMEM lane
         const int key = jb * BKV + krow;
@@ -278,42 +296,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             named_barrier_sync(1, 128);
             if (ok) {
                 tc_fence_after();
-                uint32_t sr[64], dr[64];
+                // P^T in place over the S^T registers, then dS^T with dP^T streamed in halves
+                uint32_t sr[64];
                 tmem_ld_x64(buf + B_ST, sr);
-                tmem_ld_x64(buf + B_DPT, dr);
                 const bool need_mask = (CAUSAL && q0 < jb * BKV + BKV) || (q0 + BQ > N) ||
                                        (jb * BKV + BKV > N);
                 const float4 *l4 = reinterpret_cast<const float4 *>(sbuf);
                 const float4 *d4 = reinterpret_cast<const float4 *>(sbuf + BQ);
-                uint32_t pp[32], dd[32];
+                float pf[64];
 #pragma unroll
                 for (int c = 0; c < BQ; c += 4) {
                     const float4 lse = l4[c >> 2];
-                    const float4 dv = d4[c >> 2];
-                    float2 pa = f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
-                                                 c2, f2_pack(-lse.x, -lse.y)));
-                    float2 pb = f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])),
-                                                 c2, f2_pack(-lse.z, -lse.w)));
-                    pa.x = ex2_approx(pa.x);
-                    pa.y = ex2_approx(pa.y);
-                    pb.x = ex2_approx(pb.x);
-                    pb.y = ex2_approx(pb.y);
-                    if (need_mask) {
+                    const float2 pa = f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                                                       c2, f2_pack(-lse.x, -lse.y)));
+                    const float2 pb = f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])),
+                                                       c2, f2_pack(-lse.z, -lse.w)));
+                    pf[c] = ex2_approx(pa.x);
+                    pf[c + 1] = ex2_approx(pa.y);
+                    pf[c + 2] = ex2_approx(pb.x);
+                    pf[c + 3] = ex2_approx(pb.y);
+                }
+                if (need_mask) {
+#pragma unroll
+                    for (int c = 0; c < BQ; ++c) {
                         const int q = q0 + c;
-                        if ((CAUSAL && key > q) || q >= N || key >= N) pa.x = 0.f;
-                        if ((CAUSAL && key > q + 1) || q + 1 >= N || key >= N) pa.y = 0.f;
-                        if ((CAUSAL && key > q + 2) || q + 2 >= N || key >= N) pb.x = 0.f;
-                        if ((CAUSAL && key > q + 3) || q + 3 >= N || key >= N) pb.y = 0.f;
+                        if ((CAUSAL && key > q) || q >= N || key >= N) pf[c] = 0.f;
                     }
-                    const uint64_t pa2 = f2_pack(pa.x, pa.y), pb2 = f2_pack(pb.x, pb.y);
-                    const float2 da = f2_unpack(f2_mul(pa2, f2_add(
-                        f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), f2_pack(-dv.x, -dv.y))));
-                    const float2 db = f2_unpack(f2_mul(pb2, f2_add(
-                        f2_pack(__uint_as_float(dr[c + 2]), __uint_as_float(dr[c + 3])), f2_pack(-dv.z, -dv.w))));
-                    pp[c >> 1] = pack_bf16x2(pa.x, pa.y);
-                    pp[(c >> 1) + 1] = pack_bf16x2(pb.x, pb.y);
-                    dd[c >> 1] = pack_bf16x2(da.x, da.y);
-                    dd[(c >> 1) + 1] = pack_bf16x2(db.x, db.y);
+                }
+                uint32_t pp[32], dd[32];
+#pragma unroll
+                for (int c = 0; c < BQ; c += 2) pp[c >> 1] = pack_bf16x2(pf[c], pf[c + 1]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t dr[32];
+                    tmem_ld_x32(buf + B_DPT + 32 * h, dr);
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 dv = d4[(32 * h + c) >> 2];
+                        const float2 da = f2_unpack(f2_mul(
+                            f2_pack(pf[32 * h + c], pf[32 * h + c + 1]),
+                            f2_add(f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])),
+                                   f2_pack(-dv.x, -dv.y))));
+                        const float2 db = f2_unpack(f2_mul(
+                            f2_pack(pf[32 * h + c + 2], pf[32 * h + c + 3]),
+                            f2_add(f2_pack(__uint_as_float(dr[c + 2]), __uint_as_float(dr[c + 3])),
+                                   f2_pack(-dv.z, -dv.w))));
+                        dd[(32 * h + c) >> 1] = pack_bf16x2(da.x, da.y);
+                        dd[((32 * h + c) >> 1) + 1] = pack_bf16x2(db.x, db.y);
+                    }
                 }
                 tmem_st_x32(buf + B_PT, pp);
                 tmem_st_x32(buf + B_DST, dd);
@@ -366,7 +396,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tma_store_commit_and_wait_read();
             }
         }
-    } else if (warp < 8) {
+        tc_fence_before();
+        __syncthreads();
+    } else {
+        regs_dec<REGS_DRAIN>();
         // ------------------------------------------------------------------ dQ drain warps
         const int wq = warp - 4;
         const int dcol = wq * 32 + lane;            // column of dQ = TMEM lane of dQ^T
@@ -388,14 +421,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int c = 0; c < BQ; ++c)
                 if (c < nvalid) atomicAdd(dst + static_cast<size_t>(c) * D, __uint_as_float(a[c]) * scale);
         }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == WARP_MMA) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tc_fence_before();
+        __syncthreads();
     }
 }
 
@@ -492,10 +519,14 @@ cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const
     const int smem = bwd::Layout<128>::BYTES;
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     cudaError_t e;
+    cudaFuncAttributes attr{};
     if (p.causal) {
         auto kern = bwd::bwd_main_kernel<128, true>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
+        // the in-kernel register split needs at least REGS_NEEDED registers at launch
+        if ((e = cudaFuncGetAttributes(&attr, kern)) != cudaSuccess) return e;
+        if (attr.numRegs * bwd::NUM_THREADS < bwd::REGS_NEEDED) return cudaErrorInvalidConfiguration;
         kern<<<static_cast<unsigned>(grid), bwd::NUM_THREADS, smem, stream>>>(
             tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, HC, p.scale,
             scale_log2, status);
@@ -503,6 +534,8 @@ cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const
         auto kern = bwd::bwd_main_kernel<128, false>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
+        if ((e = cudaFuncGetAttributes(&attr, kern)) != cudaSuccess) return e;
+        if (attr.numRegs * bwd::NUM_THREADS < bwd::REGS_NEEDED) return cudaErrorInvalidConfiguration;
         kern<<<static_cast<unsigned>(grid), bwd::NUM_THREADS, smem, stream>>>(
             tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, HC, p.scale,
             scale_log2, status);

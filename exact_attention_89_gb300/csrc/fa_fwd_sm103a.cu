@@ -10,11 +10,12 @@
 // the sequence.  LSE = m + ln l is stored for the backward pass (mzeromiko blog, end of the
 // "blocked form with online-softmax rescaling" section: logsumexp placement).
 //
-// GB300 mapping (one CTA = two 128-row query tiles of one (batch, head), 320 threads):
+// GB300 mapping (one CTA = two 128-row query tiles of one (batch, head), 384 threads):
 //   warps 0-3 : softmax for query tile 0  (thread = query row = TMEM lane)
 //   warps 4-7 : softmax for query tile 1
 //   warp 8    : TMA producer (Q tiles once, then K_j / V_j through a 4-stage ring)
 //   warp 9    : TMEM allocator and single-thread tcgen05.mma issuer
+//   warps 10-11 complete the third warpgroup so its registers can be handed to the softmax.
 // TMEM (512 columns): S/P of tile t at columns 128 t, O of tile t at 256 + 128 t.
 // S = Q K_j^T runs as SS MMAs (both operands K-major in 128B-swizzled smem); P is written back
 // over S as packed bf16 and O += P V_j runs as a TS MMA (P from TMEM, V MN-major in smem).
@@ -35,9 +36,12 @@ namespace fwd {
 constexpr int BM = 128;           // query rows per tile (= TMEM lanes)
 constexpr int BN = 128;           // keys per block
 constexpr int NS = 4;             // K/V ring stages
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 384;   // three warpgroups
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
+// Register split: softmax warpgroups 0 and 1 grow, warpgroup 2 (TMA, MMA, two idle warps) shrinks.
+constexpr uint32_t REGS_SOFTMAX = 216, REGS_OTHER = 40;
+constexpr int REGS_NEEDED = 2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER;
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr float LN2 = 0.693147180559945309f;
 
@@ -143,7 +147,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == WARP_TMA) {
+    // Each role branch starts with its register budget and ends with its own copy of the final
+    // barrier, so no code is shared between budgets.
+    if (warp >= 8) {
+        regs_dec<REGS_OTHER>();
+      if (warp == WARP_TMA) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
@@ -242,7 +250,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mma_commit(mma_done);
             mbar_drain(mma_done, 0);
         }
+      }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == WARP_MMA) {
+            __syncwarp();
+            tc_fence_after();
+            tmem_dealloc(tmem, 512);
+        }
     } else {
+        regs_inc<REGS_SOFTMAX>();
         // ------------------------------------------------------------------ softmax warps
         const int t = warp >> 2, wq = warp & 3;
         const int row = wq * 32 + lane;             // row within the tile = TMEM lane
@@ -360,14 +377,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tma_store_commit_and_wait_read();
             }
         }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == WARP_MMA) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tc_fence_before();
+        __syncthreads();
     }
 }
 
@@ -379,6 +390,11 @@ cudaError_t launch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &
     const int smem = Layout<D>::BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // The in-kernel register split needs the launch to provide at least REGS_NEEDED registers.
+    cudaFuncAttributes attr{};
+    e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs * NUM_THREADS < REGS_NEEDED) return cudaErrorInvalidConfiguration;
     const int BH = p.B * p.Hq;
     const long long n_pairs = (p.N + 2 * BM - 1) / (2 * BM);
     const long long grid = n_pairs * BH;

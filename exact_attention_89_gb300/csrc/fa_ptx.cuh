@@ -221,6 +221,18 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Per-warpgroup register budget changes.  Every warp of a warpgroup must execute the same
+// one; the sum over warpgroups must stay within threads x registers-at-launch (checked on the
+// host before every launch of a kernel that uses them).
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+
 // Blackwell packed fp32 pairs (one instruction for two lanes of work).
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
     uint64_t r;
