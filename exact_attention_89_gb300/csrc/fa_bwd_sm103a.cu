@@ -45,7 +45,7 @@ constexpr int NUM_THREADS = 384;   // three warpgroups
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
 // Register split: softmax-gradient warpgroup grows; dQ drain and TMA/MMA warpgroups shrink.
-constexpr uint32_t REGS_GRAD = 256, REGS_DRAIN = 104, REGS_OTHER = 40;
+constexpr uint32_t REGS_GRAD = 256, REGS_DRAIN = 104, REGS_OTHER = 64;
 constexpr int REGS_NEEDED = 128 * (REGS_GRAD + REGS_DRAIN + REGS_OTHER);
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -191,27 +191,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             constexpr uint32_t IDESC_SP = idesc_bf16(BKV, BQ, false, false);   // S^T, dP^T
             constexpr uint32_t IDESC_KV = idesc_bf16(BKV, D, false, true);     // dV, dK
             constexpr uint32_t IDESC_DQ = idesc_bf16(D, BQ, true, true);       // dQ^T
-            const uint32_t k_base = smem_u32(smem + L::K_OFF);
-            const uint32_t v_base = smem_u32(smem + L::V_OFF);
-            const uint32_t ds_base = smem_u32(smem + L::DS_OFF);
-            auto qring = [&](int s) { return smem_u32(smem + L::QR_OFF + (s % NSQ) * 2 * L::Q_BYTES); };
+            // Descriptors are built once; each k-step only moves the start address.
+            const uint64_t dk_k = sdesc_sw128(smem_u32(smem + L::K_OFF), 16, 1024);        // K, K-major
+            const uint64_t dv_k = sdesc_sw128(smem_u32(smem + L::V_OFF), 16, 1024);        // V, K-major
+            const uint64_t dk_mn = sdesc_sw128(smem_u32(smem + L::K_OFF), L::KV_CHUNK, 1024);  // K, MN-major
+            const uint64_t dq_k = sdesc_sw128(smem_u32(smem + L::QR_OFF), 16, 1024);       // ring, K-major
+            const uint64_t dq_mn = sdesc_sw128(smem_u32(smem + L::QR_OFF), L::Q_CHUNK, 1024);  // ring, MN-major
+            const uint64_t dds = sdesc_sw128(smem_u32(smem + L::DS_OFF), L::DS_BYTES, 1024);   // dS^T
+            auto ring_off = [&](int s) { return static_cast<uint32_t>((s % NSQ) * 2 * L::Q_BYTES); };
             // S^T(s) and dP^T(s) into buffer s & 1
             auto issue_sp = [&](int s) {
-                const uint32_t q_base = qring(s), do_base = q_base + L::Q_BYTES;
+                const uint64_t dq = sdesc_add(dq_k, ring_off(s));
+                const uint64_t ddo = sdesc_add(dq, L::Q_BYTES);
                 const uint32_t buf = tmem + T_BUF + (s & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
-                    mma_ss(buf + B_ST, sdesc_sw128(k_base + oa, 16, 1024),
-                           sdesc_sw128(q_base + ob, 16, 1024), IDESC_SP, kk > 0);
+                    mma_ss(buf + B_ST, sdesc_add(dk_k, oa), sdesc_add(dq, ob), IDESC_SP, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
-                    mma_ss(buf + B_DPT, sdesc_sw128(v_base + oa, 16, 1024),
-                           sdesc_sw128(do_base + ob, 16, 1024), IDESC_SP, kk > 0);
+                    mma_ss(buf + B_DPT, sdesc_add(dv_k, oa), sdesc_add(ddo, ob), IDESC_SP, kk > 0);
                 }
                 mma_commit(&s_full[s & 1]);
             };
@@ -233,23 +236,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 // dQ^T = K^T dS^T first (A = K MN-major, B = dS^T MN-major, K dim = 128 keys), so
                 // the drain warps read it out while dV / dK run and buffer s&1 frees up early.
-                const uint32_t dsb = ds_base + bsel * L::DS_BYTES;
+                const uint64_t dsb = sdesc_add(dds, bsel * L::DS_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < BKV / 16; ++kk)
-                    mma_ss(buf + B_DQT, sdesc_sw128(k_base + kk * 2048, L::KV_CHUNK, 1024),
-                           sdesc_sw128(dsb + kk * 2048, L::DS_BYTES, 1024), IDESC_DQ, kk > 0);
+                    mma_ss(buf + B_DQT, sdesc_add(dk_mn, kk * 2048), sdesc_add(dsb, kk * 2048),
+                           IDESC_DQ, kk > 0);
                 mma_commit(&dq_full[bsel]);
-                const uint32_t q_base = qring(s), do_base = q_base + L::Q_BYTES;
+                const uint64_t dqm = sdesc_add(dq_mn, ring_off(s));
+                const uint64_t dom = sdesc_add(dqm, L::Q_BYTES);
                 // dV += P^T dO ; dK += dS^T Q   (B operands MN-major: d contiguous)
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + T_DV, buf + B_PT + kk * 8,
-                           sdesc_sw128(do_base + kk * 2048, L::Q_CHUNK, 1024), IDESC_KV,
+                    mma_ts(tmem + T_DV, buf + B_PT + kk * 8, sdesc_add(dom, kk * 2048), IDESC_KV,
                            (s > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + T_DK, buf + B_DST + kk * 8,
-                           sdesc_sw128(q_base + kk * 2048, L::Q_CHUNK, 1024), IDESC_KV,
+                    mma_ts(tmem + T_DK, buf + B_DST + kk * 8, sdesc_add(dqm, kk * 2048), IDESC_KV,
                            (s > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&q_empty[s % NSQ]);
             }
@@ -513,7 +515,9 @@ cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const
     if (p.d != 128) return cudaErrorInvalidValue;
     const int BHkv = p.B * p.Hkv;
     const long long nkb = (p.N + bwd::BKV - 1) / bwd::BKV;
-    const int HC = static_cast<int>(std::max<long long>(1, std::min<long long>(BHkv, num_sms() / nkb)));
+    // One chunk spans every KV head (key-block-major order): measured slightly faster than
+    // chunks of heads sized for L2 residency.
+    const int HC = BHkv;
     const long long grid = nkb * BHkv;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int smem = bwd::Layout<128>::BYTES;

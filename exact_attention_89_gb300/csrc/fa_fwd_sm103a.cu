@@ -40,7 +40,7 @@ constexpr int NUM_THREADS = 384;   // three warpgroups
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
 // Register split: softmax warpgroups 0 and 1 grow, warpgroup 2 (TMA, MMA, two idle warps) shrinks.
-constexpr uint32_t REGS_SOFTMAX = 216, REGS_OTHER = 40;
+constexpr uint32_t REGS_SOFTMAX = 216, REGS_OTHER = 64;
 constexpr int REGS_NEEDED = 2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER;
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr float LN2 = 0.693147180559945309f;
@@ -190,26 +190,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false, false);
             constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, false, true);
-            const uint32_t q_base = smem_u32(smem + L::Q_OFF);
-            const uint32_t kv_base = smem_u32(smem + L::KV_OFF);
+            // Descriptors are built once; each k-step only moves the start address.
+            const uint64_t dq0 = sdesc_sw128(smem_u32(smem + L::Q_OFF), 16, 1024);
+            const uint64_t dkv0 = sdesc_sw128(smem_u32(smem + L::KV_OFF), 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(smem_u32(smem + L::KV_OFF), L::CHUNK_BYTES, 1024);
             auto issue_s = [&](int t, int st) {
-                const uint32_t qa = q_base + t * L::TILE_BYTES;
-                const uint32_t ka = kv_base + st * L::TILE_BYTES;
+                const uint64_t da = sdesc_add(dq0, t * L::TILE_BYTES);
+                const uint64_t db = sdesc_add(dkv0, st * L::TILE_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * L::CHUNK_BYTES + (kk & 3) * 32;
-                    mma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024),
-                           sdesc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
+                    mma_ss(tmem + t * 128, sdesc_add(da, off), sdesc_add(db, off), IDESC_S, kk > 0);
                 }
                 mma_commit(&s_full[t]);
             };
             auto issue_pv = [&](int t, int st, int j) {
-                const uint32_t va = kv_base + st * L::TILE_BYTES;
+                const uint64_t db = sdesc_add(dv0, st * L::TILE_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                           sdesc_sw128(va + kk * 2048, L::CHUNK_BYTES, 1024), IDESC_PV,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, sdesc_add(db, kk * 2048),
+                           IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
                 if (j == nblk[t] - 1) mma_commit(&o_full[t]);
             };
             bool ok = mbar_wait(q_full, 0, abort_flag, status) &&
@@ -277,8 +277,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             uint32_t sraw[128];
-            tmem_ld_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(&sraw[0]));
-            tmem_ld_x64(tS + 64, *reinterpret_cast<uint32_t(*)[64]>(&sraw[64]));
+            tmem_ld_x128(tS, sraw);
             float s[128];
 #pragma unroll
             for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sraw[c]);
@@ -318,9 +317,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // p = 2^(s c - m) on pairs: one packed FMA, two ex2, packed sums in 4 chains
             const uint64_t c2 = f2_pack(scale_log2, scale_log2);
             const uint64_t nm2 = f2_pack(-m_sub, -m_sub);
-            uint64_t acc[4], accr[4];
+            uint64_t acc[4];
+            float accr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) acc[k] = accr[k] = 0ull;
+            for (int k = 0; k < 4; ++k) acc[k] = 0ull;
             uint32_t p[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
@@ -330,14 +330,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
                 const uint32_t pk = pack_bf16x2(p0, p1);
                 p[c] = pk;
-                accr[c & 3] = f2_add(accr[c & 3], f2_pack(__uint_as_float(pk << 16),
-                                                          __uint_as_float(pk & 0xffff0000u)));
+                accr[c & 3] = add_bf16_hi(add_bf16_lo(accr[c & 3], pk), pk);
             }
             {
                 const float2 a = f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])));
-                const float2 r2 = f2_unpack(f2_add(f2_add(accr[0], accr[1]), f2_add(accr[2], accr[3])));
                 l += a.x + a.y;
-                lr += r2.x + r2.y;
+                lr += (accr[0] + accr[1]) + (accr[2] + accr[3]);
             }
             tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
             tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
@@ -400,7 +398,9 @@ cudaError_t launch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &
     const long long grid = n_pairs * BH;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
-    const int HC = static_cast<int>(std::max<long long>(1, std::min<long long>(BH, num_sms() / n_pairs)));
+    // One chunk spans every head: the global longest-first order measured faster than chunks
+    // of heads sized for L2 residency (the K/V re-reads it causes stay below the HBM limit).
+    const int HC = BH;
     kern<<<static_cast<unsigned>(grid), NUM_THREADS, smem, stream>>>(
         tmQ, tmK, tmV, tmO, LSE, p.Hq, p.Hkv, p.N, BH, HC, scale_log2, status);
     return cudaGetLastError();
