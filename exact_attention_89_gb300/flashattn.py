@@ -6,7 +6,7 @@ fallback: if ``libflashattn.so`` is missing or the GPU is not sm_103, calls fail
 
 Low-level functions (same names and argument order as ``include/flashattn.h``):
     fa_fwd, fa_bwd, fa_bwd_workspace_bytes, fa_fwd_fp32, fa_bwd_fp32,
-    fa_get_device_status, fa_status_string
+    fa_get_device_status, fa_status_string, fa_bwd_noalloc
 Convenience wrappers that allocate outputs with torch:
     attention_forward, attention_backward
 """
@@ -32,7 +32,10 @@ FA_ERR_DEVICE_BOUNDS = 7
 
 # Every symbol include/flashattn.h declares.
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_fp32", "fa_bwd_fp32",
-            "fa_get_device_status", "fa_status_string")
+            "fa_get_device_status", "fa_status_string", "fa_bwd_noalloc")
+
+# Size of the fixed device scratch fa_bwd_noalloc uses (FA_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +72,8 @@ def lib() -> ctypes.CDLL:
             L.fa_get_device_status.restype = i
             L.fa_status_string.argtypes = [i]
             L.fa_status_string.restype = ctypes.c_char_p
+            L.fa_bwd_noalloc.argtypes = [vp] * 9 + dims + [vp]
+            L.fa_bwd_noalloc.restype = i
             _lib = L
     return _lib
 
@@ -121,6 +126,17 @@ def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, causal: bool, scale: float, workspac
                       _ptr(dK), _ptr(dV), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
                       _ptr(workspace), wbytes, _stream(stream))
     return _check(st, "fa_bwd", check)
+
+
+def fa_bwd_noalloc(Q, K, V, O, dO, LSE, dQ, dK, dV, causal: bool, scale: float, stream=None,
+                   check: bool = True) -> int:
+    """fa_bwd for callers that cannot allocate: the scratch is the library's own fixed array of
+    NOALLOC_SCRATCH_BYTES per device, shared by every call (calls must not overlap on the GPU)."""
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    st = lib().fa_bwd_noalloc(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ),
+                              _ptr(dK), _ptr(dV), B, Hq, Hkv, N, d, int(bool(causal)),
+                              float(scale), _stream(stream))
+    return _check(st, "fa_bwd_noalloc", check)
 
 
 def fa_fwd_fp32(Q, K, V, O, LSE, causal: bool, scale: float, stream=None, check: bool = True):

@@ -86,6 +86,34 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
                  void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Size of the fixed device scratch that fa_bwd_noalloc uses: 64 MiB.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * fa_bwd without a workspace argument, for callers that cannot allocate device memory where
+ * they run the backward (for example a plugin whose host framework owns every allocation and
+ * only passes in the input and output buffers, or a runtime that plans all memory up front and
+ * forbids allocation once it is serving).  The paper has no counterpart to this entry point;
+ * it exists only for those callers.
+ *   Arguments, layouts, results and errors are those of fa_bwd.  Instead of a workspace the
+ *   call uses a fixed array of FA_NOALLOC_SCRATCH_BYTES compiled into the library, which every
+ *   GPU that loads the library holds until the library is unloaded or the process exits.
+ *   Returns FA_ERR_WORKSPACE, before touching the GPU, when fa_bwd_workspace_bytes(B,Hq,N,d)
+ *   exceeds FA_NOALLOC_SCRATCH_BYTES (with d = 128 that is B*Hq*N above about 130,000 rows).
+ *   It calls no allocation routine.  The first call on a device looks up the array's device
+ *   address (cudaGetSymbolAddress, on the current device); make that first call before any
+ *   stream capture.
+ *   All calls on one device share the array.  Each call rewrites what it needs at its start,
+ *   so what an earlier call left there does not matter, but calls that overlap on the GPU
+ *   (other streams, other host threads) race on the array and give wrong results: order them.
+ */
+fa_status fa_bwd_noalloc(const void *Q, const void *K, const void *V, const void *O,
+                         const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                         int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                         cudaStream_t stream);
+
+/*
  * Forward in fp32 on the CUDA cores (no tensor cores), for checks that need fp32 accuracy.
  * Same shapes and semantics as fa_fwd with every tensor fp32; 1 <= d <= 128.
  */
