@@ -35,7 +35,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic per launch of the dominant launch sequence from one ncu capture, keyed by the
 # sha256 of the kernel sources it was taken on; reported as null once the sources change.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # fa_bwd on causal_n4096: bwd_main 1.920 GB read + 0.990 GB write, bwd_preprocess 0.210 GB,
+    # bwd_dq_convert 0.164 GB (profiles/bwd_main_kernel_causal_n4096.md)
+    "cfbbd584a7378bef": 3.28e9,
+}
 
 
 def kernel_sources_hash() -> str:
@@ -126,6 +130,27 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def replica_seed_offset(rank: int) -> int:
+    """Each rank runs its own replica of the workload on inputs seeded seed + rank."""
+    return rank
+
+
+def max_over_ranks(ms: float, ws: int, device) -> float:
+    """The slowest rank's time (ms); the process group's MAX reduction when ws > 1."""
+    if ws == 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(ws: int, flops_per_step: float, steps: int, max_ms: float) -> float:
+    """Weak scaling: every rank processes one full step per step, so the job does ws x the FLOPs."""
+    return ws * flops_per_step * steps / (max_ms * 1e-3) / 1e12
 
 
 def cpu_oracle_sample(w, budget_s: float, max_heads: int, inputs=None, first_group: int = 0):
@@ -232,7 +257,7 @@ def main():
     fa.lib()
 
     w = WORKLOADS[args.workload]
-    Qh, Kh, Vh, dOh = workload_inputs(w, seed_offset=rank)
+    Qh, Kh, Vh, dOh = workload_inputs(w, seed_offset=replica_seed_offset(rank))
     q, k, v, do = (t.to(dev) for t in (Qh, Kh, Vh, dOh))
     B, Hq, Hkv, N, d = w.B, w.Hq, w.Hkv, w.N, w.d
     O = torch.empty_like(q)
@@ -303,13 +328,10 @@ def main():
     total_ms = t_start.elapsed_time(t_end)
     fwd_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / args.steps
     bwd_ms = sum(b.elapsed_time(c) for _, b, c in ev) / args.steps
-    t_max = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    total_ms = float(t_max.item())
+    total_ms = max_over_ranks(total_ms, ws, dev)
 
     flops_step = w.flops_fwd() + (w.flops_bwd() if w.backward else 0.0)
-    value = ws * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(ws, flops_step, args.steps, total_ms)
 
     # ---------------------------------------------------------------- end to end (host buffers)
     pin = [t.pin_memory() for t in (Qh, Kh, Vh, dOh)]
@@ -338,11 +360,8 @@ def main():
         e_e.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e_s.elapsed_time(e_e)
-    t2 = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(t2, op=dist.ReduceOp.MAX)
-    e2e_ms = float(t2.item())
-    e2e_value = ws * flops_step * args.steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, ws, dev)
+    e2e_value = whole_job_tflops(ws, flops_step, args.steps, e2e_ms)
 
     # ---------------------------------------------------------------- roofline + cpu baseline
     peaks, peaks_src = load_peaks()
@@ -363,7 +382,7 @@ def main():
                 "bwd_ms": bwd_ms, "sources": src_hash}
     cpu = None
     if rank == 0 and ws == 1 and args.cpu_budget > 0 and not args.no_extras:
-        r = cpu_oracle_sample(w, args.cpu_budget, 8)
+        r = cpu_oracle_sample(w, args.cpu_budget, w.B * w.Hq)
         cpu = {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")}
 
     if rank == 0:

@@ -1,0 +1,66 @@
+"""Multi-rank logic of the benchmark on the CPU: two gloo processes.
+
+The attention path has no data-path exchange; N > 1 runs are replicas on their own seeded
+inputs, and the only collective is the MAX over ranks of the timed region.  These tests run
+those pieces with world_size 2 on the CPU."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, ws, port, out):
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(ws), LOCAL_RANK=str(rank))
+    import bench
+    from exact_attention_89_gb300.inputs import make_inputs
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    try:
+        got_ws, got_rank, _ = bench.dist_env()
+        ms = 10.0 + 5.0 * rank                       # rank 1 is the slow one
+        mx = bench.max_over_ranks(ms, got_ws, torch.device("cpu"))
+        q, _, _, _ = make_inputs(1, 2, 1, 16, 8, seed=7 + bench.replica_seed_offset(got_rank))
+        val = bench.whole_job_tflops(got_ws, 1e12, 10, mx)
+        out[rank] = (got_ws, got_rank, mx, float(q.float().sum()), val)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_replicas_and_max_timing():
+    ws = 2
+    port = _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_worker, args=(ws, port, out), nprocs=ws, join=True)
+    r0, r1 = out[0], out[1]
+    assert (r0[0], r0[1]) == (2, 0) and (r1[0], r1[1]) == (2, 1)
+    # every rank sees the slowest rank's time
+    assert r0[2] == r1[2] == 15.0
+    # replicas draw different inputs, deterministically
+    assert r0[3] != r1[3]
+    from exact_attention_89_gb300.inputs import make_inputs
+    assert float(make_inputs(1, 2, 1, 16, 8, seed=8)[0].float().sum()) == r1[3]
+    # whole-job value: 2 ranks x 10 steps x 1 TFLOP in 15 ms
+    assert abs(r0[4] - 2 * 10 * 1e12 / 15e-3 / 1e12) < 1e-9
+
+
+def test_single_rank_helpers():
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5, 1, None) == 3.5
+    assert bench.replica_seed_offset(3) == 3
+    assert abs(bench.whole_job_tflops(1, 2e12, 4, 8.0) - 1000.0) < 1e-9
