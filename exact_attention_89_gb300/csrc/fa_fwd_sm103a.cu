@@ -22,8 +22,9 @@
 // The MMA order S0(j+1) after PV0(j) lets softmax of one tile overlap the other tile's MMAs.
 // Rescaling of O is lazy: the stale max is kept until the block max exceeds it by 8 (log2
 // units), so p <= 2^8; the shift cancels in O = u / l, so the result is unchanged.
-// O is divided by the sum of the bf16-rounded weights that entered P V (so the applied weights
-// sum to one); LSE uses the sum of the unrounded fp32 weights.
+// O is divided by the sum of the fp32 weights plus the rounding residual of each block's largest
+// bf16 weight (when one weight dominates, the weights P V applies then sum to one); LSE uses the
+// sum of the fp32 weights alone.
 #include <algorithm>
 #include <cmath>
 
@@ -268,9 +269,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t tS = tmem + lane_off + t * 128;
         const uint32_t tO = tmem + lane_off + 256 + t * 128;
         const int nb = nblk[t];
-        // l: sum of the fp32 weights (gives LSE); lr: sum of the bf16-rounded weights that the
-        // P V product actually uses (normalises O, so the weights applied sum to one).
-        float m = -INFINITY, l = 0.f, lr = 0.f;
+        // l: sum of the fp32 weights (gives LSE).  lc: rounding residual bf16(p) - p of each
+        // block's largest weight, the dominant part of (sum of the bf16 weights that P V applies)
+        // - l; O is divided by l + lc so the applied weights sum to one when one weight dominates.
+        float m = -INFINITY, l = 0.f, lc = 0.f;
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_flag, status));
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float alpha = need ? ex2_approx(m - m_blk) : 1.f;
                 if (need) {
                     l *= alpha;
-                    lr *= alpha;
+                    lc *= alpha;
                     m = m_blk;
                 }
                 if (j > 0) rescale_o_row<D>(tO, alpha);
@@ -318,7 +320,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t c2 = f2_pack(scale_log2, scale_log2);
             const uint64_t nm2 = f2_pack(-m_sub, -m_sub);
             uint64_t acc[4];
-            float accr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < 4; ++k) acc[k] = 0ull;
             uint32_t p[64];
@@ -328,14 +329,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float p0 = ex2_approx(x.x);
                 const float p1 = ex2_approx(x.y);
                 acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
-                const uint32_t pk = pack_bf16x2(p0, p1);
-                p[c] = pk;
-                accr[c & 3] = add_bf16_hi(add_bf16_lo(accr[c & 3], pk), pk);
+                p[c] = pack_bf16x2(p0, p1);
             }
             {
                 const float2 a = f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])));
                 l += a.x + a.y;
-                lr += (accr[0] + accr[1]) + (accr[2] + accr[3]);
+                // the block's largest weight is computed exactly as its element was above
+                const float ptop = ex2_approx(fmaf(mx, scale_log2, -m_sub));
+                lc += __bfloat162float(__float2bfloat16_rn(ptop)) - ptop;
             }
             tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
             tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // Every MMA reading Q tile t has completed, so its smem becomes the O staging tile,
             // in the same 128B-swizzled layout the TMA store expects.
             uint8_t *stage = smem + L::Q_OFF + t * L::TILE_BYTES;
-            const float inv_l = 1.f / lr;
+            const float inv_l = 1.f / (l + lc);
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];

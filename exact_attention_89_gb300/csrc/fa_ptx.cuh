@@ -276,18 +276,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-// acc + (float)bf16, exact conversion then one round-to-nearest add.
-__device__ __forceinline__ float add_bf16_lo(float acc, uint32_t pk) {
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %0;\n\t}"
-        : "+f"(acc) : "r"(pk));
-    return acc;
-}
-__device__ __forceinline__ float add_bf16_hi(float acc, uint32_t pk) {
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, hi, %0;\n\t}"
-        : "+f"(acc) : "r"(pk));
-    return acc;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
