@@ -15,19 +15,18 @@
 //   P^T = exp2(S^T c - LSE log2 e), dS^T = P^T (dP^T - D)   (thread = key row = TMEM lane)
 //   dV += P^T dO,  dK += dS^T Q          (TS MMAs: P^T / dS^T as bf16 in TMEM)
 //   dQ^T = K^T dS^T                      (SS MMA, M = d = 128, dS^T staged in smem)
-// and the warpgroup that computed the step then reduces scale * dQ^T into the fp32 accumulator
-// with coalesced fp32 reductions (thread = one column d of dQ).  K4 rounds it to bf16.
+// and a second warpgroup reduces scale * dQ^T into the fp32 accumulator with coalesced
+// fp32 reductions (thread = one column d of dQ).  K4 rounds the accumulator to bf16.
 // dQ strategy: recomputing S and dP in a separate dQ kernel would cost 7 products per tile
 // instead of 5 (+40% tensor work); the reduction costs L2 bandwidth instead.
 //
 // Software pipeline: S^T / dP^T are double-buffered in TMEM, so the products of step s+1 are
-// issued before those that consume step s, and two softmax-gradient warpgroups take alternate
-// steps, so gradient work, dQ drains and the tensor core overlap.  Inside a buffer, P^T and dS^T (bf16) are both written over
+// issued before those that consume step s, and the softmax-gradient warps of one step overlap
+// the tensor core's work on the other.  Inside a buffer, P^T and dS^T (bf16) are both written over
 // the S^T half, which frees the dP^T half for the dQ^T product of the same step.
 //
-// Roles (384 threads): warpgroups 0 and 1 (warps 0-7) compute P^T / dS^T for alternate steps and
-// drain their own step's dQ^T; warp 8 TMA, warp 9 MMA, warps 10-11 idle (they complete the third
-// warpgroup for the register split).
+// Roles (384 threads): warps 0-3 softmax-gradient, warps 4-7 dQ drain, warp 8 TMA, warp 9 MMA,
+// warps 10-11 idle (they complete the third warpgroup for the register split).
 // TMEM (512 columns): dK [0,128), dV [128,256), buffer b at 256 + 128 b:
 //   [+0,+64) S^T -> P^T [+0,+32) and dS^T [+32,+64);  [+64,+128) dP^T -> dQ^T.
 #include <algorithm>
@@ -45,9 +44,9 @@ constexpr int NSQ = 3;            // Q / dO ring stages
 constexpr int NUM_THREADS = 384;   // three warpgroups
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
-// Register split: the two softmax-gradient warpgroups grow, the TMA/MMA warpgroup shrinks.
-constexpr uint32_t REGS_GRAD = 216, REGS_OTHER = 64;
-constexpr int REGS_NEEDED = 128 * (2 * REGS_GRAD + REGS_OTHER);
+// Register split: softmax-gradient warpgroup grows; dQ drain and TMA/MMA warpgroups shrink.
+constexpr uint32_t REGS_GRAD = 256, REGS_DRAIN = 104, REGS_OTHER = 64;
+constexpr int REGS_NEEDED = 128 * (REGS_GRAD + REGS_DRAIN + REGS_OTHER);
 constexpr float LOG2E = 1.4426950408889634f;
 
 template <int D>
@@ -61,11 +60,11 @@ struct Layout {
     static constexpr int V_OFF = K_OFF + KV_BYTES;
     static constexpr int QR_OFF = V_OFF + KV_BYTES;        // ring: [stage][Q | dO]
     static constexpr int DS_OFF = QR_OFF + NSQ * 2 * Q_BYTES;  // [2][dS^T]
-    static constexpr int STAT_OFF = DS_OFF + 2 * DS_BYTES;     // [2 wg][2][lse2 64 | D 64] fp32
-    static constexpr int BAR_OFF = STAT_OFF + 2 * 2 * 2 * BQ * 4;
+    static constexpr int STAT_OFF = DS_OFF + 2 * DS_BYTES;     // [2][lse2 64 | D 64] fp32
+    static constexpr int BAR_OFF = STAT_OFF + 2 * 2 * BQ * 4;
     // kv_full, q_full[NSQ], q_empty[NSQ], s_full[2], p_full[2], dq_full[2], dq_empty[2],
-    // acc_full, epi[2], mma_done
-    static constexpr int NBARS = 1 + 2 * NSQ + 8 + 4;
+    // acc_full, epi, mma_done
+    static constexpr int NBARS = 1 + 2 * NSQ + 8 + 3;
     static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
     static constexpr int ABORT_OFF = TMEM_OFF + 8;
     static constexpr int BYTES = ABORT_OFF + 8 + 1024;
@@ -101,8 +100,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t *dq_full = p_full + 2;        // [2]
     uint64_t *dq_empty = dq_full + 2;      // [2]
     uint64_t *acc_full = dq_empty + 2;
-    uint64_t *epi = acc_full + 1;          // [2]
-    uint64_t *mma_done = epi + 2;
+    uint64_t *epi = acc_full + 1;
+    uint64_t *mma_done = epi + 1;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::TMEM_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ABORT_OFF);
     float *stat = reinterpret_cast<float *>(smem + L::STAT_OFF);
@@ -137,8 +136,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&dq_empty[k], 128);
         }
         mbar_init(acc_full, 1);
-        mbar_init(&epi[0], 128);
-        mbar_init(&epi[1], 128);
+        mbar_init(epi, 128);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -269,41 +267,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             tmem_dealloc(tmem, 512);
         }
-    } else {
+    } else if (warp < 4) {
         regs_inc<REGS_GRAD>();
-        // ---------------------------------------------------------- softmax-gradient warpgroups
-        // Warpgroup wg takes the steps s = wg, wg + 2, ... and with them TMEM buffer wg, dS^T
-        // buffer wg and, once the dQ^T product of its step is done, that step's dQ drain.  The two
-        // warpgroups alternate, so one computes while the other drains and waits.
-        const int wg = warp >> 2, wq = warp & 3;
-        const int krow = wq * 32 + lane;            // key row within the block = TMEM lane
+        // ------------------------------------------------------------------ P^T / dS^T warps
+        const int krow = warp * 32 + lane;          // key row within the block = TMEM lane
         const int key = jb * BKV + krow;
-        const int dcol = krow;                      // in the drain: column of dQ = TMEM lane of dQ^T
-        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
         const uint64_t c2 = f2_pack(scale_log2, scale_log2);
         bool ok = true;
-        for (int s = wg; s < T; s += 2) {
-            const int u = s >> 1;                   // use count of buffer wg
+        // Statistics of step s's query tile: thread t < 64 holds LSE_t * log2 e, t >= 64 holds
+        // D_{t-64}.  They are loaded one step ahead so the global-load latency overlaps a whole
+        // step instead of sitting between the MMAs and this step's work.
+        auto load_stat = [&](int s) -> float {
+            if (s >= T) return 0.f;
+            const int g = s / tiles_per_head, i = i0 + s % tiles_per_head;
+            const int bhq = b * Hq + hk * G + g;
+            const int q = i * BQ + (krow & (BQ - 1));
+            if (krow < BQ)
+                return (q < N) ? LSE[static_cast<size_t>(bhq) * N + q] * LOG2E : INFINITY;
+            return (q < N) ? Dvec[static_cast<size_t>(bhq) * N + q] : 0.f;
+        };
+        float v_next = load_stat(0);
+        for (int s = 0; s < T; ++s) {
             const int g = s / tiles_per_head, i = i0 + s % tiles_per_head;
             const int bhq = b * Hq + hk * G + g;
             const int q0 = i * BQ;
-            const int bsel = wg;
+            const int bsel = s & 1;
             const uint32_t buf = tmem + lane_off + T_BUF + bsel * 128;
-            float *sbuf = stat + (wg * 2 + (u & 1)) * 2 * BQ;
-            // statistics of this query tile: thread t < 64 loads LSE_t, t >= 64 loads D_{t-64};
-            // the global loads are in flight while the thread waits for the MMAs.
-            float v;
-            {
-                const int q = q0 + (krow & (BQ - 1));
-                if (krow < BQ)
-                    v = (q < N) ? LSE[static_cast<size_t>(bhq) * N + q] * LOG2E : INFINITY;
-                else
-                    v = (q < N) ? Dvec[static_cast<size_t>(bhq) * N + q] : 0.f;
-            }
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[bsel], u & 1, abort_flag, status));
+            float *sbuf = stat + bsel * 2 * BQ;
+            const float v = v_next;
+            v_next = load_stat(s + 1);
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[bsel], (s >> 1) & 1, abort_flag, status));
             sbuf[krow] = v;
             // executed by all four warps every step (even after a failed wait) so the counts match
-            named_barrier_sync(1 + wg, 128);
+            named_barrier_sync(1, 128);
             if (ok) {
                 tc_fence_after();
                 // P^T in place over the S^T registers, then dS^T with dP^T streamed in halves
@@ -358,63 +355,78 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_st_x32(buf + B_PT, pp);
                 tmem_st_x32(buf + B_DST, dd);
                 // dS^T row -> smem buffer (128B-swizzled, MN-major B operand of the dQ^T product)
-                uint8_t *ds_row = smem + L::DS_OFF + wg * L::DS_BYTES + krow * 128;
+                uint8_t *ds_row = smem + L::DS_OFF + bsel * L::DS_BYTES + krow * 128;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    uint4 w4 = make_uint4(dd[4 * k], dd[4 * k + 1], dd[4 * k + 2], dd[4 * k + 3]);
-                    *reinterpret_cast<uint4 *>(ds_row + ((k ^ (krow & 7)) << 4)) = w4;
+                for (int u = 0; u < 8; ++u) {
+                    uint4 w4 = make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+                    *reinterpret_cast<uint4 *>(ds_row + ((u ^ (krow & 7)) << 4)) = w4;
                 }
                 tmem_wait_st();
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(&p_full[bsel]);
             }
-            // dQ drain of this step: scale * dQ^T -> fp32 reductions into the accumulator
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[bsel], u & 1, abort_flag, status));
-            if (ok) {
-                tc_fence_after();
-                uint32_t a[64];
-                tmem_ld_x64(tmem + lane_off + T_BUF + bsel * 128 + B_DQT, a);
-                tc_fence_before();
-                mbar_arrive(&dq_empty[bsel]);
-                float *dst = dQacc + (static_cast<size_t>(bhq) * N + q0) * D + dcol;
-                const int nvalid = min(BQ, N - q0);
-#pragma unroll
-                for (int c = 0; c < BQ; ++c)
-                    if (c < nvalid) atomicAdd(dst + static_cast<size_t>(c) * D, __uint_as_float(a[c]) * scale);
-            }
         }
-        // epilogue: warpgroup 0 stores dK (scaled), warpgroup 1 dV: TMEM -> bf16 -> smem (over
-        // K / V, free once every product has completed) -> TMA store
+        // epilogue: dK (scaled) and dV rows -> bf16 -> smem (over K / V) -> TMA store
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, status));
         if (ok) {
             tc_fence_after();
-            const uint32_t tcol = wg ? T_DV : T_DK;
-            const float mul = wg ? 1.f : scale;
-            uint8_t *dst = smem + (wg ? L::V_OFF : L::K_OFF);
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t a[32];
-                tmem_ld_x32(tmem + lane_off + tcol + c0, a);
-                uint8_t *rowp = dst + (c0 / 64) * L::KV_CHUNK + krow * 128;
-                const int u0 = (c0 % 64) / 8;
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t tcol = which ? T_DV : T_DK;
+                const float mul = which ? 1.f : scale;
+                uint8_t *dst = smem + (which ? L::V_OFF : L::K_OFF);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint4 w4;
-                    w4.x = pack_bf16x2(__uint_as_float(a[8 * k + 0]) * mul, __uint_as_float(a[8 * k + 1]) * mul);
-                    w4.y = pack_bf16x2(__uint_as_float(a[8 * k + 2]) * mul, __uint_as_float(a[8 * k + 3]) * mul);
-                    w4.z = pack_bf16x2(__uint_as_float(a[8 * k + 4]) * mul, __uint_as_float(a[8 * k + 5]) * mul);
-                    w4.w = pack_bf16x2(__uint_as_float(a[8 * k + 6]) * mul, __uint_as_float(a[8 * k + 7]) * mul);
-                    *reinterpret_cast<uint4 *>(rowp + (((u0 + k) ^ (krow & 7)) << 4)) = w4;
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t a[32];
+                    tmem_ld_x32(tmem + lane_off + tcol + c0, a);
+                    uint8_t *rowp = dst + (c0 / 64) * L::KV_CHUNK + krow * 128;
+                    const int u0 = (c0 % 64) / 8;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        uint4 w4;
+                        w4.x = pack_bf16x2(__uint_as_float(a[8 * u + 0]) * mul, __uint_as_float(a[8 * u + 1]) * mul);
+                        w4.y = pack_bf16x2(__uint_as_float(a[8 * u + 2]) * mul, __uint_as_float(a[8 * u + 3]) * mul);
+                        w4.z = pack_bf16x2(__uint_as_float(a[8 * u + 4]) * mul, __uint_as_float(a[8 * u + 5]) * mul);
+                        w4.w = pack_bf16x2(__uint_as_float(a[8 * u + 6]) * mul, __uint_as_float(a[8 * u + 7]) * mul);
+                        *reinterpret_cast<uint4 *>(rowp + (((u0 + u) ^ (krow & 7)) << 4)) = w4;
+                    }
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(&epi[wg]);
-            if (krow == 0 && mbar_wait(&epi[wg], 0, abort_flag, status)) {
-                for (int ch = 0; ch < D / 64; ++ch)
-                    tma_store_3d(wg ? &tmdV : &tmdK, dst + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
+            mbar_arrive(epi);
+            if (krow == 0 && mbar_wait(epi, 0, abort_flag, status)) {
+                for (int ch = 0; ch < D / 64; ++ch) {
+                    tma_store_3d(&tmdK, smem + L::K_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
+                    tma_store_3d(&tmdV, smem + L::V_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
+                }
                 tma_store_commit_and_wait_read();
             }
+        }
+        tc_fence_before();
+        __syncthreads();
+    } else {
+        regs_dec<REGS_DRAIN>();
+        // ------------------------------------------------------------------ dQ drain warps
+        const int wq = warp - 4;
+        const int dcol = wq * 32 + lane;            // column of dQ = TMEM lane of dQ^T
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        for (int s = 0; s < T; ++s) {
+            const int g = s / tiles_per_head, i = i0 + s % tiles_per_head;
+            const int bhq = b * Hq + hk * G + g;
+            const int q0 = i * BQ;
+            const int bsel = s & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&dq_full[bsel], (s >> 1) & 1, abort_flag, status))) break;
+            tc_fence_after();
+            uint32_t a[64];
+            tmem_ld_x64(tmem + lane_off + T_BUF + bsel * 128 + B_DQT, a);
+            tc_fence_before();
+            mbar_arrive(&dq_empty[bsel]);
+            float *dst = dQacc + (static_cast<size_t>(bhq) * N + q0) * D + dcol;
+            const int nvalid = min(BQ, N - q0);
+#pragma unroll
+            for (int c = 0; c < BQ; ++c)
+                if (c < nvalid) atomicAdd(dst + static_cast<size_t>(c) * D, __uint_as_float(a[c]) * scale);
         }
         tc_fence_before();
         __syncthreads();
