@@ -149,13 +149,12 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
     fa::DeviceInfo *di = nullptr;
     if ((st = fa::current_device(&di, true)) != FA_OK) return st;
     const Problem p{B, Hq, Hkv, N, d, causal ? 1 : 0, scale};
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv;
     if (!fa::encode_bf16(&tq, Q, d, N, 1LL * B * Hq, 128) ||
         !fa::encode_bf16(&tk, K, d, N, 1LL * B * Hkv, 128) ||
-        !fa::encode_bf16(&tv, V, d, N, 1LL * B * Hkv, 128) ||
-        !fa::encode_bf16(&to, O, d, N, 1LL * B * Hq, 128))
+        !fa::encode_bf16(&tv, V, d, N, 1LL * B * Hkv, 128))
         return FA_ERR_CUDA;
-    return fa::from_cuda(fa::launch_fwd_bf16(p, tq, tk, tv, to, LSE, di->status, stream));
+    return fa::from_cuda(fa::launch_fwd_bf16(p, tq, tk, tv, O, LSE, di->status, stream));
 }
 
 fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,

@@ -10,7 +10,8 @@
 // the sequence.  LSE = m + ln l is stored for the backward pass (mzeromiko blog, end of the
 // "blocked form with online-softmax rescaling" section: logsumexp placement).
 //
-// GB300 mapping (one CTA = two 128-row query tiles of one (batch, head), 384 threads):
+// GB300 mapping: a persistent grid of one CTA per SM walks work items (two 128-row query tiles
+// of one (batch, head)), longest first, carrying every pipeline phase across items; 384 threads:
 //   warps 0-3 : softmax for query tile 0  (thread = query row = TMEM lane)
 //   warps 4-7 : softmax for query tile 1
 //   warp 8    : TMA producer (Q tiles once, then K_j / V_j through a 4-stage ring)
@@ -41,7 +42,7 @@ constexpr int NUM_THREADS = 384;   // three warpgroups
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
 // Register split: softmax warpgroups 0 and 1 grow, warpgroup 2 (TMA, MMA, two idle warps) shrinks.
-constexpr uint32_t REGS_SOFTMAX = 216, REGS_OTHER = 64;
+constexpr uint32_t REGS_SOFTMAX = 208, REGS_OTHER = 80;
 constexpr int REGS_NEEDED = 2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER;
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr float LN2 = 0.693147180559945309f;
@@ -53,8 +54,9 @@ struct Layout {
     static constexpr int Q_OFF = 0;
     static constexpr int KV_OFF = 2 * TILE_BYTES;
     static constexpr int BAR_OFF = KV_OFF + NS * TILE_BYTES;
-    // q_full, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_full[2], epi[2], mma_done
-    static constexpr int NBARS = 1 + 2 * NS + 2 + 2 + 2 + 2 + 1;
+    // q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_full[2], o_empty[2],
+    // mma_done
+    static constexpr int NBARS = 2 + 2 * NS + 2 + 2 + 2 + 2 + 1;
     static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
     static constexpr int ABORT_OFF = TMEM_OFF + 8;
     static constexpr int BYTES = ABORT_OFF + 8 + 1024;   // + slack for 1024-byte alignment
@@ -73,11 +75,49 @@ __device__ __forceinline__ void rescale_o_row(uint32_t tO, float alpha) {
     tmem_wait_st();
 }
 
+// One work item = two 128-row query tiles (a "pair") of one (batch, head).
+struct Item {
+    int bh, bkv, q0[2], nblk[2], nmax;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Item decode_item(int k, int Hq, int Hkv, int N, int BH) {
+    // Items are numbered longest-first: under causal masking the late pairs (most key blocks) of
+    // every head come first.
+    const int n_pairs = (N + 2 * BM - 1) / (2 * BM);
+    Item it;
+    it.bh = k % BH;
+    int pair = k / BH;
+    if (CAUSAL) pair = n_pairs - 1 - pair;
+    const int hq = it.bh % Hq, b = it.bh / Hq;
+    it.bkv = b * Hkv + hq / (Hq / Hkv);
+    const int nkb = (N + BN - 1) / BN;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        it.q0[t] = pair * 2 * BM + t * BM;
+        if (it.q0[t] >= N)
+            it.nblk[t] = 0;
+        else if (CAUSAL)
+            it.nblk[t] = min(nkb, (min(it.q0[t] + BM, N) - 1) / BN + 1);
+        else
+            it.nblk[t] = nkb;
+    }
+    it.nmax = max(it.nblk[0], it.nblk[1]);
+    return it;
+}
+
+// The r-th item of this CTA: rounds of gridDim.x items, assigned in snake order (reversed on odd
+// rounds) so every CTA gets a similar share of long and short items.
+__device__ __forceinline__ int item_index(int r) {
+    const int G = gridDim.x;
+    return r * G + ((r & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x));
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-               float *__restrict__ LSE, int Hq, int Hkv, int N, int BH, int HC,
+               const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
+               float *__restrict__ LSE, int Hq, int Hkv, int N, int BH, int n_items,
                float scale_log2, unsigned *status) {
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -85,46 +125,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
     uint64_t *q_full = bars;
-    uint64_t *kv_full = bars + 1;
+    uint64_t *q_empty = bars + 1;
+    uint64_t *kv_full = bars + 2;
     uint64_t *kv_empty = kv_full + NS;
-    uint64_t *s_full = kv_empty + NS;
-    uint64_t *p_full = s_full + 2;
-    uint64_t *o_full = p_full + 2;
-    uint64_t *epi = o_full + 2;
-    uint64_t *mma_done = epi + 2;
+    uint64_t *s_full = kv_empty + NS;   // [2]
+    uint64_t *p_full = s_full + 2;      // [2]
+    uint64_t *o_full = p_full + 2;      // [2]
+    uint64_t *o_empty = o_full + 2;     // [2]
+    uint64_t *mma_done = o_empty + 2;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::TMEM_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ABORT_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // Work item: (query-tile pair, batch*head).  Heads go in chunks of HC (about one wave of
-    // CTAs), so the K/V of the heads in flight stay in L2; inside a chunk the late (heavy under
-    // causal masking) pairs go first.
-    const int n_pairs = (N + 2 * BM - 1) / (2 * BM);
-    const int chunk = blockIdx.x / (HC * n_pairs);
-    const int in_chunk = blockIdx.x - chunk * HC * n_pairs;
-    const int hc = min(HC, BH - chunk * HC);
-    const int bh = chunk * HC + in_chunk % hc;
-    int pair = in_chunk / hc;
-    if (CAUSAL) pair = n_pairs - 1 - pair;
-    const int hq = bh % Hq, b = bh / Hq;
-    const int bkv = b * Hkv + hq / (Hq / Hkv);
-    const int nkb = (N + BN - 1) / BN;
-    int q0[2], nblk[2];
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        q0[t] = pair * 2 * BM + t * BM;
-        if (q0[t] >= N)
-            nblk[t] = 0;
-        else if (CAUSAL)
-            nblk[t] = min(nkb, (min(q0[t] + BM, N) - 1) / BN + 1);
-        else
-            nblk[t] = nkb;
-    }
-    const int nmax = max(nblk[0], nblk[1]);
+    // number of items this CTA processes
+    int n_mine = 0;
+    while (item_index(n_mine) < n_items) ++n_mine;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
@@ -133,7 +152,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&s_full[t], 1);
             mbar_init(&p_full[t], BM);
             mbar_init(&o_full[t], 1);
-            mbar_init(&epi[t], BM);
+            mbar_init(&o_empty[t], BM);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -158,35 +177,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            const int ntiles = nblk[1] > 0 ? 2 : 1;
-            mbar_arrive_expect_tx(q_full, ntiles * L::TILE_BYTES);
-            for (int t = 0; t < ntiles; ++t)
-                for (int ch = 0; ch < D / 64; ++ch)
-                    tma_load_3d(smem + L::Q_OFF + t * L::TILE_BYTES + ch * L::CHUNK_BYTES, &tmQ,
-                                ch * 64, q0[t], bh, q_full);
-            int issued = 0;
+            int base = 0, issued = 0;         // K/V ring index of the current item's K_0
+            int q_issued = 0;
             bool ok = true;
-            for (int idx = 0; idx < 2 * nmax && ok; ++idx) {
-                const int j = idx >> 1, st = idx % NS, rnd = idx / NS;
-                if (!mbar_wait(&kv_empty[st], (rnd & 1) ^ 1, abort_flag, status)) {
-                    ok = false;
-                    break;
+            for (int r = 0; r < n_mine && ok; ++r) {
+                const Item it = decode_item<CAUSAL>(item_index(r), Hq, Hkv, N, BH);
+                // Q buffer: free once every S product of the previous item has completed
+                if (r > 0 && !mbar_wait(q_empty, (r - 1) & 1, abort_flag, status)) { ok = false; break; }
+                const int ntiles = it.nblk[1] > 0 ? 2 : 1;
+                mbar_arrive_expect_tx(q_full, ntiles * L::TILE_BYTES);
+                ++q_issued;
+                for (int t = 0; t < ntiles; ++t)
+                    for (int ch = 0; ch < D / 64; ++ch)
+                        tma_load_3d(smem + L::Q_OFF + t * L::TILE_BYTES + ch * L::CHUNK_BYTES, &tmQ,
+                                    ch * 64, it.q0[t], it.bh, q_full);
+                for (int e = 0; e < 2 * it.nmax; ++e) {
+                    const int idx = base + e, j = e >> 1, st = idx % NS, rnd = idx / NS;
+                    if (!mbar_wait(&kv_empty[st], (rnd & 1) ^ 1, abort_flag, status)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&kv_full[st], L::TILE_BYTES);
+                    uint8_t *dst = smem + L::KV_OFF + st * L::TILE_BYTES;
+                    const CUtensorMap *tm = (e & 1) ? &tmV : &tmK;
+                    for (int ch = 0; ch < D / 64; ++ch)
+                        tma_load_3d(dst + ch * L::CHUNK_BYTES, tm, ch * 64, j * BN, it.bkv, &kv_full[st]);
+                    ++issued;
                 }
-                mbar_arrive_expect_tx(&kv_full[st], L::TILE_BYTES);
-                uint8_t *dst = smem + L::KV_OFF + st * L::TILE_BYTES;
-                const CUtensorMap *tm = (idx & 1) ? &tmV : &tmK;
-                for (int ch = 0; ch < D / 64; ++ch)
-                    tma_load_3d(dst + ch * L::CHUNK_BYTES, tm, ch * 64, j * BN, bkv, &kv_full[st]);
-                ++issued;
+                base += 2 * it.nmax;
             }
             if (!ok || *abort_flag) {
                 // Unwinding: let copies still in flight land before the CTA's smem goes away.
                 for (int idx = max(0, issued - NS); idx < issued; ++idx)
                     mbar_drain(&kv_full[idx % NS], (idx / NS) & 1);
-                mbar_drain(q_full, 0);
+                if (q_issued > 0) mbar_drain(q_full, (q_issued - 1) & 1);
             }
         }
-    } else if (warp == WARP_MMA) {
+      } else if (warp == WARP_MMA) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false, false);
@@ -211,41 +235,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int kk = 0; kk < BN / 16; ++kk)
                     mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, sdesc_add(db, kk * 2048),
                            IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-                if (j == nblk[t] - 1) mma_commit(&o_full[t]);
             };
-            bool ok = mbar_wait(q_full, 0, abort_flag, status) &&
-                      mbar_wait(&kv_full[0], 0, abort_flag, status);
-            tc_fence_after();
-            if (ok) {
+            int base = 0;                       // K/V ring index of the current item's K_0
+            int pb[2] = {0, 0};                 // blocks consumed per tile (p_full phases)
+            int of[2] = {0, 0};                 // items finished per tile (o_full / o_empty phases)
+            bool ok = true;
+            for (int r = 0; r < n_mine && ok; ++r) {
+                const Item it = decode_item<CAUSAL>(item_index(r), Hq, Hkv, N, BH);
+                ok = mbar_wait(q_full, r & 1, abort_flag, status) &&
+                     mbar_wait(&kv_full[base % NS], (base / NS) & 1, abort_flag, status);
+                if (!ok) break;
+                tc_fence_after();
                 for (int t = 0; t < 2; ++t)
-                    if (nblk[t] > 0) issue_s(t, 0);
-                mma_commit(&kv_empty[0]);
-            }
-            for (int j = 0; j < nmax && ok; ++j) {
-                const int vidx = 2 * j + 1, kidx = 2 * j + 2;
-                const int vst = vidx % NS, kst = kidx % NS;
-                const bool next = j + 1 < nmax;
-                if (!mbar_wait(&kv_full[vst], (vidx / NS) & 1, abort_flag, status)) break;
-                if (j < nblk[0]) {
-                    if (!mbar_wait(&p_full[0], j & 1, abort_flag, status)) break;
-                    tc_fence_after();
-                    issue_pv(0, vst, j);
+                    if (it.nblk[t] > 0) issue_s(t, base % NS);
+                mma_commit(&kv_empty[base % NS]);
+                if (it.nmax == 1) mma_commit(q_empty);     // every S product of the item issued
+                for (int j = 0; j < it.nmax && ok; ++j) {
+                    const int vidx = base + 2 * j + 1, kidx = base + 2 * j + 2;
+                    const int vst = vidx % NS, kst = kidx % NS;
+                    const bool next = j + 1 < it.nmax;
+                    if (!mbar_wait(&kv_full[vst], (vidx / NS) & 1, abort_flag, status)) { ok = false; break; }
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        if (j < it.nblk[t]) {
+                            if (j == 0 && of[t] > 0 &&
+                                !mbar_wait(&o_empty[t], (of[t] - 1) & 1, abort_flag, status)) { ok = false; break; }
+                            if (!mbar_wait(&p_full[t], pb[t] & 1, abort_flag, status)) { ok = false; break; }
+                            ++pb[t];
+                            tc_fence_after();
+                            issue_pv(t, vst, j);
+                            if (j == it.nblk[t] - 1) mma_commit(&o_full[t]);
+                        }
+                        if (t == 0 && next) {
+                            // S0 of the next block goes between PV0 and PV1 of this one
+                            if (!mbar_wait(&kv_full[kst], (kidx / NS) & 1, abort_flag, status)) { ok = false; break; }
+                            tc_fence_after();
+                            if (j + 1 < it.nblk[0]) issue_s(0, kst);
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(&kv_empty[vst]);
+                    if (next) {
+                        if (j + 1 < it.nblk[1]) issue_s(1, kst);
+                        mma_commit(&kv_empty[kst]);
+                        if (j + 1 == it.nmax - 1) mma_commit(q_empty);   // last S products issued
+                    }
                 }
-                if (next) {
-                    if (!mbar_wait(&kv_full[kst], (kidx / NS) & 1, abort_flag, status)) break;
-                    tc_fence_after();
-                    if (j + 1 < nblk[0]) issue_s(0, kst);
-                }
-                if (j < nblk[1]) {
-                    if (!mbar_wait(&p_full[1], j & 1, abort_flag, status)) break;
-                    tc_fence_after();
-                    issue_pv(1, vst, j);
-                }
-                mma_commit(&kv_empty[vst]);
-                if (next) {
-                    if (j + 1 < nblk[1]) issue_s(1, kst);
-                    mma_commit(&kv_empty[kst]);
-                }
+                for (int t = 0; t < 2; ++t)
+                    if (it.nblk[t] > 0) ++of[t];
+                base += 2 * it.nmax;
             }
             // Nothing issued may still be running when TMEM is released.
             mma_commit(mma_done);
@@ -264,117 +302,121 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------------------ softmax warps
         const int t = warp >> 2, wq = warp & 3;
         const int row = wq * 32 + lane;             // row within the tile = TMEM lane
-        const int r = q0[t] + row;                  // query index
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + t * 128;
         const uint32_t tO = tmem + lane_off + 256 + t * 128;
-        const int nb = nblk[t];
-        // l: sum of the fp32 weights (gives LSE).  lc: rounding residual bf16(p) - p of each
-        // block's largest weight, the dominant part of (sum of the bf16 weights that P V applies)
-        // - l; O is divided by l + lc so the applied weights sum to one when one weight dominates.
-        float m = -INFINITY, l = 0.f, lc = 0.f;
+        int sb = 0;                                 // blocks consumed by this tile (s_full phases)
+        int of = 0;                                 // items finished by this tile (o_full phases)
         bool ok = true;
-        for (int j = 0; j < nb; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_flag, status));
+        for (int r = 0; r < n_mine && ok; ++r) {
+            const Item it = decode_item<CAUSAL>(item_index(r), Hq, Hkv, N, BH);
+            const int nb = it.nblk[t];
+            if (nb == 0) continue;
+            const int q0 = it.q0[t];
+            const int rq = q0 + row;                // query index
+            // l: sum of the fp32 weights (gives LSE).  lc: rounding residual bf16(p) - p of each
+            // block's largest weight, the dominant part of (sum of the bf16 weights that P V
+            // applies) - l; O is divided by l + lc so the applied weights sum to one when one
+            // weight dominates.
+            float m = -INFINITY, l = 0.f, lc = 0.f;
+            for (int j = 0; j < nb; ++j) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], sb & 1, abort_flag, status));
+                if (!ok) break;
+                ++sb;
+                tc_fence_after();
+                uint32_t sraw[128];
+                tmem_ld_x128(tS, sraw);
+                float s[128];
+#pragma unroll
+                for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sraw[c]);
+                const int kbase = j * BN;
+                const bool need_mask = (CAUSAL && kbase + BN - 1 > q0) || (kbase + BN > N);
+                if (need_mask) {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) {
+                        const int key = kbase + c;
+                        if ((CAUSAL && key > rq) || key >= N) s[c] = -INFINITY;
+                    }
+                }
+                // row max as a shallow tree of 3-input maxes (8 independent chains)
+                float m8[8];
+    #pragma unroll
+                for (int k = 0; k < 8; ++k) m8[k] = fmax3(s[k], s[k + 8], s[k + 16]);
+    #pragma unroll
+                for (int i = 24; i < 120; i += 16)
+    #pragma unroll
+                    for (int k = 0; k < 8; ++k) m8[k] = fmax3(m8[k], s[i + k], s[i + 8 + k]);
+    #pragma unroll
+                for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], s[120 + k]);
+                const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                                       fmaxf(m8[6], m8[7]));
+                const float m_blk = mx * scale_log2;
+                const bool need = m_blk > m + RESCALE_THRESHOLD;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float alpha = need ? ex2_approx(m - m_blk) : 1.f;
+                    if (need) {
+                        l *= alpha;
+                        lc *= alpha;
+                        m = m_blk;
+                    }
+                    if (j > 0) rescale_o_row<D>(tO, alpha);
+                }
+                const float m_sub = (m == -INFINITY) ? 0.f : m;
+                // p = 2^(s c - m) on pairs: one packed FMA, two ex2, packed sums in 4 chains
+                const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+                const uint64_t nm2 = f2_pack(-m_sub, -m_sub);
+                uint64_t acc[4];
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) acc[k] = 0ull;
+                uint32_t p[64];
+    #pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const float2 x = f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), c2, nm2));
+                    const float p0 = ex2_approx(x.x);
+                    const float p1 = ex2_approx(x.y);
+                    acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
+                    p[c] = pack_bf16x2(p0, p1);
+                }
+                {
+                    const float2 a = f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])));
+                    l += a.x + a.y;
+                    // the block's largest weight is computed exactly as its element was above
+                    const float ptop = ex2_approx(fmaf(mx, scale_log2, -m_sub));
+                    lc += __bfloat162float(__float2bfloat16_rn(ptop)) - ptop;
+                }
+                tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+                tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&p_full[t]);
+            }
             if (!ok) break;
+            // epilogue: O = C / (l + lc) -> bf16 -> global, LSE; then hand O's TMEM back
+            ok = __all_sync(0xffffffffu, mbar_wait(&o_full[t], of & 1, abort_flag, status));
+            if (!ok) break;
+            ++of;
             tc_fence_after();
-            uint32_t sraw[128];
-            tmem_ld_x128(tS, sraw);
-            float s[128];
-#pragma unroll
-            for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sraw[c]);
-            const int kbase = j * BN;
-            const bool need_mask = (CAUSAL && kbase + BN - 1 > q0[t]) || (kbase + BN > N);
-            if (need_mask) {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const int key = kbase + c;
-                    if ((CAUSAL && key > r) || key >= N) s[c] = -INFINITY;
-                }
-            }
-            // row max as a shallow tree of 3-input maxes (8 independent chains)
-            float m8[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) m8[k] = fmax3(s[k], s[k + 8], s[k + 16]);
-#pragma unroll
-            for (int i = 24; i < 120; i += 16)
-#pragma unroll
-                for (int k = 0; k < 8; ++k) m8[k] = fmax3(m8[k], s[i + k], s[i + 8 + k]);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], s[120 + k]);
-            const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
-                                   fmaxf(m8[6], m8[7]));
-            const float m_blk = mx * scale_log2;
-            const bool need = m_blk > m + RESCALE_THRESHOLD;
-            if (__any_sync(0xffffffffu, need)) {
-                const float alpha = need ? ex2_approx(m - m_blk) : 1.f;
-                if (need) {
-                    l *= alpha;
-                    lc *= alpha;
-                    m = m_blk;
-                }
-                if (j > 0) rescale_o_row<D>(tO, alpha);
-            }
-            const float m_sub = (m == -INFINITY) ? 0.f : m;
-            // p = 2^(s c - m) on pairs: one packed FMA, two ex2, packed sums in 4 chains
-            const uint64_t c2 = f2_pack(scale_log2, scale_log2);
-            const uint64_t nm2 = f2_pack(-m_sub, -m_sub);
-            uint64_t acc[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) acc[k] = 0ull;
-            uint32_t p[64];
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float2 x = f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), c2, nm2));
-                const float p0 = ex2_approx(x.x);
-                const float p1 = ex2_approx(x.y);
-                acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
-                p[c] = pack_bf16x2(p0, p1);
-            }
-            {
-                const float2 a = f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])));
-                l += a.x + a.y;
-                // the block's largest weight is computed exactly as its element was above
-                const float ptop = ex2_approx(fmaf(mx, scale_log2, -m_sub));
-                lc += __bfloat162float(__float2bfloat16_rn(ptop)) - ptop;
-            }
-            tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
-            tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&p_full[t]);
-        }
-        if (ok && nb > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[t], 0, abort_flag, status));
-        if (ok && nb > 0) {
-            tc_fence_after();
-            // Every MMA reading Q tile t has completed, so its smem becomes the O staging tile,
-            // in the same 128B-swizzled layout the TMA store expects.
-            uint8_t *stage = smem + L::Q_OFF + t * L::TILE_BYTES;
             const float inv_l = 1.f / (l + lc);
+            __nv_bfloat16 *orow = O + (static_cast<size_t>(it.bh) * N + rq) * D;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
                 tmem_ld_x32(tO + c0, o);
-                uint8_t *rowp = stage + (c0 / 64) * L::CHUNK_BYTES + row * 128;
-                const int u0 = (c0 % 64) / 8;
+                if (rq < N) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    uint4 v;
-                    v.x = pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv_l, __uint_as_float(o[8 * u + 1]) * inv_l);
-                    v.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv_l, __uint_as_float(o[8 * u + 3]) * inv_l);
-                    v.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv_l, __uint_as_float(o[8 * u + 5]) * inv_l);
-                    v.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv_l, __uint_as_float(o[8 * u + 7]) * inv_l);
-                    *reinterpret_cast<uint4 *>(rowp + (((u0 + u) ^ (row & 7)) << 4)) = v;
+                    for (int u = 0; u < 4; ++u) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv_l, __uint_as_float(o[8 * u + 1]) * inv_l);
+                        v.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv_l, __uint_as_float(o[8 * u + 3]) * inv_l);
+                        v.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv_l, __uint_as_float(o[8 * u + 5]) * inv_l);
+                        v.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv_l, __uint_as_float(o[8 * u + 7]) * inv_l);
+                        *reinterpret_cast<uint4 *>(orow + c0 + 8 * u) = v;
+                    }
                 }
             }
-            if (r < N) LSE[static_cast<size_t>(bh) * N + r] = (m + log2f(l)) * LN2;
-            fence_proxy_async_smem();
-            mbar_arrive(&epi[t]);
-            if (row == 0 && mbar_wait(&epi[t], 0, abort_flag, status)) {
-                for (int ch = 0; ch < D / 64; ++ch)
-                    tma_store_3d(&tmO, stage + ch * L::CHUNK_BYTES, ch * 64, q0[t], bh);
-                tma_store_commit_and_wait_read();
-            }
+            if (rq < N) LSE[static_cast<size_t>(it.bh) * N + rq] = (m + log2f(l)) * LN2;
+            tc_fence_before();
+            mbar_arrive(&o_empty[t]);
         }
         tc_fence_before();
         __syncthreads();
@@ -383,7 +425,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 template <int D, bool CAUSAL>
 cudaError_t launch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
-                   const CUtensorMap &tmV, const CUtensorMap &tmO, float *LSE, unsigned *status,
+                   const CUtensorMap &tmV, void *O, float *LSE, unsigned *status,
                    cudaStream_t stream) {
     auto kern = fwd_kernel<D, CAUSAL>;
     const int smem = Layout<D>::BYTES;
@@ -396,28 +438,28 @@ cudaError_t launch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &
     if (attr.numRegs * NUM_THREADS < REGS_NEEDED) return cudaErrorInvalidConfiguration;
     const int BH = p.B * p.Hq;
     const long long n_pairs = (p.N + 2 * BM - 1) / (2 * BM);
-    const long long grid = n_pairs * BH;
-    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const long long n_items = n_pairs * BH;
+    if (n_items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // persistent: one CTA per SM (TMEM and shared memory allow no second one)
+    const int grid = static_cast<int>(std::min<long long>(n_items, num_sms()));
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
-    // One chunk spans every head: the global longest-first order measured faster than chunks
-    // of heads sized for L2 residency (the K/V re-reads it causes stay below the HBM limit).
-    const int HC = BH;
-    kern<<<static_cast<unsigned>(grid), NUM_THREADS, smem, stream>>>(
-        tmQ, tmK, tmV, tmO, LSE, p.Hq, p.Hkv, p.N, BH, HC, scale_log2, status);
+    kern<<<grid, NUM_THREADS, smem, stream>>>(tmQ, tmK, tmV, static_cast<__nv_bfloat16 *>(O), LSE,
+                                              p.Hq, p.Hkv, p.N, BH, static_cast<int>(n_items),
+                                              scale_log2, status);
     return cudaGetLastError();
 }
 
 }  // namespace fwd
 
 cudaError_t launch_fwd_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
-                            const CUtensorMap &tmV, const CUtensorMap &tmO, float *LSE,
-                            unsigned *status, cudaStream_t stream) {
+                            const CUtensorMap &tmV, void *O, float *LSE, unsigned *status,
+                            cudaStream_t stream) {
     if (p.d == 128)
-        return p.causal ? fwd::launch<128, true>(p, tmQ, tmK, tmV, tmO, LSE, status, stream)
-                        : fwd::launch<128, false>(p, tmQ, tmK, tmV, tmO, LSE, status, stream);
+        return p.causal ? fwd::launch<128, true>(p, tmQ, tmK, tmV, O, LSE, status, stream)
+                        : fwd::launch<128, false>(p, tmQ, tmK, tmV, O, LSE, status, stream);
     if (p.d == 64)
-        return p.causal ? fwd::launch<64, true>(p, tmQ, tmK, tmV, tmO, LSE, status, stream)
-                        : fwd::launch<64, false>(p, tmQ, tmK, tmV, tmO, LSE, status, stream);
+        return p.causal ? fwd::launch<64, true>(p, tmQ, tmK, tmV, O, LSE, status, stream)
+                        : fwd::launch<64, false>(p, tmQ, tmK, tmV, O, LSE, status, stream);
     return cudaErrorInvalidValue;
 }
 

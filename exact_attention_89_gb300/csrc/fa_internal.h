@@ -17,10 +17,11 @@ struct Problem {
     float scale;
 };
 
-// K1: bf16 forward on tcgen05. Maps are 3-D [d, N, B*H] bf16, box [64, 128, 1], 128B swizzle.
+// K1: bf16 forward on tcgen05. Maps are 3-D [d, N, B*H] bf16, box [64, 128, 1], 128B swizzle;
+// O is written with plain stores.
 cudaError_t launch_fwd_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
-                            const CUtensorMap &tmV, const CUtensorMap &tmO, float *LSE,
-                            unsigned *status, cudaStream_t stream);
+                            const CUtensorMap &tmV, void *O, float *LSE, unsigned *status,
+                            cudaStream_t stream);
 
 // K2: D = rowsum(dO * O) in fp32 and zeroing of the fp32 dQ accumulator.
 cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const void *dO, float *D,
