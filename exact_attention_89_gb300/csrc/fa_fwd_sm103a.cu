@@ -42,7 +42,7 @@ constexpr int NUM_THREADS = 384;   // three warpgroups
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
 // Register split: softmax warpgroups 0 and 1 grow, warpgroup 2 (TMA, MMA, two idle warps) shrinks.
-constexpr uint32_t REGS_SOFTMAX = 208, REGS_OTHER = 80;
+constexpr uint32_t REGS_SOFTMAX = 208, REGS_OTHER = 88;
 constexpr int REGS_NEEDED = 2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER;
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr float LN2 = 0.693147180559945309f;
@@ -250,37 +250,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (it.nblk[t] > 0) issue_s(t, base % NS);
                 mma_commit(&kv_empty[base % NS]);
                 if (it.nmax == 1) mma_commit(q_empty);     // every S product of the item issued
-                for (int j = 0; j < it.nmax && ok; ++j) {
+                const int nb0 = it.nblk[0], nb1 = it.nblk[1], nmax = it.nmax;
+                for (int j = 0; j < nmax; ++j) {
                     const int vidx = base + 2 * j + 1, kidx = base + 2 * j + 2;
                     const int vst = vidx % NS, kst = kidx % NS;
-                    const bool next = j + 1 < it.nmax;
+                    const bool next = j + 1 < nmax;
                     if (!mbar_wait(&kv_full[vst], (vidx / NS) & 1, abort_flag, status)) { ok = false; break; }
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        if (j < it.nblk[t]) {
-                            if (j == 0 && of[t] > 0 &&
-                                !mbar_wait(&o_empty[t], (of[t] - 1) & 1, abort_flag, status)) { ok = false; break; }
-                            if (!mbar_wait(&p_full[t], pb[t] & 1, abort_flag, status)) { ok = false; break; }
-                            ++pb[t];
-                            tc_fence_after();
-                            issue_pv(t, vst, j);
-                            if (j == it.nblk[t] - 1) mma_commit(&o_full[t]);
-                        }
-                        if (t == 0 && next) {
-                            // S0 of the next block goes between PV0 and PV1 of this one
-                            if (!mbar_wait(&kv_full[kst], (kidx / NS) & 1, abort_flag, status)) { ok = false; break; }
-                            tc_fence_after();
-                            if (j + 1 < it.nblk[0]) issue_s(0, kst);
-                        }
+                    if (j < nb0) {
+                        // the item's first P V overwrites O: its previous contents must be read out
+                        if (j == 0 && of[0] > 0 &&
+                            !mbar_wait(&o_empty[0], (of[0] - 1) & 1, abort_flag, status)) { ok = false; break; }
+                        if (!mbar_wait(&p_full[0], pb[0] & 1, abort_flag, status)) { ok = false; break; }
+                        ++pb[0];
+                        tc_fence_after();
+                        issue_pv(0, vst, j);
+                        if (j == nb0 - 1) mma_commit(&o_full[0]);
                     }
-                    if (!ok) break;
+                    if (next) {
+                        // S0 of the next block goes between PV0 and PV1 of this one
+                        if (!mbar_wait(&kv_full[kst], (kidx / NS) & 1, abort_flag, status)) { ok = false; break; }
+                        tc_fence_after();
+                        if (j + 1 < nb0) issue_s(0, kst);
+                    }
+                    if (j < nb1) {
+                        if (j == 0 && of[1] > 0 &&
+                            !mbar_wait(&o_empty[1], (of[1] - 1) & 1, abort_flag, status)) { ok = false; break; }
+                        if (!mbar_wait(&p_full[1], pb[1] & 1, abort_flag, status)) { ok = false; break; }
+                        ++pb[1];
+                        tc_fence_after();
+                        issue_pv(1, vst, j);
+                        if (j == nb1 - 1) mma_commit(&o_full[1]);
+                    }
                     mma_commit(&kv_empty[vst]);
                     if (next) {
-                        if (j + 1 < it.nblk[1]) issue_s(1, kst);
+                        if (j + 1 < nb1) issue_s(1, kst);
                         mma_commit(&kv_empty[kst]);
-                        if (j + 1 == it.nmax - 1) mma_commit(q_empty);   // last S products issued
+                        if (j + 1 == nmax - 1) mma_commit(q_empty);   // last S products issued
                     }
                 }
+                if (!ok) break;
                 for (int t = 0; t < 2; ++t)
                     if (it.nblk[t] > 0) ++of[t];
                 base += 2 * it.nmax;
@@ -340,13 +348,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 // row max as a shallow tree of 3-input maxes (8 independent chains)
                 float m8[8];
-    #pragma unroll
+#pragma unroll
                 for (int k = 0; k < 8; ++k) m8[k] = fmax3(s[k], s[k + 8], s[k + 16]);
-    #pragma unroll
+#pragma unroll
                 for (int i = 24; i < 120; i += 16)
-    #pragma unroll
+#pragma unroll
                     for (int k = 0; k < 8; ++k) m8[k] = fmax3(m8[k], s[i + k], s[i + 8 + k]);
-    #pragma unroll
+#pragma unroll
                 for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], s[120 + k]);
                 const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
                                        fmaxf(m8[6], m8[7]));
@@ -366,10 +374,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint64_t c2 = f2_pack(scale_log2, scale_log2);
                 const uint64_t nm2 = f2_pack(-m_sub, -m_sub);
                 uint64_t acc[4];
-    #pragma unroll
+#pragma unroll
                 for (int k = 0; k < 4; ++k) acc[k] = 0ull;
                 uint32_t p[64];
-    #pragma unroll
+#pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const float2 x = f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), c2, nm2));
                     const float p0 = ex2_approx(x.x);
