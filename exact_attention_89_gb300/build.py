@@ -47,8 +47,8 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def _compile(src: str, extra) -> tuple[str, str]:
-    obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+def _compile(src: str, extra, build_dir: str = BUILD_DIR) -> tuple[str, str]:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     cmd = [nvcc()] + ARCH + NVCC_FLAGS + list(extra) + ["-I", INCLUDE, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -56,24 +56,30 @@ def _compile(src: str, extra) -> tuple[str, str]:
     return obj, r.stderr
 
 
-def build(force: bool = False, extra_flags=(), verbose: bool = False) -> str:
-    """Compile and link libflashattn.so; returns its path. Skips work when up to date."""
-    if not force and not extra_flags and up_to_date():
+def build(force: bool = False, extra_flags=(), verbose: bool = False, out_dir: str | None = None) -> str:
+    """Compile and link libflashattn.so; returns its path. Skips work when up to date.
+
+    With out_dir, objects and the library go there instead (used by tests for builds with extra
+    macros); the in-tree library is left alone.
+    """
+    lib = LIB if out_dir is None else os.path.join(out_dir, "libflashattn.so")
+    bdir = BUILD_DIR if out_dir is None else os.path.join(out_dir, "obj")
+    if out_dir is None and not force and not extra_flags and up_to_date():
         return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra_flags), srcs))
+        results = list(ex.map(lambda s: _compile(s, extra_flags, bdir), srcs))
     if verbose:
         for _, log in results:
             print(log)
-    tmp = LIB + ".%d.tmp" % os.getpid()
+    tmp = lib + ".%d.tmp" % os.getpid()
     cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -194,12 +194,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int e = 0; e < 2 * it.nmax; ++e) {
                     const int idx = base + e, j = e >> 1, st = idx % NS, rnd = idx / NS;
                     if (!mbar_wait(&kv_empty[st], (rnd & 1) ^ 1, abort_flag, status)) { ok = false; break; }
+#ifdef FA_FAULT_INJECT
+                    // Test builds only: CTA 0 never delivers its first K block, so the MMA warp's
+                    // bounded wait runs out, the CTA unwinds and FA_ERR_DEVICE_TIMEOUT is recorded.
+                    if (blockIdx.x == 0 && idx == 0) continue;
+#endif
                     mbar_arrive_expect_tx(&kv_full[st], L::TILE_BYTES);
                     uint8_t *dst = smem + L::KV_OFF + st * L::TILE_BYTES;
                     const CUtensorMap *tm = (e & 1) ? &tmV : &tmK;
                     for (int ch = 0; ch < D / 64; ++ch)
                         tma_load_3d(dst + ch * L::CHUNK_BYTES, tm, ch * 64, j * BN, it.bkv, &kv_full[st]);
-                    ++issued;
+                    issued = idx + 1;                 // ring index after the last load issued
                 }
                 base += 2 * it.nmax;
             }
