@@ -163,7 +163,7 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
                  cudaStream_t stream) {
     fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
     if (st != FA_OK) return st;
-    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     if (!fa::aligned16(Q) || !fa::aligned16(K) || !fa::aligned16(V) || !fa::aligned16(O) ||
         !fa::aligned16(dO) || !fa::aligned16(LSE) || !fa::aligned16(dQ) || !fa::aligned16(dK) ||
         !fa::aligned16(dV))

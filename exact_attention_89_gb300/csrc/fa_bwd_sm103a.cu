@@ -78,7 +78,7 @@ __device__ __forceinline__ int first_q_tile(int jb) {
     return CAUSAL ? (jb * BKV) / BQ : 0;
 }
 
-template <int D, bool CAUSAL>
+template <int D, int DR, bool CAUSAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -86,7 +86,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const float *__restrict__ LSE, const float *__restrict__ Dvec,
                     float *__restrict__ dQacc, int Hq, int Hkv, int N, int BHkv, int HC,
                     float scale, float scale_log2, unsigned *status) {
+    // Laid out for d = 128.  With a real head dim DR = 64 the tensor maps are 64 wide, so the
+    // second 64-column chunk of every load is TMA zero fill: all products see zero-padded
+    // operands and are unchanged; only the dQ reductions and the dK / dV stores use DR.
     static_assert(D == 128, "the bf16 backward main loop is laid out for d = 128");
+    static_assert(DR == 64 || DR == 128, "real head dim 64 or 128");
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -396,7 +400,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             fence_proxy_async_smem();
             mbar_arrive(epi);
             if (krow == 0 && mbar_wait(epi, 0, abort_flag, status)) {
-                for (int ch = 0; ch < D / 64; ++ch) {
+                for (int ch = 0; ch < DR / 64; ++ch) {
                     tma_store_3d(&tmdK, smem + L::K_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
                     tma_store_3d(&tmdV, smem + L::V_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
                 }
@@ -422,11 +426,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_ld_x64(tmem + lane_off + T_BUF + bsel * 128 + B_DQT, a);
             tc_fence_before();
             mbar_arrive(&dq_empty[bsel]);
-            float *dst = dQacc + (static_cast<size_t>(bhq) * N + q0) * D + dcol;
-            const int nvalid = min(BQ, N - q0);
+            float *dst = dQacc + (static_cast<size_t>(bhq) * N + q0) * DR + dcol;
+            // rows of this tile inside the sequence; with DR = 64 the upper 64 lanes hold zeros
+            const int nvalid = (DR == D || dcol < DR) ? min(BQ, N - q0) : 0;
 #pragma unroll
             for (int c = 0; c < BQ; ++c)
-                if (c < nvalid) atomicAdd(dst + static_cast<size_t>(c) * D, __uint_as_float(a[c]) * scale);
+                if (c < nvalid) atomicAdd(dst + static_cast<size_t>(c) * DR, __uint_as_float(a[c]) * scale);
         }
         tc_fence_before();
         __syncthreads();
@@ -517,7 +522,7 @@ cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const
                                  const CUtensorMap &tmdK, const CUtensorMap &tmdV,
                                  const float *LSE, const float *D, float *dQacc, unsigned *status,
                                  cudaStream_t stream) {
-    if (p.d != 128) return cudaErrorInvalidValue;
+    if (p.d != 128 && p.d != 64) return cudaErrorInvalidValue;
     const int BHkv = p.B * p.Hkv;
     const long long nkb = (p.N + bwd::BKV - 1) / bwd::BKV;
     // One chunk spans every KV head (key-block-major order): measured slightly faster than
@@ -527,28 +532,23 @@ cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int smem = bwd::Layout<128>::BYTES;
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
-    cudaError_t e;
+    using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                          const float *, const float *, float *, int, int, int, int, int, float, float,
+                          unsigned *);
+    Kern kern;
+    if (p.d == 128)
+        kern = p.causal ? bwd::bwd_main_kernel<128, 128, true> : bwd::bwd_main_kernel<128, 128, false>;
+    else
+        kern = p.causal ? bwd::bwd_main_kernel<128, 64, true> : bwd::bwd_main_kernel<128, 64, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    // the in-kernel register split needs at least REGS_NEEDED registers at launch
     cudaFuncAttributes attr{};
-    if (p.causal) {
-        auto kern = bwd::bwd_main_kernel<128, true>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        // the in-kernel register split needs at least REGS_NEEDED registers at launch
-        if ((e = cudaFuncGetAttributes(&attr, kern)) != cudaSuccess) return e;
-        if (attr.numRegs * bwd::NUM_THREADS < bwd::REGS_NEEDED) return cudaErrorInvalidConfiguration;
-        kern<<<static_cast<unsigned>(grid), bwd::NUM_THREADS, smem, stream>>>(
-            tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, HC, p.scale,
-            scale_log2, status);
-    } else {
-        auto kern = bwd::bwd_main_kernel<128, false>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        if ((e = cudaFuncGetAttributes(&attr, kern)) != cudaSuccess) return e;
-        if (attr.numRegs * bwd::NUM_THREADS < bwd::REGS_NEEDED) return cudaErrorInvalidConfiguration;
-        kern<<<static_cast<unsigned>(grid), bwd::NUM_THREADS, smem, stream>>>(
-            tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, HC, p.scale,
-            scale_log2, status);
-    }
+    if ((e = cudaFuncGetAttributes(&attr, kern)) != cudaSuccess) return e;
+    if (attr.numRegs * bwd::NUM_THREADS < bwd::REGS_NEEDED) return cudaErrorInvalidConfiguration;
+    kern<<<static_cast<unsigned>(grid), bwd::NUM_THREADS, smem, stream>>>(
+        tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, HC, p.scale,
+        scale_log2, status);
     return cudaGetLastError();
 }
 

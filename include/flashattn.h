@@ -75,7 +75,8 @@ size_t fa_bwd_workspace_bytes(int B, int Hq, int N, int d);
  *   Q, K, V, O, dO: bf16 inputs as in fa_fwd (O is the forward output; D is formed from it).
  *   LSE: the fp32 LSE fa_fwd wrote for these inputs.
  *   dQ [B,Hq,N,d], dK [B,Hkv,N,d], dV [B,Hkv,N,d]: bf16 outputs (dK, dV summed over the group).
- *   d must be 128 (other head dims return FA_ERR_UNSUPPORTED).
+ *   d must be 64 or 128 (d = 64 runs the d = 128 tiling on zero-padded operands, so it costs
+ *   the FLOPs of d = 128).
  *   workspace: caller-owned device scratch of at least fa_bwd_workspace_bytes(B,Hq,N,d) bytes,
  *   16-byte aligned; its contents on entry do not matter and are clobbered.
  *   Calls that share one workspace must not overlap on the GPU.

@@ -87,7 +87,7 @@ def test_backward_rejects_invalid_arguments(built_lib, fp32):
     assert bwd(L, Hq=4, Hkv=3, fp32=fp32) == E.FA_ERR_INVALID_ARG
     assert bwd(L, scale=math.nan, fp32=fp32) == E.FA_ERR_INVALID_ARG
     if not fp32:
-        assert bwd(L, d=64, fp32=fp32) == E.FA_ERR_UNSUPPORTED
+        assert bwd(L, d=96, fp32=fp32) == E.FA_ERR_UNSUPPORTED
     assert bwd(L, d=200, fp32=fp32) == E.FA_ERR_UNSUPPORTED
     for k in range(9):
         ptrs = [A] * 9

@@ -38,10 +38,10 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("B,Hq,Hkv,N,causal", SMALL)
-def test_backward_small_shapes(flash, oracle_mod, B, Hq, Hkv, N, causal):
-    d = 128
-    Q, K, V, dO = make_inputs(B, Hq, Hkv, N, d, seed=200 + N)
+def test_backward_small_shapes(flash, oracle_mod, B, Hq, Hkv, N, causal, d):
+    Q, K, V, dO = make_inputs(B, Hq, Hkv, N, d, seed=200 + N + d)
     scale = 1.0 / np.sqrt(d)
     got = gpu_fwd_bwd(flash, Q, K, V, dO, causal, scale)
     ref = oracle_mod.backward(f64(Q), f64(K), f64(V), f64(dO), causal, scale)
