@@ -36,9 +36,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch of the dominant launch sequence from one ncu capture, keyed by the
 # sha256 of the kernel sources it was taken on; reported as null once the sources change.
 NCU_TRAFFIC = {
-    # fa_bwd on causal_n4096: bwd_main 1.920 GB read + 0.990 GB write, bwd_preprocess 0.210 GB,
+    # fa_bwd on causal_n4096: bwd_main 1.917 GB read + 0.990 GB write, bwd_preprocess 0.210 GB,
     # bwd_dq_convert 0.164 GB (profiles/bwd_main_kernel_causal_n4096.md)
-    "cfbbd584a7378bef": 3.28e9,
+    "14243a636aa449c0": 3.28e9,
 }
 
 
