@@ -56,9 +56,13 @@ def _load():
             lib.oracle_forward_rows.argtypes = common + [_D, _D, _D, ctypes.c_int, _L, _D, _D]
             lib.oracle_backward_dq_rows.argtypes = common + [_D, _D, _D, _D, ctypes.c_int, _L, _D]
             lib.oracle_backward_dkv_cols.argtypes = common + [_D, _D, _D, _D, ctypes.c_int, _L, _D, _D]
+            lib.oracle_attention_forward_keys.argtypes = common + [_D, _D, _D, ctypes.c_int, ctypes.c_int,
+                                                                   ctypes.c_int, _I, _D, _D]
+            lib.oracle_merge_partials.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, _D, _D, _D, _D]
             for name in ("oracle_attention_forward", "oracle_attention_backward",
                          "oracle_forward_rows", "oracle_backward_dq_rows",
-                         "oracle_backward_dkv_cols", "oracle_num_threads"):
+                         "oracle_backward_dkv_cols", "oracle_num_threads",
+                         "oracle_attention_forward_keys", "oracle_merge_partials"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -181,3 +185,33 @@ def backward_dkv_cols(Q, K, V, dO, causal: bool, scale: float, cols):
                                           _ptr(cols, _L), _ptr(dK), _ptr(dV))
     _check(rc, "oracle_backward_dkv_cols")
     return dK, dV
+
+
+def forward_keys(Q, K, V, causal: bool, scale: float, key_begin: int, key_end: int):
+    """Partial forward over the keys key_begin <= j < key_end (and the causal mask): returns
+    (O [B, Hq, N, d], LSE [B, Hq, N]); rows with no allowed key get O = 0, LSE = -inf."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, Hq, Hkv, N, d = _shape(Q, K)
+    hs = np.ascontiguousarray(np.arange(B * Hq, dtype=np.int32))
+    O = np.zeros((B * Hq, N, d))
+    L = np.zeros((B * Hq, N))
+    rc = _load().oracle_attention_forward_keys(B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                                               _ptr(Q), _ptr(K), _ptr(V), int(key_begin),
+                                               int(key_end), len(hs), _ptr(hs, _I), _ptr(O),
+                                               _ptr(L))
+    _check(rc, "oracle_attention_forward_keys")
+    return O.reshape(B, Hq, N, d), L.reshape(B, Hq, N)
+
+
+def merge_partials(O_parts, LSE_parts):
+    """Merge of S partial results over disjoint key sets: O_parts [S, ..., d], LSE_parts [S, ...]
+    -> (O [..., d], LSE [...])."""
+    O_parts, LSE_parts = _f64(O_parts), _f64(LSE_parts)
+    S = O_parts.shape[0]
+    d = O_parts.shape[-1]
+    rows = int(np.prod(LSE_parts.shape[1:]))
+    O = np.zeros(LSE_parts.shape[1:] + (d,))
+    L = np.zeros(LSE_parts.shape[1:])
+    rc = _load().oracle_merge_partials(S, rows, d, _ptr(O_parts), _ptr(LSE_parts), _ptr(O), _ptr(L))
+    _check(rc, "oracle_merge_partials")
+    return O, L

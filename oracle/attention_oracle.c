@@ -141,6 +141,90 @@ int oracle_attention_forward(int B, int Hq, int Hkv, int N, int d, int causal, d
 }
 
 /*
+ * Forward restricted to the keys key_begin <= j < key_end (on top of the causal mask), over a
+ * list of heads, materialising one score/probability row at a time: the partial result one key
+ * range contributes (split-KV).  A row with no allowed key in the range gets O = 0 and
+ * LSE = -inf.  O_out is [nheads, N, d], LSE_out [nheads, N].
+ */
+int oracle_attention_forward_keys(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
+                                  const double *Q, const double *K, const double *V, int key_begin,
+                                  int key_end, int nheads, const int *heads, double *O_out,
+                                  double *LSE_out) {
+    if (check_shape(B, Hq, Hkv, N, d) || nheads < 0) return 1;
+    if (key_begin < 0 || key_end > N || key_begin > key_end) return 1;
+    const int G = Hq / Hkv;
+    const i64 nd = (i64)N * d;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * N);
+#pragma omp for schedule(dynamic, 16) collapse(2)
+        for (int h = 0; h < nheads; ++h)
+            for (i64 i = 0; i < N; ++i) {
+                const int bh = heads[h];
+                if (!p || bh < 0 || bh >= B * Hq) { bad = 1; continue; }
+                const int b = bh / Hq, hk = (bh % Hq) / G;
+                const double *q = Q + (i64)bh * nd + i * d;
+                const double *k = K + ((i64)b * Hkv + hk) * nd, *v = V + ((i64)b * Hkv + hk) * nd;
+                double *o = O_out + (i64)h * nd + i * d;
+                double m = -INFINITY;
+                for (i64 j = 0; j < N; ++j) {
+                    const int ok = is_allowed(causal, i, j) && j >= key_begin && j < key_end;
+                    p[j] = ok ? scale * dot(q, k + j * d, d) : -INFINITY;
+                    if (p[j] > m) m = p[j];
+                }
+                for (int c = 0; c < d; ++c) o[c] = 0.0;
+                if (m == -INFINITY) { LSE_out[(i64)h * N + i] = -INFINITY; continue; }
+                double l = 0.0;
+                for (i64 j = 0; j < N; ++j) {
+                    p[j] = (p[j] == -INFINITY) ? 0.0 : exp(p[j] - m);
+                    l += p[j];
+                }
+                for (i64 j = 0; j < N; ++j)
+                    if (p[j] != 0.0)
+                        for (int c = 0; c < d; ++c) o[c] += p[j] / l * v[j * d + c];
+                LSE_out[(i64)h * N + i] = m + log(l);
+            }
+        free(p);
+    }
+    return bad;
+}
+
+/*
+ * Merge of S partial results over disjoint key sets, in the form of the reading note's update
+ * (FlashAttention DAC'24 reading note, Methods): with the running state (m, l, O), each new part
+ * with its own normalised output O~ and log-sum-exp L~ = m~ + ln l~ updates
+ *   m' = max(m, L~),  l' = e^{m - m'} l + e^{L~ - m'},  O' = (e^{m - m'} l O + e^{L~ - m'} O~) / l'
+ * (a part is a block whose l~ is folded into its LSE); the result is O and LSE = m + ln l.
+ * Parts with LSE = -inf (no allowed key) contribute nothing.  O_parts is [S, rows, d] and
+ * LSE_parts [S, rows]; O_out [rows, d], LSE_out [rows].
+ */
+int oracle_merge_partials(int S, i64 rows, int d, const double *O_parts, const double *LSE_parts,
+                          double *O_out, double *LSE_out) {
+    if (S < 1 || rows < 0 || d < 1) return 1;
+#pragma omp parallel for schedule(static)
+    for (i64 r = 0; r < rows; ++r) {
+        double m = -INFINITY, l = 0.0;
+        double *o = O_out + r * d;
+        for (int c = 0; c < d; ++c) o[c] = 0.0;
+        for (int s = 0; s < S; ++s) {
+            const double Ls = LSE_parts[(i64)s * rows + r];
+            if (Ls == -INFINITY) continue;
+            const double *os = O_parts + ((i64)s * rows + r) * d;
+            const double mn = m > Ls ? m : Ls;
+            const double a = (m == -INFINITY) ? 0.0 : exp(m - mn) * l;   /* old weight */
+            const double bw = exp(Ls - mn);                               /* new part's weight */
+            const double ln = a + bw;
+            for (int c = 0; c < d; ++c) o[c] = (a * o[c] + bw * os[c]) / ln;
+            m = mn;
+            l = ln;
+        }
+        LSE_out[r] = (l == 0.0) ? -INFINITY : m + log(l);
+    }
+    return 0;
+}
+
+/*
  * Backward over a list of KV groups, materialising P and dS (N x N) for each query head.
  *   groups[g] = b * Hkv + hk.  dQ_out is [ngroups, G, N, d] (the group's query heads in order),
  *   dK_out and dV_out are [ngroups, N, d].  O and D come from the oracle's own fp64 forward.

@@ -319,3 +319,40 @@ def test_invalid_arguments_raise(oracle_mod):
         oracle_mod.forward(Q, K, K, False, 1.0)
     with pytest.raises(RuntimeError):
         oracle_mod.forward(rand(1, 2, 4, 2), K, K, False, 1.0, heads=[7])
+
+
+# --------------------------------------------------------------------------- split-KV merge
+def test_worked_example_merged_from_its_two_blocks(oracle_mod):
+    """FlashAttention note (paweldubiel.com) worked example: the two blocks' own results (0 and 1,
+    with LSE ln 2 and ln 6) merged by the rescale recurrence give 0.75 and LSE ln 8, not the
+    block mean 0.5."""
+    g = _worked()
+    O_parts = np.array(g["block_results"]).reshape(2, 1, 1)
+    LSE_parts = np.array([math.log(2.0), math.log(6.0)]).reshape(2, 1)
+    O, L = oracle_mod.merge_partials(O_parts, LSE_parts)
+    assert abs(O[0, 0] - g["expected_output"]) < 1e-15
+    assert abs(L[0] - math.log(8.0)) < 1e-15
+
+
+def test_key_range_partials_merge_to_one_shot(oracle_mod):
+    """Any partition of the keys into ranges: each range's partial (O, LSE) from the ranged
+    forward, merged, equals the one-shot forward; empty ranges (LSE = -inf) change nothing."""
+    rng = np.random.default_rng(3)
+    B, Hq, Hkv, N, d, scale = 1, 4, 2, 45, 6, 0.4
+    Q, K, V = rand(B, Hq, N, d) * 2, rand(B, Hkv, N, d), rand(B, Hkv, N, d)
+    for causal in (False, True):
+        O1, L1 = oracle_mod.forward(Q, K, V, causal, scale)
+        for bounds in (_random_bounds(N, rng), [(0, N)], [(0, 1), (1, 44), (44, 45)]):
+            parts = [oracle_mod.forward_keys(Q, K, V, causal, scale, a, b) for a, b in bounds]
+            O, L = oracle_mod.merge_partials(np.stack([p[0] for p in parts]),
+                                             np.stack([p[1] for p in parts]))
+            assert np.allclose(O, O1, atol=1e-13) and np.allclose(L, L1, atol=1e-13)
+        # causal rows before a range's first key see nothing from it
+        O0, L0 = oracle_mod.forward_keys(Q, K, V, True, scale, 20, 30)
+        assert np.isneginf(L0[:, :, :20]).all() and (O0[:, :, :20] == 0).all()
+
+
+def test_merge_with_a_single_part_is_identity(oracle_mod):
+    O_parts, L_parts = rand(1, 5, 3), rand(1, 5)
+    O, L = oracle_mod.merge_partials(O_parts, L_parts)
+    assert np.allclose(O, O_parts[0], atol=1e-15) and np.allclose(L, L_parts[0], atol=1e-15)
