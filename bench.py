@@ -42,6 +42,13 @@ NCU_TRAFFIC = {
 }
 
 
+def split_key_ranges(N: int, S: int):
+    """[begin, end) keys of each range of the split-KV forward (ceil(nb/S) 128-key blocks)."""
+    nb = -(-N // 128)
+    c = -(-nb // S)
+    return [(min(N, s * c * 128), min(N, (s + 1) * c * 128)) for s in range(S)]
+
+
 def kernel_sources_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_89_gb300", "csrc")
@@ -153,12 +160,41 @@ def whole_job_tflops(ws: int, flops_per_step: float, steps: int, max_ms: float) 
     return ws * flops_per_step * steps / (max_ms * 1e-3) / 1e12
 
 
+def cpu_oracle_rows_sample(w, budget_s: float, inputs=None):
+    """Forward-only workloads: times the fp64 oracle on batches of random query rows (each row
+    costs its own keys; random rows average to the formula's FLOPs per row)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from exact_attention_89_gb300.inputs import workload_inputs
+    Q, K, V, _ = inputs if inputs is not None else workload_inputs(w)
+    q, k, v = (t.to(torch.float64).numpy() for t in (Q, K, V))
+    rng = np.random.default_rng(w.seed)
+    total_rows = w.B * w.Hq * w.N
+    rows_done, t_total = 0, 0.0
+    while t_total < budget_s or rows_done == 0:
+        rows = rng.integers(0, total_rows, size=64)
+        t0 = time.perf_counter()
+        oracle.forward_rows(q, k, v, w.causal, w.scale, rows)
+        t_total += time.perf_counter() - t0
+        rows_done += len(rows)
+    per_row = w.flops_fwd() / total_rows
+    return {"value": per_row * rows_done / t_total / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d random query rows of %s (B%d Hq%d Hkv%d N%d d%d causal), fp64 forward, "
+                      "%.1f s" % (rows_done, w.name, w.B, w.Hq, w.Hkv, w.N, w.d, t_total),
+            "seconds": t_total, "rows": rows_done}
+
+
 def cpu_oracle_sample(w, budget_s: float, max_heads: int, inputs=None, first_group: int = 0):
     """Times the fp64 oracle (forward + backward of whole KV groups) on the host cores."""
     import torch
 
     import oracle
     from exact_attention_89_gb300.inputs import workload_inputs
+    if not w.backward:
+        return cpu_oracle_rows_sample(w, budget_s, inputs)
     Q, K, V, dO = inputs if inputs is not None else workload_inputs(w)
     G = w.Hq // w.Hkv
     heads_done, t_total = 0, 0.0
@@ -258,18 +294,38 @@ def main():
 
     w = WORKLOADS[args.workload]
     Qh, Kh, Vh, dOh = workload_inputs(w, seed_offset=replica_seed_offset(rank))
-    q, k, v, do = (t.to(dev) for t in (Qh, Kh, Vh, dOh))
+    q, k, v = (t.to(dev) for t in (Qh, Kh, Vh))
+    do = dOh.to(dev) if dOh is not None else None
     B, Hq, Hkv, N, d = w.B, w.Hq, w.Hkv, w.N, w.d
+    S = w.num_splits
+    split = S > 1
     O = torch.empty_like(q)
     LSE = torch.empty(B, Hq, N, dtype=torch.float32, device=dev)
-    dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    wsp = torch.empty(fa.fa_bwd_workspace_bytes(B, Hq, N, d), dtype=torch.uint8, device=dev)
+    if w.backward:
+        dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        wsp = torch.empty(fa.fa_bwd_workspace_bytes(B, Hq, N, d), dtype=torch.uint8, device=dev)
+    if split:
+        Op = torch.empty(S, B, Hq, N, d, dtype=torch.float32, device=dev)
+        Lp = torch.empty(S, B, Hq, N, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
-        fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
-        if w.backward:
+    def fwd_first():
+        # the forward's tensor-core launch
+        if split:
+            fa.fa_fwd_split(q, k, v, Op, Lp, w.causal, w.scale, S)
+        else:
+            fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
+
+    def second():
+        # what follows it in a step: the merge of the partials, or the backward
+        if split:
+            fa.fa_merge(Op, Lp, O, LSE)
+        elif w.backward:
             fa.fa_bwd(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsp)
+
+    def step():
+        fwd_first()
+        second()
 
     def barrier():
         if ws > 1:
@@ -311,10 +367,9 @@ def main():
     t_start.record(stream)
     for e0, e1, e2 in ev:
         e0.record(stream)
-        fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
+        fwd_first()
         e1.record(stream)
-        if w.backward:
-            fa.fa_bwd(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsp)
+        second()
         e2.record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -326,24 +381,45 @@ def main():
     if st != fa.FA_OK:
         raise RuntimeError("device status after timed region: " + fa.fa_status_string(st))
     total_ms = t_start.elapsed_time(t_end)
-    fwd_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / args.steps
-    bwd_ms = sum(b.elapsed_time(c) for _, b, c in ev) / args.steps
+    first_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / args.steps
+    second_ms = sum(b.elapsed_time(c) for _, b, c in ev) / args.steps
     total_ms = max_over_ranks(total_ms, ws, dev)
 
     flops_step = w.flops_fwd() + (w.flops_bwd() if w.backward else 0.0)
     value = whole_job_tflops(ws, flops_step, args.steps, total_ms)
 
+    # the one-pass forward on the same inputs, for comparison with the split path
+    one_pass_ms = None
+    if split and not args.no_extras:
+        for _ in range(3):
+            fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
+        o_s = torch.cuda.Event(enable_timing=True)
+        o_e = torch.cuda.Event(enable_timing=True)
+        o_s.record(stream)
+        for _ in range(args.steps):
+            fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
+        o_e.record(stream)
+        torch.cuda.synchronize()
+        one_pass_ms = o_s.elapsed_time(o_e) / args.steps
+
     # ---------------------------------------------------------------- end to end (host buffers)
-    pin = [t.pin_memory() for t in (Qh, Kh, Vh, dOh)]
-    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (O, LSE, dQ, dK, dV)]
+    pin = [t.pin_memory() for t in (Qh, Kh, Vh, dOh) if t is not None]
+    outs = (O, LSE, dQ, dK, dV) if w.backward else (O, LSE)
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in pin)
     d2h = sum(t.numel() * t.element_size() for t in outs_h)
 
     def e2e_step():
-        qd, kd, vd, dod = (t.to(dev, non_blocking=True) for t in pin)
-        Od, Ld = fa.attention_forward(qd, kd, vd, w.causal, w.scale)
-        gq, gk, gv = fa.attention_backward(qd, kd, vd, Od, dod, Ld, w.causal, w.scale, workspace=wsp)
-        for hbuf, dbuf in zip(outs_h, (Od, Ld, gq, gk, gv)):
+        dev_in = [t.to(dev, non_blocking=True) for t in pin]
+        qd, kd, vd = dev_in[:3]
+        if split:
+            res = fa.attention_forward_split(qd, kd, vd, w.causal, w.scale, num_splits=S)
+        else:
+            res = fa.attention_forward(qd, kd, vd, w.causal, w.scale)
+        if w.backward:
+            res = res + fa.attention_backward(qd, kd, vd, res[0], dev_in[3], res[1], w.causal,
+                                              w.scale, workspace=wsp)
+        for hbuf, dbuf in zip(outs_h, res):
             hbuf.copy_(dbuf, non_blocking=True)
 
     e2e_ms = float("nan")
@@ -367,40 +443,72 @@ def main():
     peaks, peaks_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
     src_hash = kernel_sources_hash()
-    bwd_achieved = w.flops_bwd() / (bwd_ms * 1e-3) / 1e12 if w.backward else None
-    fwd_achieved = w.flops_fwd() / (fwd_ms * 1e-3) / 1e12
-    traffic = NCU_TRAFFIC.get(src_hash)
-    roofline = {"bound": "tensor", "kernel": "fa_bwd (bwd_main + preprocess + dq_convert)",
-                "achieved": bwd_achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": bwd_achieved / peak if bwd_achieved else None,
-                "traffic": traffic, "peak_source": "%s burst bf16 (MEASURED_PEAKS.json)" % peaks_src
-                if peaks_src == "measured" else "fallback 1.9 PFLOP/s bf16",
-                "flops_per_launch": w.flops_bwd(),
-                "fwd": {"kernel": "fa_fwd", "achieved": fwd_achieved,
-                        "frac": fwd_achieved / peak, "ms": fwd_ms,
-                        "flops_per_launch": w.flops_fwd()},
-                "bwd_ms": bwd_ms, "sources": src_hash}
+    peak_source = ("%s burst bf16 (MEASURED_PEAKS.json)" % peaks_src if peaks_src == "measured"
+                   else "fallback 1.9 PFLOP/s bf16")
+    fwd_achieved = w.flops_fwd() / (first_ms * 1e-3) / 1e12
+    if split:
+        # the merge reads every LSE part and the O parts of rows with an allowed key in that
+        # range, and writes O (bf16) and LSE
+        rows = B * Hq * N
+        live = sum((B * Hq * max(0, N - k0) if w.causal else rows) if k1 > k0 else 0
+                   for k0, k1 in split_key_ranges(N, S))
+        merge_bytes = S * rows * 4 + live * d * 4 + rows * (d * 2 + 4)
+        hbm = float(peaks["hbm_gbs"])
+        merge_gbs = merge_bytes / (second_ms * 1e-3) / 1e9
+        roofline = {"bound": "tensor", "kernel": "fa_fwd_split", "achieved": fwd_achieved,
+                    "peak": peak, "unit": "TFLOP/s", "frac": fwd_achieved / peak,
+                    "traffic": NCU_TRAFFIC.get(src_hash + ":" + w.name), "peak_source": peak_source,
+                    "flops_per_launch": w.flops_fwd(), "ms": first_ms,
+                    "merge": {"kernel": "fa_merge", "bound": "hbm", "unit": "GB/s",
+                              "bytes_per_launch": merge_bytes, "ms": second_ms,
+                              "achieved": merge_gbs, "peak": hbm, "frac": merge_gbs / hbm},
+                    "one_pass_fwd_ms": one_pass_ms, "sources": src_hash}
+    elif w.backward:
+        bwd_achieved = w.flops_bwd() / (second_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "fa_bwd (bwd_main + preprocess + dq_convert)",
+                    "achieved": bwd_achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": bwd_achieved / peak,
+                    "traffic": NCU_TRAFFIC.get(src_hash), "peak_source": peak_source,
+                    "flops_per_launch": w.flops_bwd(),
+                    "fwd": {"kernel": "fa_fwd", "achieved": fwd_achieved,
+                            "frac": fwd_achieved / peak, "ms": first_ms,
+                            "flops_per_launch": w.flops_fwd()},
+                    "bwd_ms": second_ms, "sources": src_hash}
+    else:
+        roofline = {"bound": "tensor", "kernel": "fa_fwd", "achieved": fwd_achieved,
+                    "peak": peak, "unit": "TFLOP/s", "frac": fwd_achieved / peak,
+                    "traffic": NCU_TRAFFIC.get(src_hash + ":" + w.name), "peak_source": peak_source,
+                    "flops_per_launch": w.flops_fwd(), "ms": first_ms, "sources": src_hash}
     cpu = None
     if rank == 0 and ws == 1 and args.cpu_budget > 0 and not args.no_extras:
         r = cpu_oracle_sample(w, args.cpu_budget, w.B * w.Hq)
         cpu = {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")}
 
     if rank == 0:
-        line = {"metric": "attention TFLOP/s fwd+bwd, bf16 d=128 causal", "value": value,
+        if w.backward:
+            what = "fwd+bwd"
+            l2 = ("inputs larger than L2 (Q,K,V,dO,O = 5 x %.0f MB), no flush"
+                  % (q.numel() * 2 / 1e6))
+        else:
+            what = "fwd (split-KV x%d + merge)" % S if split else "fwd"
+            l2 = ("Q,K,V,O = 4 x %.0f MB%s; no flush" % (
+                q.numel() * 2 / 1e6,
+                " + fp32 partials %.0f MB" % (Op.numel() * 4 / 1e6) if split else ""))
+        line = {"metric": "attention TFLOP/s %s, bf16 d=%d %s"
+                          % (what, d, "causal" if w.causal else "non-causal"),
+                "value": value,
                 "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": total_ms / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
                            "causal": w.causal, "seed": w.seed, "scale": w.scale,
-                           "l2": "inputs larger than L2 (Q,K,V,dO,O = 5 x %.0f MB), no flush"
-                                 % (q.numel() * 2 / 1e6),
-                           "parallelism": "replicas x%d" % ws},
-                "fwd_tflops": w.flops_fwd() / (fwd_ms * 1e-3) / 1e12,
+                           "num_splits": S, "l2": l2, "parallelism": "replicas x%d" % ws},
+                "fwd_tflops": fwd_achieved,
                 "fwd_frac_of_peak": fwd_achieved / peak,
-                "fwd_bwd_frac_of_peak": value / ws / peak,
+                "fwd_bwd_frac_of_peak": value / ws / peak if w.backward else None,
                 "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
-                "gpu_launches": args.steps * (1 + (3 if w.backward else 0)),
+                "gpu_launches": args.steps * (2 if split else (1 + (3 if w.backward else 0))),
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks}
         print(json.dumps(line))
     if ws > 1:

@@ -157,6 +157,42 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
     return fa::from_cuda(fa::launch_fwd_bf16(p, tq, tk, tv, O, LSE, di->status, stream));
 }
 
+fa_status fa_fwd_split(const void *Q, const void *K, const void *V, float *O_parts,
+                       float *LSE_parts, int B, int Hq, int Hkv, int N, int d, int causal,
+                       float scale, int num_splits, cudaStream_t stream) {
+    fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!fa::aligned16(Q) || !fa::aligned16(K) || !fa::aligned16(V) || !fa::aligned16(O_parts) ||
+        !fa::aligned16(LSE_parts))
+        return FA_ERR_MISALIGNED;
+    fa::DeviceInfo *di = nullptr;
+    if ((st = fa::current_device(&di, true)) != FA_OK) return st;
+    const Problem p{B, Hq, Hkv, N, d, causal ? 1 : 0, scale};
+    CUtensorMap tq, tk, tv;
+    if (!fa::encode_bf16(&tq, Q, d, N, 1LL * B * Hq, 128) ||
+        !fa::encode_bf16(&tk, K, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tv, V, d, N, 1LL * B * Hkv, 128))
+        return FA_ERR_CUDA;
+    return fa::from_cuda(fa::launch_fwd_split_bf16(p, tq, tk, tv, O_parts, LSE_parts, num_splits,
+                                                   di->status, stream));
+}
+
+fa_status fa_merge(const float *O_parts, const float *LSE_parts, int num_parts, long long rows,
+                   int d, void *O, int o_bf16, float *LSE, cudaStream_t stream) {
+    if (num_parts < 1 || num_parts > FA_MAX_SPLITS || rows < 1 || d < 4 || d % 4 != 0 || d > 1024)
+        return FA_ERR_INVALID_ARG;
+    if (!fa::aligned16(O_parts) || !fa::aligned16(LSE_parts) || !fa::aligned16(O) ||
+        !fa::aligned16(LSE))
+        return FA_ERR_MISALIGNED;
+    fa::DeviceInfo *di = nullptr;
+    fa_status st = fa::current_device(&di, true);
+    if (st != FA_OK) return st;
+    return fa::from_cuda(
+        fa::launch_merge(O_parts, LSE_parts, num_parts, rows, d, O, o_bf16 != 0, LSE, stream));
+}
+
 fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
                  const float *LSE, void *dQ, void *dK, void *dV, int B, int Hq, int Hkv, int N,
                  int d, int causal, float scale, void *workspace, size_t workspace_bytes,

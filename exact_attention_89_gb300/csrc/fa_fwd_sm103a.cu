@@ -75,32 +75,41 @@ __device__ __forceinline__ void rescale_o_row(uint32_t tO, float alpha) {
     tmem_wait_st();
 }
 
-// One work item = two 128-row query tiles (a "pair") of one (batch, head).
+// One work item = two 128-row query tiles (a "pair") of one (batch, head) against one range of key
+// blocks: all of them, or split sp of S contiguous ranges (split-KV partial results).
 struct Item {
-    int bh, bkv, q0[2], nblk[2], nmax;
+    int bh, bkv, split, jb0, q0[2], nblk[2], nmax;   // nblk: key blocks of each tile in the range
 };
 
-template <bool CAUSAL>
-__device__ __forceinline__ Item decode_item(int k, int Hq, int Hkv, int N, int BH) {
-    // Items are numbered longest-first: under causal masking the late pairs (most key blocks) of
-    // every head come first.
+template <bool CAUSAL, bool SPLIT>
+__device__ __forceinline__ Item decode_item(int k, int Hq, int Hkv, int N, int BH, int S) {
+    // Items are numbered split by split, longest-first inside a split: under causal masking the
+    // late pairs (most key blocks) of every head come first.
     const int n_pairs = (N + 2 * BM - 1) / (2 * BM);
+    const int per_split = n_pairs * BH;
     Item it;
-    it.bh = k % BH;
-    int pair = k / BH;
+    it.split = SPLIT ? k / per_split : 0;
+    const int kk = k - it.split * per_split;
+    it.bh = kk % BH;
+    int pair = kk / BH;
     if (CAUSAL) pair = n_pairs - 1 - pair;
     const int hq = it.bh % Hq, b = it.bh / Hq;
     it.bkv = b * Hkv + hq / (Hq / Hkv);
     const int nkb = (N + BN - 1) / BN;
+    const int bps = SPLIT ? (nkb + S - 1) / S : nkb;
+    it.jb0 = it.split * bps;
+    const int jb1 = SPLIT ? min(nkb, it.jb0 + bps) : nkb;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
         it.q0[t] = pair * 2 * BM + t * BM;
+        int full;
         if (it.q0[t] >= N)
-            it.nblk[t] = 0;
+            full = 0;
         else if (CAUSAL)
-            it.nblk[t] = min(nkb, (min(it.q0[t] + BM, N) - 1) / BN + 1);
+            full = min(nkb, (min(it.q0[t] + BM, N) - 1) / BN + 1);
         else
-            it.nblk[t] = nkb;
+            full = nkb;
+        it.nblk[t] = max(0, min(full, jb1) - it.jb0);
     }
     it.nmax = max(it.nblk[0], it.nblk[1]);
     return it;
@@ -113,11 +122,14 @@ __device__ __forceinline__ int item_index(int r) {
     return r * G + ((r & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x));
 }
 
-template <int D, bool CAUSAL>
+// SPLIT = false: O (bf16) and LSE of the whole key range.  SPLIT = true: for each of S key
+// ranges, the partial result over that range alone as fp32 O_parts [S, B*Hq, N, d] and
+// LSE_parts [S, B*Hq, N] (LSE = -inf where a row has no allowed key in the range).
+template <int D, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
-               float *__restrict__ LSE, int Hq, int Hkv, int N, int BH, int n_items,
+               const __grid_constant__ CUtensorMap tmV, void *__restrict__ Out,
+               float *__restrict__ LSE, int Hq, int Hkv, int N, int BH, int n_items, int S,
                float scale_log2, unsigned *status) {
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -181,9 +193,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int q_issued = 0;
             bool ok = true;
             for (int r = 0; r < n_mine && ok; ++r) {
-                const Item it = decode_item<CAUSAL>(item_index(r), Hq, Hkv, N, BH);
+                const Item it = decode_item<CAUSAL, SPLIT>(item_index(r), Hq, Hkv, N, BH, S);
+                if (it.nmax == 0) continue;               // no key block of the range: no work
                 // Q buffer: free once every S product of the previous item has completed
-                if (r > 0 && !mbar_wait(q_empty, (r - 1) & 1, abort_flag, status)) { ok = false; break; }
+                if (q_issued > 0 && !mbar_wait(q_empty, (q_issued - 1) & 1, abort_flag, status)) { ok = false; break; }
                 const int ntiles = it.nblk[1] > 0 ? 2 : 1;
                 mbar_arrive_expect_tx(q_full, ntiles * L::TILE_BYTES);
                 ++q_issued;
@@ -192,7 +205,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tma_load_3d(smem + L::Q_OFF + t * L::TILE_BYTES + ch * L::CHUNK_BYTES, &tmQ,
                                     ch * 64, it.q0[t], it.bh, q_full);
                 for (int e = 0; e < 2 * it.nmax; ++e) {
-                    const int idx = base + e, j = e >> 1, st = idx % NS, rnd = idx / NS;
+                    const int idx = base + e, j = it.jb0 + (e >> 1), st = idx % NS, rnd = idx / NS;
                     if (!mbar_wait(&kv_empty[st], (rnd & 1) ^ 1, abort_flag, status)) { ok = false; break; }
 #ifdef FA_FAULT_INJECT
                     // Test builds only: CTA 0 never delivers its first K block, so the MMA warp's
@@ -245,9 +258,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int pb[2] = {0, 0};                 // blocks consumed per tile (p_full phases)
             int of[2] = {0, 0};                 // items finished per tile (o_full / o_empty phases)
             bool ok = true;
+            int qn = 0;                         // items with work so far (q_full phases)
             for (int r = 0; r < n_mine && ok; ++r) {
-                const Item it = decode_item<CAUSAL>(item_index(r), Hq, Hkv, N, BH);
-                ok = mbar_wait(q_full, r & 1, abort_flag, status) &&
+                const Item it = decode_item<CAUSAL, SPLIT>(item_index(r), Hq, Hkv, N, BH, S);
+                if (it.nmax == 0) continue;
+                ok = mbar_wait(q_full, qn & 1, abort_flag, status) &&
                      mbar_wait(&kv_full[base % NS], (base / NS) & 1, abort_flag, status);
                 if (!ok) break;
                 tc_fence_after();
@@ -297,6 +312,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int t = 0; t < 2; ++t)
                     if (it.nblk[t] > 0) ++of[t];
                 base += 2 * it.nmax;
+                ++qn;
             }
             // Nothing issued may still be running when TMEM is released.
             mma_commit(mma_done);
@@ -322,11 +338,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int of = 0;                                 // items finished by this tile (o_full phases)
         bool ok = true;
         for (int r = 0; r < n_mine && ok; ++r) {
-            const Item it = decode_item<CAUSAL>(item_index(r), Hq, Hkv, N, BH);
+            const Item it = decode_item<CAUSAL, SPLIT>(item_index(r), Hq, Hkv, N, BH, S);
             const int nb = it.nblk[t];
-            if (nb == 0) continue;
             const int q0 = it.q0[t];
             const int rq = q0 + row;                // query index
+            if (nb == 0) {
+                // Split-KV: these rows have no allowed key in the range; the merge skips them.
+                if (SPLIT && rq < N)
+                    LSE[(static_cast<size_t>(it.split) * BH + it.bh) * N + rq] = -INFINITY;
+                continue;
+            }
             // l: sum of the fp32 weights (gives LSE).  lc: rounding residual bf16(p) - p of each
             // block's largest weight, the dominant part of (sum of the bf16 weights that P V
             // applies) - l; O is divided by l + lc so the applied weights sum to one when one
@@ -342,7 +363,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 float s[128];
 #pragma unroll
                 for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sraw[c]);
-                const int kbase = j * BN;
+                const int kbase = (it.jb0 + j) * BN;
                 const bool need_mask = (CAUSAL && kbase + BN - 1 > q0) || (kbase + BN > N);
                 if (need_mask) {
 #pragma unroll
@@ -410,24 +431,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ++of;
             tc_fence_after();
             const float inv_l = 1.f / (l + lc);
-            __nv_bfloat16 *orow = O + (static_cast<size_t>(it.bh) * N + rq) * D;
+            const size_t orow_idx = ((SPLIT ? static_cast<size_t>(it.split) * BH : 0) + it.bh) *
+                                        static_cast<size_t>(N) + rq;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
                 tmem_ld_x32(tO + c0, o);
                 if (rq < N) {
+                    if constexpr (SPLIT) {
+                        float *orow = static_cast<float *>(Out) + orow_idx * D;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv_l, __uint_as_float(o[8 * u + 1]) * inv_l);
-                        v.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv_l, __uint_as_float(o[8 * u + 3]) * inv_l);
-                        v.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv_l, __uint_as_float(o[8 * u + 5]) * inv_l);
-                        v.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv_l, __uint_as_float(o[8 * u + 7]) * inv_l);
-                        *reinterpret_cast<uint4 *>(orow + c0 + 8 * u) = v;
+                        for (int u = 0; u < 8; ++u) {
+                            float4 v;
+                            v.x = __uint_as_float(o[4 * u + 0]) * inv_l;
+                            v.y = __uint_as_float(o[4 * u + 1]) * inv_l;
+                            v.z = __uint_as_float(o[4 * u + 2]) * inv_l;
+                            v.w = __uint_as_float(o[4 * u + 3]) * inv_l;
+                            *reinterpret_cast<float4 *>(orow + c0 + 4 * u) = v;
+                        }
+                    } else {
+                        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(Out) + orow_idx * D;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv_l, __uint_as_float(o[8 * u + 1]) * inv_l);
+                            v.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv_l, __uint_as_float(o[8 * u + 3]) * inv_l);
+                            v.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv_l, __uint_as_float(o[8 * u + 5]) * inv_l);
+                            v.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv_l, __uint_as_float(o[8 * u + 7]) * inv_l);
+                            *reinterpret_cast<uint4 *>(orow + c0 + 8 * u) = v;
+                        }
                     }
                 }
             }
-            if (rq < N) LSE[static_cast<size_t>(it.bh) * N + rq] = (m + log2f(l)) * LN2;
+            if (rq < N) LSE[orow_idx] = (m + log2f(l)) * LN2;
             tc_fence_before();
             mbar_arrive(&o_empty[t]);
         }
@@ -436,11 +472,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPLIT>
 cudaError_t launch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
-                   const CUtensorMap &tmV, void *O, float *LSE, unsigned *status,
+                   const CUtensorMap &tmV, void *Out, float *LSE, int S, unsigned *status,
                    cudaStream_t stream) {
-    auto kern = fwd_kernel<D, CAUSAL>;
+    auto kern = fwd_kernel<D, CAUSAL, SPLIT>;
     const int smem = Layout<D>::BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -451,15 +487,27 @@ cudaError_t launch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &
     if (attr.numRegs * NUM_THREADS < REGS_NEEDED) return cudaErrorInvalidConfiguration;
     const int BH = p.B * p.Hq;
     const long long n_pairs = (p.N + 2 * BM - 1) / (2 * BM);
-    const long long n_items = n_pairs * BH;
+    const long long n_items = n_pairs * BH * S;
     if (n_items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     // persistent: one CTA per SM (TMEM and shared memory allow no second one)
     const int grid = static_cast<int>(std::min<long long>(n_items, num_sms()));
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
-    kern<<<grid, NUM_THREADS, smem, stream>>>(tmQ, tmK, tmV, static_cast<__nv_bfloat16 *>(O), LSE,
-                                              p.Hq, p.Hkv, p.N, BH, static_cast<int>(n_items),
-                                              scale_log2, status);
+    kern<<<grid, NUM_THREADS, smem, stream>>>(tmQ, tmK, tmV, Out, LSE, p.Hq, p.Hkv, p.N, BH,
+                                              static_cast<int>(n_items), S, scale_log2, status);
     return cudaGetLastError();
+}
+
+template <bool SPLIT>
+cudaError_t dispatch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                     const CUtensorMap &tmV, void *Out, float *LSE, int S, unsigned *status,
+                     cudaStream_t stream) {
+    if (p.d == 128)
+        return p.causal ? launch<128, true, SPLIT>(p, tmQ, tmK, tmV, Out, LSE, S, status, stream)
+                        : launch<128, false, SPLIT>(p, tmQ, tmK, tmV, Out, LSE, S, status, stream);
+    if (p.d == 64)
+        return p.causal ? launch<64, true, SPLIT>(p, tmQ, tmK, tmV, Out, LSE, S, status, stream)
+                        : launch<64, false, SPLIT>(p, tmQ, tmK, tmV, Out, LSE, S, status, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace fwd
@@ -467,13 +515,13 @@ cudaError_t launch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &
 cudaError_t launch_fwd_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                             const CUtensorMap &tmV, void *O, float *LSE, unsigned *status,
                             cudaStream_t stream) {
-    if (p.d == 128)
-        return p.causal ? fwd::launch<128, true>(p, tmQ, tmK, tmV, O, LSE, status, stream)
-                        : fwd::launch<128, false>(p, tmQ, tmK, tmV, O, LSE, status, stream);
-    if (p.d == 64)
-        return p.causal ? fwd::launch<64, true>(p, tmQ, tmK, tmV, O, LSE, status, stream)
-                        : fwd::launch<64, false>(p, tmQ, tmK, tmV, O, LSE, status, stream);
-    return cudaErrorInvalidValue;
+    return fwd::dispatch<false>(p, tmQ, tmK, tmV, O, LSE, 1, status, stream);
+}
+
+cudaError_t launch_fwd_split_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                                  const CUtensorMap &tmV, float *O_parts, float *LSE_parts,
+                                  int num_splits, unsigned *status, cudaStream_t stream) {
+    return fwd::dispatch<true>(p, tmQ, tmK, tmV, O_parts, LSE_parts, num_splits, status, stream);
 }
 
 }  // namespace fa

@@ -23,6 +23,16 @@ cudaError_t launch_fwd_bf16(const Problem &p, const CUtensorMap &tmQ, const CUte
                             const CUtensorMap &tmV, void *O, float *LSE, unsigned *status,
                             cudaStream_t stream);
 
+// K1 split-KV variant: num_splits contiguous ranges of key blocks, each giving an fp32 partial
+// O_parts [S, B*Hq, N, d] and LSE_parts [S, B*Hq, N] (-inf for rows with no key in the range).
+cudaError_t launch_fwd_split_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                                  const CUtensorMap &tmV, float *O_parts, float *LSE_parts,
+                                  int num_splits, unsigned *status, cudaStream_t stream);
+
+// K6: merge of S partials per row into O (bf16 or fp32) and LSE.
+cudaError_t launch_merge(const float *O_parts, const float *LSE_parts, int S, long long rows, int d,
+                         void *O, bool out_bf16, float *LSE, cudaStream_t stream);
+
 // K2: D = rowsum(dO * O) in fp32 and zeroing of the fp32 dQ accumulator.
 cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const void *dO, float *D,
                                        float *dQacc, cudaStream_t stream);

@@ -6,9 +6,9 @@ fallback: if ``libflashattn.so`` is missing or the GPU is not sm_103, calls fail
 
 Low-level functions (same names and argument order as ``include/flashattn.h``):
     fa_fwd, fa_bwd, fa_bwd_workspace_bytes, fa_fwd_fp32, fa_bwd_fp32,
-    fa_get_device_status, fa_status_string, fa_bwd_noalloc
+    fa_get_device_status, fa_status_string, fa_bwd_noalloc, fa_fwd_split, fa_merge
 Convenience wrappers that allocate outputs with torch:
-    attention_forward, attention_backward
+    attention_forward, attention_backward, attention_forward_split
 """
 from __future__ import annotations
 
@@ -32,7 +32,11 @@ FA_ERR_DEVICE_BOUNDS = 7
 
 # Every symbol include/flashattn.h declares.
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_fp32", "fa_bwd_fp32",
-            "fa_get_device_status", "fa_status_string", "fa_bwd_noalloc")
+            "fa_get_device_status", "fa_status_string", "fa_bwd_noalloc", "fa_fwd_split",
+            "fa_merge")
+
+# Largest number of key ranges fa_fwd_split / fa_merge accept (FA_MAX_SPLITS).
+MAX_SPLITS = 256
 
 # Size of the fixed device scratch fa_bwd_noalloc uses (FA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -74,6 +78,10 @@ def lib() -> ctypes.CDLL:
             L.fa_status_string.restype = ctypes.c_char_p
             L.fa_bwd_noalloc.argtypes = [vp] * 9 + dims + [vp]
             L.fa_bwd_noalloc.restype = i
+            L.fa_fwd_split.argtypes = [vp] * 5 + dims + [i, vp]
+            L.fa_fwd_split.restype = i
+            L.fa_merge.argtypes = [vp, vp, i, ctypes.c_longlong, i, vp, i, vp, vp]
+            L.fa_merge.restype = i
             _lib = L
     return _lib
 
@@ -139,6 +147,27 @@ def fa_bwd_noalloc(Q, K, V, O, dO, LSE, dQ, dK, dV, causal: bool, scale: float, 
     return _check(st, "fa_bwd_noalloc", check)
 
 
+def fa_fwd_split(Q, K, V, O_parts, LSE_parts, causal: bool, scale: float, num_splits: int,
+                 stream=None, check: bool = True) -> int:
+    """Partial results of num_splits key ranges: O_parts fp32 [S,B,Hq,N,d], LSE_parts fp32
+    [S,B,Hq,N] (-inf where a row has no key in the range)."""
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    st = lib().fa_fwd_split(_ptr(Q), _ptr(K), _ptr(V), _ptr(O_parts), _ptr(LSE_parts), B, Hq,
+                            Hkv, N, d, int(bool(causal)), float(scale), int(num_splits),
+                            _stream(stream))
+    return _check(st, "fa_fwd_split", check)
+
+
+def fa_merge(O_parts, LSE_parts, O, LSE, stream=None, check: bool = True) -> int:
+    """O, LSE <- merge of the parts along dim 0; O bf16 or fp32 by its dtype."""
+    S = O_parts.shape[0]
+    d = O_parts.shape[-1]
+    rows = LSE_parts.numel() // S if S > 0 else 0
+    st = lib().fa_merge(_ptr(O_parts), _ptr(LSE_parts), int(S), int(rows), int(d), _ptr(O),
+                        int(O.dtype == torch.bfloat16), _ptr(LSE), _stream(stream))
+    return _check(st, "fa_merge", check)
+
+
 def fa_fwd_fp32(Q, K, V, O, LSE, causal: bool, scale: float, stream=None, check: bool = True):
     B, Hq, Hkv, N, d = _dims(Q, K)
     st = lib().fa_fwd_fp32(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d,
@@ -170,6 +199,24 @@ def attention_forward(Q, K, V, causal: bool, scale: float | None = None, stream=
     LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=Q.device)
     f = fa_fwd_fp32 if Q.dtype == torch.float32 else fa_fwd
     f(Q, K, V, O, LSE, causal, scale, stream)
+    return O, LSE
+
+
+def attention_forward_split(Q, K, V, causal: bool, scale: float | None = None,
+                            num_splits: int = 2, stream=None, return_parts: bool = False):
+    """bf16 forward as fa_fwd_split over num_splits key ranges followed by fa_merge; returns O
+    (bf16) and LSE, plus the partials when return_parts is set."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(Q.shape[-1])
+    B, Hq, N, d = Q.shape
+    O_parts = torch.empty((num_splits, B, Hq, N, d), dtype=torch.float32, device=Q.device)
+    LSE_parts = torch.empty((num_splits, B, Hq, N), dtype=torch.float32, device=Q.device)
+    fa_fwd_split(Q, K, V, O_parts, LSE_parts, causal, scale, num_splits, stream)
+    O = torch.empty_like(Q)
+    LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=Q.device)
+    fa_merge(O_parts, LSE_parts, O, LSE, stream)
+    if return_parts:
+        return O, LSE, O_parts, LSE_parts
     return O, LSE
 
 

@@ -26,6 +26,7 @@ class Workload:
     dtype: torch.dtype
     backward: bool
     q_mult: float = 1.0
+    num_splits: int = 1          # key ranges of the split-KV forward (1: the one-pass forward)
 
     @property
     def scale(self) -> float:
@@ -41,7 +42,7 @@ class Workload:
         return 2.5 * self.flops_fwd()
 
 
-# The five workloads of the method's evaluation plan.
+# The five workloads of the method's evaluation plan, and one for the split-KV forward.
 WORKLOADS = {
     "tiny_fp32": Workload("tiny_fp32", 1, 1, 1, 256, 64, False, 0, torch.float32, True),
     "fwd_d64": Workload("fwd_d64", 4, 16, 16, 1024, 64, False, 1, torch.bfloat16, False),
@@ -49,6 +50,10 @@ WORKLOADS = {
     "gqa_n8192": Workload("gqa_n8192", 1, 32, 8, 8192, 128, True, 3, torch.bfloat16, True),
     "long_n32768": Workload("long_n32768", 1, 16, 16, 32768, 128, True, 4, torch.bfloat16, True,
                             q_mult=4.0),
+    # One head over a long causal sequence: its 128 (256-query) items fill fewer SMs than a
+    # GB300 has, the case the split-KV forward (num_splits key ranges + merge) is for.
+    "splitkv_n32768": Workload("splitkv_n32768", 1, 1, 1, 32768, 128, True, 5, torch.bfloat16,
+                               False, num_splits=4),
 }
 
 

@@ -64,6 +64,45 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
                  int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                  cudaStream_t stream);
 
+/* Largest number of key ranges fa_fwd_split and fa_merge accept. */
+#define FA_MAX_SPLITS 256
+
+/*
+ * Split-KV forward: the keys are cut into num_splits contiguous ranges and each range gives a
+ * partial result on its own, to be combined by fa_merge.  Defined by the update of m, l and O
+ * after each key block (FlashAttention DAC'24 reading note, paper.adslab.icu, Methods), applied
+ * once more across ranges; a plain average of the range results would be wrong (FlashAttention
+ * note, paweldubiel.com, on why each block's output needs its normaliser).  It spreads a
+ * problem with few (batch, head, 256-query) items over more SMs.
+ *   Q, K, V: bf16 as in fa_fwd; d must be 64 or 128; 1 <= num_splits <= FA_MAX_SPLITS.
+ *   The N keys are cut in 128-key blocks; range s covers blocks [s*c, min((s+1)*c, nb)) with
+ *   nb = ceil(N/128) and c = ceil(nb/num_splits) (ranges past the end are empty).
+ *   O_parts [num_splits, B*Hq, N, d] fp32: range s's attention output over its keys alone,
+ *     normalised over that range; unspecified for rows whose LSE_parts entry is -inf.
+ *   LSE_parts [num_splits, B*Hq, N] fp32: natural-log log-sum-exp of the scaled scores over the
+ *     range's allowed keys; -inf where a row has none (a range wholly after the row under the
+ *     causal mask, or an empty range).
+ *   Both caller-owned, 16-byte aligned, written entirely (O_parts only where LSE is finite).
+ *   Errors as for fa_fwd, plus FA_ERR_INVALID_ARG for num_splits out of range.
+ */
+fa_status fa_fwd_split(const void *Q, const void *K, const void *V, float *O_parts,
+                       float *LSE_parts, int B, int Hq, int Hkv, int N, int d, int causal,
+                       float scale, int num_splits, cudaStream_t stream);
+
+/*
+ * Merge of partial attention results over disjoint key sets, row by row:
+ *     LSE = ln sum_s e^{LSE_s},   O = sum_s e^{LSE_s - LSE} O_s
+ * (the same reading-note update of m, l and O, in log-sum-exp form).  Parts with LSE_s = -inf
+ * are skipped (their O_s is not read); a row whose parts are all -inf gets O = 0, LSE = -inf.
+ *   O_parts [num_parts, rows, d] fp32 and LSE_parts [num_parts, rows] fp32 (the layout
+ *   fa_fwd_split writes, with rows = B*Hq*N); 1 <= num_parts <= FA_MAX_SPLITS.
+ *   O [rows, d]: bf16 when o_bf16 != 0 (the dtype fa_fwd writes), else fp32.  LSE [rows] fp32.
+ *   d a multiple of 4, 4 <= d <= 1024.  All pointers 16-byte aligned device memory.
+ *   Runs on the CUDA cores in fp32; computes in place of nothing (outputs must not alias inputs).
+ */
+fa_status fa_merge(const float *O_parts, const float *LSE_parts, int num_parts, long long rows,
+                   int d, void *O, int o_bf16, float *LSE, cudaStream_t stream);
+
 /*
  * Bytes of device workspace fa_bwd and fa_bwd_fp32 need: D [B,Hq,N] fp32 followed (at a
  * 256-byte boundary) by the fp32 dQ accumulator [B,Hq,N,d].  Returns 0 for invalid sizes.

@@ -101,6 +101,39 @@ def test_backward_rejects_invalid_arguments(built_lib, fp32):
     assert bwd(L, ws=MIS, fp32=fp32) == E.FA_ERR_WORKSPACE
 
 
+def test_split_forward_rejects_invalid_arguments(built_lib):
+    L = built_lib.lib()
+    E = built_lib
+
+    def split(Q=A, K=A, V=A, Op=A, Lp=A, B=1, Hq=2, Hkv=1, N=300, d=128, S=3, scale=0.1):
+        return L.fa_fwd_split(Q, K, V, Op, Lp, B, Hq, Hkv, N, d, 1, scale, S, None)
+
+    assert split(B=0) == E.FA_ERR_INVALID_ARG
+    assert split(Hq=3, Hkv=2) == E.FA_ERR_INVALID_ARG
+    assert split(scale=math.nan) == E.FA_ERR_INVALID_ARG
+    assert split(S=0) == E.FA_ERR_INVALID_ARG
+    assert split(S=E.MAX_SPLITS + 1) == E.FA_ERR_INVALID_ARG
+    assert split(d=96) == E.FA_ERR_UNSUPPORTED
+    for k in ("Q", "K", "V", "Op", "Lp"):
+        assert split(**{k: None}) == E.FA_ERR_MISALIGNED
+        assert split(**{k: MIS}) == E.FA_ERR_MISALIGNED
+
+
+def test_merge_rejects_invalid_arguments(built_lib):
+    L = built_lib.lib()
+    E = built_lib
+
+    def merge(Op=A, Lp=A, S=2, rows=4, d=8, O=A, bf16=1, Lo=A):
+        return L.fa_merge(Op, Lp, S, rows, d, O, bf16, Lo, None)
+
+    for kw in ({"S": 0}, {"S": E.MAX_SPLITS + 1}, {"rows": 0}, {"d": 0}, {"d": 6},
+               {"d": 1028}):
+        assert merge(**kw) == E.FA_ERR_INVALID_ARG, kw
+    for k in ("Op", "Lp", "O", "Lo"):
+        assert merge(**{k: None}) == E.FA_ERR_MISALIGNED
+        assert merge(**{k: MIS}) == E.FA_ERR_MISALIGNED
+
+
 def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     """The binding never falls back: a missing library is an error, not a CPU path."""
     from exact_attention_89_gb300 import flashattn
