@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             for (int r = 0; r < n_mine && ok; ++r) {
                 const Item it = decode_item<CAUSAL, SPLIT>(item_index(r), Hq, Hkv, N, BH, S);
-                if (it.nmax == 0) continue;               // no key block of the range: no work
+                if (SPLIT && it.nmax == 0) continue;     // no key block of the range: no work
                 // Q buffer: free once every S product of the previous item has completed
                 if (q_issued > 0 && !mbar_wait(q_empty, (q_issued - 1) & 1, abort_flag, status)) { ok = false; break; }
                 const int ntiles = it.nblk[1] > 0 ? 2 : 1;
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int qn = 0;                         // items with work so far (q_full phases)
             for (int r = 0; r < n_mine && ok; ++r) {
                 const Item it = decode_item<CAUSAL, SPLIT>(item_index(r), Hq, Hkv, N, BH, S);
-                if (it.nmax == 0) continue;
+                if (SPLIT && it.nmax == 0) continue;
                 ok = mbar_wait(q_full, qn & 1, abort_flag, status) &&
                      mbar_wait(&kv_full[base % NS], (base / NS) & 1, abort_flag, status);
                 if (!ok) break;
