@@ -33,12 +33,13 @@ sys.path.insert(0, ROOT)
 WORKLOAD = "causal_n4096"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic per launch of the dominant launch sequence from one ncu capture, keyed by the
-# sha256 of the kernel sources it was taken on; reported as null once the sources change.
+# DRAM traffic per launch of the reported kernel from one ncu capture, keyed by
+# "<kernel file>:<sha256 prefix of that file and fa_ptx.cuh>:<workload>"; a key that no longer
+# matches the sources (the kernel changed since the capture) reports null.
 NCU_TRAFFIC = {
     # fa_bwd on causal_n4096: bwd_main 1.917 GB read + 0.990 GB write, bwd_preprocess 0.210 GB,
     # bwd_dq_convert 0.164 GB (profiles/bwd_main_kernel_causal_n4096.md)
-    "14243a636aa449c0": 3.28e9,
+    "fa_bwd_sm103a.cu:5648148527b57a99:causal_n4096": 3.28e9,
 }
 
 
@@ -49,14 +50,14 @@ def split_key_ranges(N: int, S: int):
     return [(min(N, s * c * 128), min(N, (s + 1) * c * 128)) for s in range(S)]
 
 
-def kernel_sources_hash() -> str:
+def kernel_sources_hash(kernel_file: str) -> str:
+    """Key prefix for NCU_TRAFFIC: the kernel's source file and the device primitives it uses."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_89_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + f.read())
-    return h.hexdigest()[:16]
+    for fn in (kernel_file, "fa_ptx.cuh"):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return "%s:%s" % (kernel_file, h.hexdigest()[:16])
 
 
 def load_peaks():
@@ -442,7 +443,8 @@ def main():
     # ---------------------------------------------------------------- roofline + cpu baseline
     peaks, peaks_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
-    src_hash = kernel_sources_hash()
+    fwd_key = kernel_sources_hash("fa_fwd_sm103a.cu") + ":" + w.name
+    bwd_key = kernel_sources_hash("fa_bwd_sm103a.cu") + ":" + w.name
     peak_source = ("%s burst bf16 (MEASURED_PEAKS.json)" % peaks_src if peaks_src == "measured"
                    else "fallback 1.9 PFLOP/s bf16")
     fwd_achieved = w.flops_fwd() / (first_ms * 1e-3) / 1e12
@@ -457,28 +459,28 @@ def main():
         merge_gbs = merge_bytes / (second_ms * 1e-3) / 1e9
         roofline = {"bound": "tensor", "kernel": "fa_fwd_split", "achieved": fwd_achieved,
                     "peak": peak, "unit": "TFLOP/s", "frac": fwd_achieved / peak,
-                    "traffic": NCU_TRAFFIC.get(src_hash + ":" + w.name), "peak_source": peak_source,
+                    "traffic": NCU_TRAFFIC.get(fwd_key), "peak_source": peak_source,
                     "flops_per_launch": w.flops_fwd(), "ms": first_ms,
                     "merge": {"kernel": "fa_merge", "bound": "hbm", "unit": "GB/s",
                               "bytes_per_launch": merge_bytes, "ms": second_ms,
                               "achieved": merge_gbs, "peak": hbm, "frac": merge_gbs / hbm},
-                    "one_pass_fwd_ms": one_pass_ms, "sources": src_hash}
+                    "one_pass_fwd_ms": one_pass_ms, "sources": fwd_key}
     elif w.backward:
         bwd_achieved = w.flops_bwd() / (second_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "kernel": "fa_bwd (bwd_main + preprocess + dq_convert)",
                     "achieved": bwd_achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": bwd_achieved / peak,
-                    "traffic": NCU_TRAFFIC.get(src_hash), "peak_source": peak_source,
+                    "traffic": NCU_TRAFFIC.get(bwd_key), "peak_source": peak_source,
                     "flops_per_launch": w.flops_bwd(),
                     "fwd": {"kernel": "fa_fwd", "achieved": fwd_achieved,
                             "frac": fwd_achieved / peak, "ms": first_ms,
                             "flops_per_launch": w.flops_fwd()},
-                    "bwd_ms": second_ms, "sources": src_hash}
+                    "bwd_ms": second_ms, "sources": bwd_key}
     else:
         roofline = {"bound": "tensor", "kernel": "fa_fwd", "achieved": fwd_achieved,
                     "peak": peak, "unit": "TFLOP/s", "frac": fwd_achieved / peak,
-                    "traffic": NCU_TRAFFIC.get(src_hash + ":" + w.name), "peak_source": peak_source,
-                    "flops_per_launch": w.flops_fwd(), "ms": first_ms, "sources": src_hash}
+                    "traffic": NCU_TRAFFIC.get(fwd_key), "peak_source": peak_source,
+                    "flops_per_launch": w.flops_fwd(), "ms": first_ms, "sources": fwd_key}
     cpu = None
     if rank == 0 and ws == 1 and args.cpu_budget > 0 and not args.no_extras:
         r = cpu_oracle_sample(w, args.cpu_budget, w.B * w.Hq)

@@ -83,15 +83,16 @@ struct Item {
 
 template <bool CAUSAL, bool SPLIT>
 __device__ __forceinline__ Item decode_item(int k, int Hq, int Hkv, int N, int BH, int S) {
-    // Items are numbered split by split, longest-first inside a split: under causal masking the
-    // late pairs (most key blocks) of every head come first.
+    // Items are numbered longest-first: under causal masking the late pairs (most key blocks)
+    // of every head come first.  With S ranges the ranges of one pair are adjacent, so the
+    // full-length ranges of the late pairs lead and the short last ranges of the early pairs
+    // come at the end.
     const int n_pairs = (N + 2 * BM - 1) / (2 * BM);
-    const int per_split = n_pairs * BH;
     Item it;
-    it.split = SPLIT ? k / per_split : 0;
-    const int kk = k - it.split * per_split;
-    it.bh = kk % BH;
-    int pair = kk / BH;
+    it.bh = k % BH;
+    const int rest = k / BH;
+    it.split = SPLIT ? rest % S : 0;
+    int pair = SPLIT ? rest / S : rest;
     if (CAUSAL) pair = n_pairs - 1 - pair;
     const int hq = it.bh % Hq, b = it.bh / Hq;
     it.bkv = b * Hkv + hq / (Hq / Hkv);
