@@ -31,6 +31,7 @@ _lib = None
 _D = ctypes.POINTER(ctypes.c_double)
 _I = ctypes.POINTER(ctypes.c_int)
 _L = ctypes.POINTER(ctypes.c_int64)
+_U8 = ctypes.POINTER(ctypes.c_uint8)
 
 
 def build(force: bool = False) -> str:
@@ -59,10 +60,21 @@ def _load():
             lib.oracle_attention_forward_keys.argtypes = common + [_D, _D, _D, ctypes.c_int, ctypes.c_int,
                                                                    ctypes.c_int, _I, _D, _D]
             lib.oracle_merge_partials.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, _D, _D, _D, _D]
+            masked = [ctypes.c_int] * 6 + [_I, _I, _U8, ctypes.c_int, ctypes.c_int, ctypes.c_double]
+            lib.oracle_attention_forward_masked.argtypes = masked + [_D, _D, _D, ctypes.c_int, _I, _D, _D]
+            lib.oracle_attention_backward_masked.argtypes = masked + [_D, _D, _D, _D, ctypes.c_int, _I,
+                                                                      _D, _D, _D]
+            lib.oracle_forward_rows_masked.argtypes = masked + [_D, _D, _D, ctypes.c_int, _L, _D, _D]
+            lib.oracle_backward_dq_rows_masked.argtypes = masked + [_D, _D, _D, _D, ctypes.c_int, _L, _D]
+            lib.oracle_backward_dkv_cols_masked.argtypes = masked + [_D, _D, _D, _D, ctypes.c_int, _L,
+                                                                     _D, _D]
             for name in ("oracle_attention_forward", "oracle_attention_backward",
                          "oracle_forward_rows", "oracle_backward_dq_rows",
                          "oracle_backward_dkv_cols", "oracle_num_threads",
-                         "oracle_attention_forward_keys", "oracle_merge_partials"):
+                         "oracle_attention_forward_keys", "oracle_merge_partials",
+                         "oracle_attention_forward_masked", "oracle_attention_backward_masked",
+                         "oracle_forward_rows_masked", "oracle_backward_dq_rows_masked",
+                         "oracle_backward_dkv_cols_masked"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -215,3 +227,109 @@ def merge_partials(O_parts, LSE_parts):
     rc = _load().oracle_merge_partials(S, rows, d, _ptr(O_parts), _ptr(LSE_parts), _ptr(O), _ptr(L))
     _check(rc, "oracle_merge_partials")
     return O, L
+
+
+# ----------------------------------------------------------------------------- general masks
+class Mask:
+    """A general mask (see attention_oracle.c): per-batch valid query / key lengths q_len, k_len
+    ([B] ints, None = all N) and a 0/1 block mask [mask_heads, nb, nb] over block x block tiles
+    (None = all tiles), on top of the causal rule."""
+
+    def __init__(self, q_len=None, k_len=None, block_mask=None, block: int = 128):
+        self.q_len = None if q_len is None else np.ascontiguousarray(np.asarray(q_len, np.int32))
+        self.k_len = None if k_len is None else np.ascontiguousarray(np.asarray(k_len, np.int32))
+        self.block_mask = (None if block_mask is None
+                           else np.ascontiguousarray(np.asarray(block_mask, np.uint8)))
+        self.block = int(block)
+
+    def args(self, causal):
+        """ctypes arguments (causal, q_len, k_len, block_mask, mask_heads, block)."""
+        bm = self.block_mask
+        return (int(bool(causal)),
+                None if self.q_len is None else _ptr(self.q_len, _I),
+                None if self.k_len is None else _ptr(self.k_len, _I),
+                None if bm is None else _ptr(bm, _U8),
+                0 if bm is None else int(bm.shape[0]), self.block)
+
+
+def forward_masked(Q, K, V, causal: bool, scale: float, mask: Mask, heads=None):
+    """forward() under a general mask: (O [B, Hq, N, d], LSE [B, Hq, N]) for all heads, or
+    ([nh, N, d], [nh, N]) for the listed heads."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, Hq, Hkv, N, d = _shape(Q, K)
+    full = heads is None
+    hs = np.ascontiguousarray(np.arange(B * Hq, dtype=np.int32) if full
+                              else np.asarray(heads, dtype=np.int32))
+    O = np.zeros((len(hs), N, d))
+    L = np.zeros((len(hs), N))
+    rc = _load().oracle_attention_forward_masked(B, Hq, Hkv, N, d, *mask.args(causal), float(scale),
+                                                 _ptr(Q), _ptr(K), _ptr(V), len(hs), _ptr(hs, _I),
+                                                 _ptr(O), _ptr(L))
+    _check(rc, "oracle_attention_forward_masked")
+    if full:
+        return O.reshape(B, Hq, N, d), L.reshape(B, Hq, N)
+    return O, L
+
+
+def backward_masked(Q, K, V, dO, causal: bool, scale: float, mask: Mask, groups=None):
+    """backward() under a general mask (same return shapes as backward())."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, Hq, Hkv, N, d = _shape(Q, K)
+    G = Hq // Hkv
+    full = groups is None
+    gs = np.ascontiguousarray(np.arange(B * Hkv, dtype=np.int32) if full
+                              else np.asarray(groups, dtype=np.int32))
+    ng = len(gs)
+    dQ = np.zeros((ng, G, N, d))
+    dK = np.zeros((ng, N, d))
+    dV = np.zeros((ng, N, d))
+    rc = _load().oracle_attention_backward_masked(B, Hq, Hkv, N, d, *mask.args(causal),
+                                                  float(scale), _ptr(Q), _ptr(K), _ptr(V),
+                                                  _ptr(dO), ng, _ptr(gs, _I), _ptr(dQ), _ptr(dK),
+                                                  _ptr(dV))
+    _check(rc, "oracle_attention_backward_masked")
+    if full:
+        return dQ.reshape(B, Hq, N, d), dK.reshape(B, Hkv, N, d), dV.reshape(B, Hkv, N, d)
+    return dQ, dK, dV
+
+
+def forward_rows_masked(Q, K, V, causal: bool, scale: float, mask: Mask, rows):
+    """forward_rows() under a general mask."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, Hq, Hkv, N, d = _shape(Q, K)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    O = np.zeros((len(rows), d))
+    L = np.zeros(len(rows))
+    rc = _load().oracle_forward_rows_masked(B, Hq, Hkv, N, d, *mask.args(causal), float(scale),
+                                            _ptr(Q), _ptr(K), _ptr(V), len(rows), _ptr(rows, _L),
+                                            _ptr(O), _ptr(L))
+    _check(rc, "oracle_forward_rows_masked")
+    return O, L
+
+
+def backward_dq_rows_masked(Q, K, V, dO, causal: bool, scale: float, mask: Mask, rows):
+    """backward_dq_rows() under a general mask."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, Hq, Hkv, N, d = _shape(Q, K)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    dQ = np.zeros((len(rows), d))
+    rc = _load().oracle_backward_dq_rows_masked(B, Hq, Hkv, N, d, *mask.args(causal),
+                                                float(scale), _ptr(Q), _ptr(K), _ptr(V),
+                                                _ptr(dO), len(rows), _ptr(rows, _L), _ptr(dQ))
+    _check(rc, "oracle_backward_dq_rows_masked")
+    return dQ
+
+
+def backward_dkv_cols_masked(Q, K, V, dO, causal: bool, scale: float, mask: Mask, cols):
+    """backward_dkv_cols() under a general mask."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, Hq, Hkv, N, d = _shape(Q, K)
+    cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+    dK = np.zeros((len(cols), d))
+    dV = np.zeros((len(cols), d))
+    rc = _load().oracle_backward_dkv_cols_masked(B, Hq, Hkv, N, d, *mask.args(causal),
+                                                 float(scale), _ptr(Q), _ptr(K), _ptr(V),
+                                                 _ptr(dO), len(cols), _ptr(cols, _L), _ptr(dK),
+                                                 _ptr(dV))
+    _check(rc, "oracle_backward_dkv_cols_masked")
+    return dK, dV

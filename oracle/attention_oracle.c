@@ -33,9 +33,16 @@
  *  - GQA: FlashAttention note (paweldubiel.com), last section: grouped-query attention combines
  *    with the method.  Query head hq reads key/value head hq / (Hq / Hkv) (consecutive groups).
  *
+ *  - General masks (the *_masked entry points): the same rule, "the mask acts on each block of
+ *    QK^T" (reading note, "other operators"), with the allowed set of a pair (i, j) of head
+ *    (b, hq) being the AND of: the causal rule; i < q_len[b] and j < k_len[b] (per-batch valid
+ *    lengths of a padded batch, clamped to [0, N]); and block_mask[h][i / block][j / block] != 0
+ *    for a 0/1 mask over block x block tiles, h = 0, hq or b * Hq + hq when the mask holds 1,
+ *    Hq or B * Hq heads.  A row with no allowed key (every row i >= q_len[b], or one whose tiles
+ *    are all masked) gets O = 0 and LSE = -inf, and passes no gradient.
+ *
  * Layout: every tensor is contiguous [B, H, N, d] fp64 (d fastest); K, V, dK, dV use H = Hkv.
  * LSE is [B, Hq, N].  Causal means key j <= query i (top-left aligned, Nq = Nk = N).
- * A row with no allowed key (impossible with these masks) would get O = 0 and LSE = -inf.
  *
  * Parallelism: OpenMP over independent rows (or key columns); no blocking or reordering of the
  * sums beyond what the definition states.  Every function returns 0 on success, nonzero on
@@ -52,7 +59,50 @@
 
 typedef int64_t i64;
 
-static int is_allowed(int causal, i64 i, i64 j) { return !causal || j <= i; }
+/* Which (query i, key j) pairs are allowed; see the header.  NULL members mean "no limit". */
+typedef struct {
+    int causal;
+    const int *q_len, *k_len;          /* [B] */
+    const unsigned char *block_mask;   /* [mask_heads, nb, nb] */
+    int mask_heads, block, nb;
+    int B, Hq, N;
+} mask_t;
+
+static mask_t causal_only(int causal, int B, int Hq, int N) {
+    mask_t m = {causal, NULL, NULL, NULL, 0, 1, 1, B, Hq, N};
+    return m;
+}
+
+static i64 clamp_len(int len, int N) { return len < 0 ? 0 : (len > N ? N : len); }
+
+static int allowed(const mask_t *M, i64 b, i64 hq, i64 i, i64 j) {
+    if (M->causal && j > i) return 0;
+    if (M->q_len && i >= clamp_len(M->q_len[b], M->N)) return 0;
+    if (M->k_len && j >= clamp_len(M->k_len[b], M->N)) return 0;
+    if (M->block_mask) {
+        const i64 h = M->mask_heads == 1 ? 0
+                    : (M->mask_heads == M->B * M->Hq ? b * M->Hq + hq : hq);
+        if (!M->block_mask[(h * M->nb + i / M->block) * M->nb + j / M->block]) return 0;
+    }
+    return 1;
+}
+
+/* Builds the general mask; returns nonzero for an invalid mask description. */
+static int make_mask(mask_t *M, int causal, int B, int Hq, int N, const int *q_len,
+                     const int *k_len, const unsigned char *block_mask, int mask_heads, int block) {
+    *M = causal_only(causal, B, Hq, N);
+    M->q_len = q_len;
+    M->k_len = k_len;
+    if (block_mask) {
+        if (block < 1) return 1;
+        if (mask_heads != 1 && mask_heads != Hq && mask_heads != B * Hq) return 1;
+        M->block_mask = block_mask;
+        M->mask_heads = mask_heads;
+        M->block = block;
+        M->nb = (N + block - 1) / block;
+    }
+    return 0;
+}
 
 static double dot(const double *a, const double *b, int d) {
     double acc = 0.0;
@@ -78,11 +128,12 @@ int oracle_num_threads(void) {
  * One query row of one head: fills s_row[0..N) with the scores (-INFINITY where masked), turns it
  * into the probability row in place, writes o_row[0..d) and returns LSE_i.
  */
-static double softmax_row(const double *qi, const double *k, const double *v, i64 i, int N, int d,
-                          int causal, double scale, double *p_row, double *o_row) {
+static double softmax_row(const mask_t *M, i64 b, i64 hq, const double *qi, const double *k,
+                          const double *v, i64 i, int N, int d, double scale, double *p_row,
+                          double *o_row) {
     double m = -INFINITY;
     for (i64 j = 0; j < N; ++j) {
-        if (is_allowed(causal, i, j)) {
+        if (allowed(M, b, hq, i, j)) {
             p_row[j] = scale * dot(qi, k + j * d, d);
             if (p_row[j] > m) m = p_row[j];
         } else {
@@ -96,7 +147,7 @@ static double softmax_row(const double *qi, const double *k, const double *v, i6
     }
     double l = 0.0;
     for (i64 j = 0; j < N; ++j) {
-        double e = is_allowed(causal, i, j) ? exp(p_row[j] - m) : 0.0;
+        double e = allowed(M, b, hq, i, j) ? exp(p_row[j] - m) : 0.0;
         p_row[j] = e;
         l += e;
     }
@@ -115,9 +166,9 @@ static double softmax_row(const double *qi, const double *k, const double *v, i6
  *   heads[h] = b * Hq + hq.  O_out is [nheads, N, d], LSE_out is [nheads, N].
  *   P_out (optional, may be NULL) receives the probability matrices [nheads, N, N].
  */
-int oracle_attention_forward(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
-                             const double *Q, const double *K, const double *V, int nheads,
-                             const int *heads, double *O_out, double *LSE_out, double *P_out) {
+static int forward_impl(const mask_t *M, int B, int Hq, int Hkv, int N, int d, double scale,
+                        const double *Q, const double *K, const double *V, int nheads,
+                        const int *heads, double *O_out, double *LSE_out, double *P_out) {
     if (check_shape(B, Hq, Hkv, N, d) || nheads < 0) return 1;
     const int G = Hq / Hkv;
     const i64 nn = (i64)N * N, nd = (i64)N * d;
@@ -133,11 +184,32 @@ int oracle_attention_forward(int B, int Hq, int Hkv, int N, int d, int causal, d
         double *Ph = P_out ? P_out + (i64)h * nn : P;
 #pragma omp parallel for schedule(dynamic, 16)
         for (i64 i = 0; i < N; ++i)
-            LSE_out[(i64)h * N + i] = softmax_row(q + i * d, k, v, i, N, d, causal, scale,
+            LSE_out[(i64)h * N + i] = softmax_row(M, b, hq, q + i * d, k, v, i, N, d, scale,
                                                   Ph + i * N, O_out + (i64)h * nd + i * d);
     }
     free(P);
     return 0;
+}
+
+int oracle_attention_forward(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
+                             const double *Q, const double *K, const double *V, int nheads,
+                             const int *heads, double *O_out, double *LSE_out, double *P_out) {
+    const mask_t M = causal_only(causal, B, Hq, N);
+    return forward_impl(&M, B, Hq, Hkv, N, d, scale, Q, K, V, nheads, heads, O_out, LSE_out, P_out);
+}
+
+/* oracle_attention_forward under the general mask (see the header). */
+int oracle_attention_forward_masked(int B, int Hq, int Hkv, int N, int d, int causal,
+                                    const int *q_len, const int *k_len,
+                                    const unsigned char *block_mask, int mask_heads, int block,
+                                    double scale, const double *Q, const double *K,
+                                    const double *V, int nheads, const int *heads, double *O_out,
+                                    double *LSE_out) {
+    mask_t M;
+    if (check_shape(B, Hq, Hkv, N, d) ||
+        make_mask(&M, causal, B, Hq, N, q_len, k_len, block_mask, mask_heads, block))
+        return 1;
+    return forward_impl(&M, B, Hq, Hkv, N, d, scale, Q, K, V, nheads, heads, O_out, LSE_out, NULL);
 }
 
 /*
@@ -169,7 +241,7 @@ int oracle_attention_forward_keys(int B, int Hq, int Hkv, int N, int d, int caus
                 double *o = O_out + (i64)h * nd + i * d;
                 double m = -INFINITY;
                 for (i64 j = 0; j < N; ++j) {
-                    const int ok = is_allowed(causal, i, j) && j >= key_begin && j < key_end;
+                    const int ok = (!causal || j <= i) && j >= key_begin && j < key_end;
                     p[j] = ok ? scale * dot(q, k + j * d, d) : -INFINITY;
                     if (p[j] > m) m = p[j];
                 }
@@ -229,10 +301,10 @@ int oracle_merge_partials(int S, i64 rows, int d, const double *O_parts, const d
  *   groups[g] = b * Hkv + hk.  dQ_out is [ngroups, G, N, d] (the group's query heads in order),
  *   dK_out and dV_out are [ngroups, N, d].  O and D come from the oracle's own fp64 forward.
  */
-int oracle_attention_backward(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
-                              const double *Q, const double *K, const double *V, const double *dO,
-                              int ngroups, const int *groups, double *dQ_out, double *dK_out,
-                              double *dV_out) {
+static int backward_impl(const mask_t *M, int B, int Hq, int Hkv, int N, int d, double scale,
+                         const double *Q, const double *K, const double *V, const double *dO,
+                         int ngroups, const int *groups, double *dQ_out, double *dK_out,
+                         double *dV_out) {
     if (check_shape(B, Hq, Hkv, N, d) || ngroups < 0) return 1;
     const int G = Hq / Hkv;
     const i64 nn = (i64)N * N, nd = (i64)N * d;
@@ -256,7 +328,7 @@ int oracle_attention_backward(int B, int Hq, int Hkv, int N, int d, int causal, 
             /* forward: P, O, then D_i = <dO_i, O_i> */
 #pragma omp parallel for schedule(dynamic, 16)
             for (i64 i = 0; i < N; ++i) {
-                softmax_row(q + i * d, k, v, i, N, d, causal, scale, P + i * N, O + i * d);
+                softmax_row(M, b, hq, q + i * d, k, v, i, N, d, scale, P + i * N, O + i * d);
                 D[i] = dot(dor + i * d, O + i * d, d);
             }
             /* dV_j += sum_i P_ij dO_i  (parallel over key columns j) */
@@ -294,13 +366,38 @@ int oracle_attention_backward(int B, int Hq, int Hkv, int N, int d, int causal, 
     return 0;
 }
 
+int oracle_attention_backward(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
+                              const double *Q, const double *K, const double *V, const double *dO,
+                              int ngroups, const int *groups, double *dQ_out, double *dK_out,
+                              double *dV_out) {
+    const mask_t M = causal_only(causal, B, Hq, N);
+    return backward_impl(&M, B, Hq, Hkv, N, d, scale, Q, K, V, dO, ngroups, groups, dQ_out,
+                         dK_out, dV_out);
+}
+
+/* oracle_attention_backward under the general mask (see the header). */
+int oracle_attention_backward_masked(int B, int Hq, int Hkv, int N, int d, int causal,
+                                     const int *q_len, const int *k_len,
+                                     const unsigned char *block_mask, int mask_heads, int block,
+                                     double scale, const double *Q, const double *K,
+                                     const double *V, const double *dO, int ngroups,
+                                     const int *groups, double *dQ_out, double *dK_out,
+                                     double *dV_out) {
+    mask_t M;
+    if (check_shape(B, Hq, Hkv, N, d) ||
+        make_mask(&M, causal, B, Hq, N, q_len, k_len, block_mask, mask_heads, block))
+        return 1;
+    return backward_impl(&M, B, Hq, Hkv, N, d, scale, Q, K, V, dO, ngroups, groups, dQ_out,
+                         dK_out, dV_out);
+}
+
 /*
  * Sampled forward rows: rows[r] = (b * Hq + hq) * N + i.  O_rows is [nrows, d], LSE_rows [nrows].
  * Each row materialises its own score/probability row; cost O(N d) per row.
  */
-int oracle_forward_rows(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
-                        const double *Q, const double *K, const double *V, int nrows,
-                        const i64 *rows, double *O_rows, double *LSE_rows) {
+static int forward_rows_impl(const mask_t *M, int B, int Hq, int Hkv, int N, int d, double scale,
+                             const double *Q, const double *K, const double *V, int nrows,
+                             const i64 *rows, double *O_rows, double *LSE_rows) {
     if (check_shape(B, Hq, Hkv, N, d) || nrows < 0) return 1;
     const int G = Hq / Hkv;
     const i64 nd = (i64)N * d;
@@ -315,7 +412,7 @@ int oracle_forward_rows(int B, int Hq, int Hkv, int N, int d, int causal, double
             const i64 bh = idx / N, i = idx % N;
             const i64 b = bh / Hq, hq = bh % Hq, hk = hq / G;
             const double *k = K + (b * Hkv + hk) * nd, *v = V + (b * Hkv + hk) * nd;
-            LSE_rows[r] = softmax_row(Q + bh * nd + i * d, k, v, i, N, d, causal, scale, p,
+            LSE_rows[r] = softmax_row(M, b, hq, Q + bh * nd + i * d, k, v, i, N, d, scale, p,
                                       O_rows + (i64)r * d);
         }
         free(p);
@@ -323,10 +420,29 @@ int oracle_forward_rows(int B, int Hq, int Hkv, int N, int d, int causal, double
     return bad;
 }
 
+int oracle_forward_rows(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
+                        const double *Q, const double *K, const double *V, int nrows,
+                        const i64 *rows, double *O_rows, double *LSE_rows) {
+    const mask_t M = causal_only(causal, B, Hq, N);
+    return forward_rows_impl(&M, B, Hq, Hkv, N, d, scale, Q, K, V, nrows, rows, O_rows, LSE_rows);
+}
+
+int oracle_forward_rows_masked(int B, int Hq, int Hkv, int N, int d, int causal, const int *q_len,
+                               const int *k_len, const unsigned char *block_mask, int mask_heads,
+                               int block, double scale, const double *Q, const double *K,
+                               const double *V, int nrows, const i64 *rows, double *O_rows,
+                               double *LSE_rows) {
+    mask_t M;
+    if (check_shape(B, Hq, Hkv, N, d) ||
+        make_mask(&M, causal, B, Hq, N, q_len, k_len, block_mask, mask_heads, block))
+        return 1;
+    return forward_rows_impl(&M, B, Hq, Hkv, N, d, scale, Q, K, V, nrows, rows, O_rows, LSE_rows);
+}
+
 /* Sampled dQ rows (same row encoding as oracle_forward_rows). dQ_rows is [nrows, d]. */
-int oracle_backward_dq_rows(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
-                            const double *Q, const double *K, const double *V, const double *dO,
-                            int nrows, const i64 *rows, double *dQ_rows) {
+static int dq_rows_impl(const mask_t *M, int B, int Hq, int Hkv, int N, int d, double scale,
+                        const double *Q, const double *K, const double *V, const double *dO,
+                        int nrows, const i64 *rows, double *dQ_rows) {
     if (check_shape(B, Hq, Hkv, N, d) || nrows < 0) return 1;
     const int G = Hq / Hkv;
     const i64 nd = (i64)N * d;
@@ -343,7 +459,7 @@ int oracle_backward_dq_rows(int B, int Hq, int Hkv, int N, int d, int causal, do
             const i64 b = bh / Hq, hq = bh % Hq, hk = hq / G;
             const double *k = K + (b * Hkv + hk) * nd, *v = V + (b * Hkv + hk) * nd;
             const double *doi = dO + bh * nd + i * d;
-            softmax_row(Q + bh * nd + i * d, k, v, i, N, d, causal, scale, p, o);
+            softmax_row(M, b, hq, Q + bh * nd + i * d, k, v, i, N, d, scale, p, o);
             const double Di = dot(doi, o, d);
             double *dq = dQ_rows + (i64)r * d;
             for (int c = 0; c < d; ++c) dq[c] = 0.0;
@@ -359,14 +475,34 @@ int oracle_backward_dq_rows(int B, int Hq, int Hkv, int N, int d, int causal, do
     return bad;
 }
 
+int oracle_backward_dq_rows(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
+                            const double *Q, const double *K, const double *V, const double *dO,
+                            int nrows, const i64 *rows, double *dQ_rows) {
+    const mask_t M = causal_only(causal, B, Hq, N);
+    return dq_rows_impl(&M, B, Hq, Hkv, N, d, scale, Q, K, V, dO, nrows, rows, dQ_rows);
+}
+
+int oracle_backward_dq_rows_masked(int B, int Hq, int Hkv, int N, int d, int causal,
+                                   const int *q_len, const int *k_len,
+                                   const unsigned char *block_mask, int mask_heads, int block,
+                                   double scale, const double *Q, const double *K,
+                                   const double *V, const double *dO, int nrows, const i64 *rows,
+                                   double *dQ_rows) {
+    mask_t M;
+    if (check_shape(B, Hq, Hkv, N, d) ||
+        make_mask(&M, causal, B, Hq, N, q_len, k_len, block_mask, mask_heads, block))
+        return 1;
+    return dq_rows_impl(&M, B, Hq, Hkv, N, d, scale, Q, K, V, dO, nrows, rows, dQ_rows);
+}
+
 /*
  * Sampled dK / dV rows: cols[r] = (b * Hkv + hk) * N + j.  dK_rows and dV_rows are [ncols, d].
  * First a row pass computes LSE_i and D_i for every query row of each touched KV group (one
  * group at a time), then each key column recomputes P_ij = exp(s_ij - LSE_i) and dS_ij.
  */
-int oracle_backward_dkv_cols(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
-                             const double *Q, const double *K, const double *V, const double *dO,
-                             int ncols, const i64 *cols, double *dK_rows, double *dV_rows) {
+static int dkv_cols_impl(const mask_t *M, int B, int Hq, int Hkv, int N, int d, double scale,
+                         const double *Q, const double *K, const double *V, const double *dO,
+                         int ncols, const i64 *cols, double *dK_rows, double *dV_rows) {
     if (check_shape(B, Hq, Hkv, N, d) || ncols < 0) return 1;
     const int G = Hq / Hkv;
     const i64 nd = (i64)N * d;
@@ -391,8 +527,8 @@ int oracle_backward_dkv_cols(int B, int Hq, int Hkv, int N, int d, int causal, d
 #pragma omp for schedule(dynamic, 16)
                 for (i64 i = 0; i < N; ++i) {
                     if (!p || !o) { bad = 2; continue; }
-                    LSE[(i64)g * N + i] = softmax_row(Q + bh * nd + i * d, k, v, i, N, d, causal,
-                                                      scale, p, o);
+                    LSE[(i64)g * N + i] = softmax_row(M, b, hk * G + g, Q + bh * nd + i * d, k, v,
+                                                      i, N, d, scale, p, o);
                     D[(i64)g * N + i] = dot(dO + bh * nd + i * d, o, d);
                 }
                 free(p); free(o);
@@ -410,7 +546,7 @@ int oracle_backward_dkv_cols(int B, int Hq, int Hkv, int N, int d, int causal, d
                 const i64 bh = b * Hq + hk * G + g;
                 const double *q = Q + bh * nd, *dor = dO + bh * nd;
                 for (i64 i = 0; i < N; ++i) {
-                    if (!is_allowed(causal, i, j)) continue;
+                    if (!allowed(M, b, hk * G + g, i, j)) continue;
                     const double lse = LSE[(i64)g * N + i];
                     if (lse == -INFINITY) continue;
                     const double pij = exp(scale * dot(q + i * d, k + j * d, d) - lse);
@@ -425,4 +561,24 @@ int oracle_backward_dkv_cols(int B, int Hq, int Hkv, int N, int d, int causal, d
     }
     free(LSE); free(D); free(done);
     return bad;
+}
+
+int oracle_backward_dkv_cols(int B, int Hq, int Hkv, int N, int d, int causal, double scale,
+                             const double *Q, const double *K, const double *V, const double *dO,
+                             int ncols, const i64 *cols, double *dK_rows, double *dV_rows) {
+    const mask_t M = causal_only(causal, B, Hq, N);
+    return dkv_cols_impl(&M, B, Hq, Hkv, N, d, scale, Q, K, V, dO, ncols, cols, dK_rows, dV_rows);
+}
+
+int oracle_backward_dkv_cols_masked(int B, int Hq, int Hkv, int N, int d, int causal,
+                                    const int *q_len, const int *k_len,
+                                    const unsigned char *block_mask, int mask_heads, int block,
+                                    double scale, const double *Q, const double *K,
+                                    const double *V, const double *dO, int ncols, const i64 *cols,
+                                    double *dK_rows, double *dV_rows) {
+    mask_t M;
+    if (check_shape(B, Hq, Hkv, N, d) ||
+        make_mask(&M, causal, B, Hq, N, q_len, k_len, block_mask, mask_heads, block))
+        return 1;
+    return dkv_cols_impl(&M, B, Hq, Hkv, N, d, scale, Q, K, V, dO, ncols, cols, dK_rows, dV_rows);
 }
