@@ -157,6 +157,52 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
     return fa::from_cuda(fa::launch_fwd_bf16(p, tq, tk, tv, O, LSE, di->status, stream));
 }
 
+}  // extern "C"
+
+namespace fa {
+namespace {
+// Host checks of a general mask; fills the kernel's MaskArgs.
+fa_status check_mask(int B, int Hq, const int *q_len, const int *k_len,
+                     const unsigned char *block_mask, int mask_heads, MaskArgs *mk) {
+    if ((q_len && (reinterpret_cast<uintptr_t>(q_len) & 3u)) ||
+        (k_len && (reinterpret_cast<uintptr_t>(k_len) & 3u)))
+        return FA_ERR_MISALIGNED;
+    if (block_mask && mask_heads != 1 && mask_heads != Hq && mask_heads != B * Hq)
+        return FA_ERR_INVALID_ARG;
+    mk->q_len = q_len;
+    mk->k_len = k_len;
+    mk->block_mask = block_mask;
+    mk->mask_heads = block_mask ? mask_heads : 0;
+    return FA_OK;
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_fwd_masked(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                        int Hq, int Hkv, int N, int d, int causal, float scale, const int *q_len,
+                        const int *k_len, const unsigned char *block_mask, int mask_heads,
+                        cudaStream_t stream) {
+    fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!fa::aligned16(Q) || !fa::aligned16(K) || !fa::aligned16(V) || !fa::aligned16(O) ||
+        !fa::aligned16(LSE))
+        return FA_ERR_MISALIGNED;
+    fa::MaskArgs mk;
+    if ((st = fa::check_mask(B, Hq, q_len, k_len, block_mask, mask_heads, &mk)) != FA_OK) return st;
+    fa::DeviceInfo *di = nullptr;
+    if ((st = fa::current_device(&di, true)) != FA_OK) return st;
+    const Problem p{B, Hq, Hkv, N, d, causal ? 1 : 0, scale};
+    CUtensorMap tq, tk, tv;
+    if (!fa::encode_bf16(&tq, Q, d, N, 1LL * B * Hq, 128) ||
+        !fa::encode_bf16(&tk, K, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tv, V, d, N, 1LL * B * Hkv, 128))
+        return FA_ERR_CUDA;
+    return fa::from_cuda(fa::launch_fwd_masked_bf16(p, tq, tk, tv, O, LSE, mk, di->status, stream));
+}
+
 fa_status fa_fwd_split(const void *Q, const void *K, const void *V, float *O_parts,
                        float *LSE_parts, int B, int Hq, int Hkv, int N, int d, int causal,
                        float scale, int num_splits, cudaStream_t stream) {

@@ -77,12 +77,17 @@ __device__ __forceinline__ void rescale_o_row(uint32_t tO, float alpha) {
 
 // One work item = two 128-row query tiles (a "pair") of one (batch, head) against one range of key
 // blocks: all of them, or split sp of S contiguous ranges (split-KV partial results).
+// Under a general mask (MASK) the valid lengths bound the range and a tile mask row decides which
+// of its blocks a tile takes; the pair still shares one K/V stream (the union of both tiles').
 struct Item {
     int bh, bkv, split, jb0, q0[2], nblk[2], nmax;   // nblk: key blocks of each tile in the range
+    int lq, lk;                                     // valid query rows / keys of the batch (MASK)
+    const uint8_t *row[2];                          // tile mask row of each tile, or null (MASK)
 };
 
-template <bool CAUSAL, bool SPLIT>
-__device__ __forceinline__ Item decode_item(int k, int Hq, int Hkv, int N, int BH, int S) {
+template <bool CAUSAL, bool SPLIT, bool MASK>
+__device__ __forceinline__ Item decode_item(int k, int Hq, int Hkv, int N, int BH, int S,
+                                            const MaskArgs &mk) {
     // Items are numbered longest-first: under causal masking the late pairs (most key blocks)
     // of every head come first.  With S ranges the ranges of one pair are adjacent, so the
     // full-length ranges of the late pairs lead and the short last ranges of the early pairs
@@ -97,23 +102,68 @@ __device__ __forceinline__ Item decode_item(int k, int Hq, int Hkv, int N, int B
     const int hq = it.bh % Hq, b = it.bh / Hq;
     it.bkv = b * Hkv + hq / (Hq / Hkv);
     const int nkb = (N + BN - 1) / BN;
+    it.lq = N;
+    it.lk = N;
+    if (MASK) {
+        if (mk.q_len) it.lq = min(max(__ldg(mk.q_len + b), 0), N);
+        if (mk.k_len) it.lk = min(max(__ldg(mk.k_len + b), 0), N);
+    }
+    const int nkb_lim = MASK ? (it.lk + BN - 1) / BN : nkb;
     const int bps = SPLIT ? (nkb + S - 1) / S : nkb;
     it.jb0 = it.split * bps;
-    const int jb1 = SPLIT ? min(nkb, it.jb0 + bps) : nkb;
+    const int jb1 = SPLIT ? min(nkb, it.jb0 + bps) : nkb_lim;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
         it.q0[t] = pair * 2 * BM + t * BM;
         int full;
-        if (it.q0[t] >= N)
+        if (it.q0[t] >= (MASK ? it.lq : N))
             full = 0;
         else if (CAUSAL)
-            full = min(nkb, (min(it.q0[t] + BM, N) - 1) / BN + 1);
+            full = min(nkb_lim, (min(it.q0[t] + BM, N) - 1) / BN + 1);
         else
-            full = nkb;
+            full = nkb_lim;
         it.nblk[t] = max(0, min(full, jb1) - it.jb0);
+        it.row[t] = nullptr;
+        if (MASK && mk.block_mask && it.nblk[t] > 0) {
+            const int h = mk.mask_heads == 1 ? 0 : (mk.mask_heads == BH ? it.bh : hq);
+            it.row[t] = mk.block_mask + (static_cast<size_t>(h) * nkb + it.q0[t] / BM) * nkb;
+        }
     }
     it.nmax = max(it.nblk[0], it.nblk[1]);
     return it;
+}
+
+// Does tile t take key block jj (relative to the item's range)?  Without MASK every block of its
+// prefix; with MASK also only those its tile mask row keeps.
+template <bool MASK>
+__device__ __forceinline__ bool takes(const Item &it, int t, int jj) {
+    if (!MASK) return jj < it.nblk[t];
+    return jj < it.nblk[t] && (it.row[t] == nullptr || __ldg(it.row[t] + jj) != 0);
+}
+
+// First block >= jj that tile t takes, or it.nblk[t].
+template <bool MASK>
+__device__ __forceinline__ int next_of_tile(const Item &it, int t, int jj) {
+    if (!MASK) return jj;
+    while (jj < it.nblk[t] && !takes<MASK>(it, t, jj)) ++jj;
+    return min(jj, it.nblk[t]);
+}
+
+// First block >= jj that either tile takes (the pair's K/V stream), or it.nmax.
+template <bool MASK>
+__device__ __forceinline__ int next_of_pair(const Item &it, int jj) {
+    if (!MASK) return jj;
+    while (jj < it.nmax && !takes<MASK>(it, 0, jj) && !takes<MASK>(it, 1, jj)) ++jj;
+    return min(jj, it.nmax);
+}
+
+// Last block tile t takes, or -1.
+template <bool MASK>
+__device__ __forceinline__ int last_of_tile(const Item &it, int t) {
+    int jj = it.nblk[t] - 1;
+    if (MASK)
+        while (jj >= 0 && !takes<MASK>(it, t, jj)) --jj;
+    return jj;
 }
 
 // The r-th item of this CTA: rounds of gridDim.x items, assigned in snake order (reversed on odd
@@ -126,12 +176,16 @@ __device__ __forceinline__ int item_index(int r) {
 // SPLIT = false: O (bf16) and LSE of the whole key range.  SPLIT = true: for each of S key
 // ranges, the partial result over that range alone as fp32 O_parts [S, B*Hq, N, d] and
 // LSE_parts [S, B*Hq, N] (LSE = -inf where a row has no allowed key in the range).
-template <int D, bool CAUSAL, bool SPLIT>
+// MASK = true: the general mask mk on top of the causal rule; rows with no allowed key (and rows
+// past the batch's valid length) get O = 0 and LSE = -inf.
+template <int D, bool CAUSAL, bool SPLIT, bool MASK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, void *__restrict__ Out,
                float *__restrict__ LSE, int Hq, int Hkv, int N, int BH, int n_items, int S,
-               float scale_log2, unsigned *status) {
+               float scale_log2, const MaskArgs mk, unsigned *status) {
+    static_assert(!(SPLIT && MASK), "the split-KV forward takes no general mask");
+    constexpr bool SKIP_EMPTY = SPLIT || MASK;      // items may have no key block at all
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -194,8 +248,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int q_issued = 0;
             bool ok = true;
             for (int r = 0; r < n_mine && ok; ++r) {
-                const Item it = decode_item<CAUSAL, SPLIT>(item_index(r), Hq, Hkv, N, BH, S);
-                if (SPLIT && it.nmax == 0) continue;     // no key block of the range: no work
+                const Item it = decode_item<CAUSAL, SPLIT, MASK>(item_index(r), Hq, Hkv, N, BH, S, mk);
+                const int jfirst = next_of_pair<MASK>(it, 0);
+                if (SKIP_EMPTY && jfirst >= it.nmax) continue;   // no key block: no work
                 // Q buffer: free once every S product of the previous item has completed
                 if (q_issued > 0 && !mbar_wait(q_empty, (q_issued - 1) & 1, abort_flag, status)) { ok = false; break; }
                 const int ntiles = it.nblk[1] > 0 ? 2 : 1;
@@ -205,22 +260,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int ch = 0; ch < D / 64; ++ch)
                         tma_load_3d(smem + L::Q_OFF + t * L::TILE_BYTES + ch * L::CHUNK_BYTES, &tmQ,
                                     ch * 64, it.q0[t], it.bh, q_full);
-                for (int e = 0; e < 2 * it.nmax; ++e) {
-                    const int idx = base + e, j = it.jb0 + (e >> 1), st = idx % NS, rnd = idx / NS;
-                    if (!mbar_wait(&kv_empty[st], (rnd & 1) ^ 1, abort_flag, status)) { ok = false; break; }
+                int e = 0;                            // ring slots of this item so far
+                for (int jj = jfirst; jj < it.nmax && ok; jj = next_of_pair<MASK>(it, jj + 1)) {
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const int idx = base + e, j = it.jb0 + jj, st = idx % NS, rnd = idx / NS;
+                        ++e;
+                        if (!mbar_wait(&kv_empty[st], (rnd & 1) ^ 1, abort_flag, status)) { ok = false; break; }
 #ifdef FA_FAULT_INJECT
-                    // Test builds only: CTA 0 never delivers its first K block, so the MMA warp's
-                    // bounded wait runs out, the CTA unwinds and FA_ERR_DEVICE_TIMEOUT is recorded.
-                    if (blockIdx.x == 0 && idx == 0) continue;
+                        // Test builds only: CTA 0 never delivers its first K block, so the MMA
+                        // warp's bounded wait runs out, the CTA unwinds and FA_ERR_DEVICE_TIMEOUT
+                        // is recorded.
+                        if (blockIdx.x == 0 && idx == 0) continue;
 #endif
-                    mbar_arrive_expect_tx(&kv_full[st], L::TILE_BYTES);
-                    uint8_t *dst = smem + L::KV_OFF + st * L::TILE_BYTES;
-                    const CUtensorMap *tm = (e & 1) ? &tmV : &tmK;
-                    for (int ch = 0; ch < D / 64; ++ch)
-                        tma_load_3d(dst + ch * L::CHUNK_BYTES, tm, ch * 64, j * BN, it.bkv, &kv_full[st]);
-                    issued = idx + 1;                 // ring index after the last load issued
+                        mbar_arrive_expect_tx(&kv_full[st], L::TILE_BYTES);
+                        uint8_t *dst = smem + L::KV_OFF + st * L::TILE_BYTES;
+                        const CUtensorMap *tm = kv ? &tmV : &tmK;
+                        for (int ch = 0; ch < D / 64; ++ch)
+                            tma_load_3d(dst + ch * L::CHUNK_BYTES, tm, ch * 64, j * BN, it.bkv, &kv_full[st]);
+                        issued = idx + 1;             // ring index after the last load issued
+                    }
                 }
-                base += 2 * it.nmax;
+                base += e;
             }
             if (!ok || *abort_flag) {
                 // Unwinding: let copies still in flight land before the CTA's smem goes away.
@@ -248,21 +308,87 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 mma_commit(&s_full[t]);
             };
-            auto issue_pv = [&](int t, int st, int j) {
+            auto issue_pv = [&](int t, int st, bool accumulate) {
                 const uint64_t db = sdesc_add(dv0, st * L::TILE_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, sdesc_add(db, kk * 2048),
-                           IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                           IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
             };
             int base = 0;                       // K/V ring index of the current item's K_0
             int pb[2] = {0, 0};                 // blocks consumed per tile (p_full phases)
             int of[2] = {0, 0};                 // items finished per tile (o_full / o_empty phases)
             bool ok = true;
             int qn = 0;                         // items with work so far (q_full phases)
+            if constexpr (MASK) {
+            // Same issue order as below, over the blocks either tile takes: S of the next block of
+            // tile 0 goes between P V of tiles 0 and 1; each tile's first P V overwrites its O
+            // and its last one signals o_full; the item's last S products free the Q buffer.
             for (int r = 0; r < n_mine && ok; ++r) {
-                const Item it = decode_item<CAUSAL, SPLIT>(item_index(r), Hq, Hkv, N, BH, S);
-                if (SPLIT && it.nmax == 0) continue;
+                const Item it = decode_item<CAUSAL, SPLIT, MASK>(item_index(r), Hq, Hkv, N, BH, S, mk);
+                int u = next_of_pair<MASK>(it, 0);
+                if (u >= it.nmax) continue;
+                const int last0 = last_of_tile<MASK>(it, 0), last1 = last_of_tile<MASK>(it, 1);
+                const int ulast = max(last0, last1);
+                ok = mbar_wait(q_full, qn & 1, abort_flag, status) &&
+                     mbar_wait(&kv_full[base % NS], (base / NS) & 1, abort_flag, status);
+                if (!ok) break;
+                tc_fence_after();
+                for (int t = 0; t < 2; ++t)
+                    if (takes<MASK>(it, t, u)) issue_s(t, base % NS);
+                mma_commit(&kv_empty[base % NS]);
+                if (u == ulast) mma_commit(q_empty);
+                bool started[2] = {false, false};
+                int idx = base;                 // ring index of K_u
+                while (true) {
+                    const int vidx = idx + 1, kidx = idx + 2;
+                    const int vst = vidx % NS, kst = kidx % NS;
+                    const int un = (u == ulast) ? it.nmax : next_of_pair<MASK>(it, u + 1);
+                    const bool next = un < it.nmax;
+                    if (!mbar_wait(&kv_full[vst], (vidx / NS) & 1, abort_flag, status)) { ok = false; break; }
+                    if (takes<MASK>(it, 0, u)) {
+                        if (!started[0] && of[0] > 0 &&
+                            !mbar_wait(&o_empty[0], (of[0] - 1) & 1, abort_flag, status)) { ok = false; break; }
+                        if (!mbar_wait(&p_full[0], pb[0] & 1, abort_flag, status)) { ok = false; break; }
+                        ++pb[0];
+                        tc_fence_after();
+                        issue_pv(0, vst, started[0]);
+                        started[0] = true;
+                        if (u == last0) mma_commit(&o_full[0]);
+                    }
+                    if (next) {
+                        if (!mbar_wait(&kv_full[kst], (kidx / NS) & 1, abort_flag, status)) { ok = false; break; }
+                        tc_fence_after();
+                        if (takes<MASK>(it, 0, un)) issue_s(0, kst);
+                    }
+                    if (takes<MASK>(it, 1, u)) {
+                        if (!started[1] && of[1] > 0 &&
+                            !mbar_wait(&o_empty[1], (of[1] - 1) & 1, abort_flag, status)) { ok = false; break; }
+                        if (!mbar_wait(&p_full[1], pb[1] & 1, abort_flag, status)) { ok = false; break; }
+                        ++pb[1];
+                        tc_fence_after();
+                        issue_pv(1, vst, started[1]);
+                        started[1] = true;
+                        if (u == last1) mma_commit(&o_full[1]);
+                    }
+                    mma_commit(&kv_empty[vst]);
+                    if (!next) break;
+                    if (takes<MASK>(it, 1, un)) issue_s(1, kst);
+                    mma_commit(&kv_empty[kst]);
+                    if (un == ulast) mma_commit(q_empty);
+                    u = un;
+                    idx += 2;
+                }
+                if (!ok) break;
+                for (int t = 0; t < 2; ++t)
+                    if (started[t]) ++of[t];
+                base = idx + 2;
+                ++qn;
+            }
+            } else {
+            for (int r = 0; r < n_mine && ok; ++r) {
+                const Item it = decode_item<CAUSAL, SPLIT, MASK>(item_index(r), Hq, Hkv, N, BH, S, mk);
+                if (SKIP_EMPTY && it.nmax == 0) continue;
                 ok = mbar_wait(q_full, qn & 1, abort_flag, status) &&
                      mbar_wait(&kv_full[base % NS], (base / NS) & 1, abort_flag, status);
                 if (!ok) break;
@@ -284,7 +410,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (!mbar_wait(&p_full[0], pb[0] & 1, abort_flag, status)) { ok = false; break; }
                         ++pb[0];
                         tc_fence_after();
-                        issue_pv(0, vst, j);
+                        issue_pv(0, vst, j > 0);
                         if (j == nb0 - 1) mma_commit(&o_full[0]);
                     }
                     if (next) {
@@ -299,7 +425,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (!mbar_wait(&p_full[1], pb[1] & 1, abort_flag, status)) { ok = false; break; }
                         ++pb[1];
                         tc_fence_after();
-                        issue_pv(1, vst, j);
+                        issue_pv(1, vst, j > 0);
                         if (j == nb1 - 1) mma_commit(&o_full[1]);
                     }
                     mma_commit(&kv_empty[vst]);
@@ -314,6 +440,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (it.nblk[t] > 0) ++of[t];
                 base += 2 * it.nmax;
                 ++qn;
+            }
             }
             // Nothing issued may still be running when TMEM is released.
             mma_commit(mma_done);
@@ -339,14 +466,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int of = 0;                                 // items finished by this tile (o_full phases)
         bool ok = true;
         for (int r = 0; r < n_mine && ok; ++r) {
-            const Item it = decode_item<CAUSAL, SPLIT>(item_index(r), Hq, Hkv, N, BH, S);
+            const Item it = decode_item<CAUSAL, SPLIT, MASK>(item_index(r), Hq, Hkv, N, BH, S, mk);
             const int nb = it.nblk[t];
             const int q0 = it.q0[t];
             const int rq = q0 + row;                // query index
-            if (nb == 0) {
+            const int jfirst = next_of_tile<MASK>(it, t, 0);
+            if (nb == 0 || (MASK && jfirst >= nb)) {
                 // Split-KV: these rows have no allowed key in the range; the merge skips them.
                 if (SPLIT && rq < N)
                     LSE[(static_cast<size_t>(it.split) * BH + it.bh) * N + rq] = -INFINITY;
+                // General mask: no allowed key at all, so O = 0 and LSE = -inf.
+                if (MASK && rq < N) {
+                    uint4 *orow = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(Out) +
+                                                            (static_cast<size_t>(it.bh) * N + rq) * D);
+#pragma unroll
+                    for (int u = 0; u < D / 8; ++u) orow[u] = make_uint4(0u, 0u, 0u, 0u);
+                    LSE[static_cast<size_t>(it.bh) * N + rq] = -INFINITY;
+                }
                 continue;
             }
             // l: sum of the fp32 weights (gives LSE).  lc: rounding residual bf16(p) - p of each
@@ -354,7 +490,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // applies) - l; O is divided by l + lc so the applied weights sum to one when one
             // weight dominates.
             float m = -INFINITY, l = 0.f, lc = 0.f;
-            for (int j = 0; j < nb; ++j) {
+            for (int j = jfirst, jj = 0; j < nb; j = next_of_tile<MASK>(it, t, j + 1), ++jj) {
                 ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], sb & 1, abort_flag, status));
                 if (!ok) break;
                 ++sb;
@@ -365,12 +501,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sraw[c]);
                 const int kbase = (it.jb0 + j) * BN;
-                const bool need_mask = (CAUSAL && kbase + BN - 1 > q0) || (kbase + BN > N);
+                const int kend = MASK ? it.lk : N;    // keys past the valid length are masked
+                const bool need_mask = (CAUSAL && kbase + BN - 1 > q0) || (kbase + BN > kend);
                 if (need_mask) {
 #pragma unroll
                     for (int c = 0; c < 128; ++c) {
                         const int key = kbase + c;
-                        if ((CAUSAL && key > rq) || key >= N) s[c] = -INFINITY;
+                        if ((CAUSAL && key > rq) || key >= kend) s[c] = -INFINITY;
                     }
                 }
                 // row max as a shallow tree of 3-input maxes (8 independent chains)
@@ -394,7 +531,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         lc *= alpha;
                         m = m_blk;
                     }
-                    if (j > 0) rescale_o_row<D>(tO, alpha);
+                    if ((MASK ? jj : j) > 0) rescale_o_row<D>(tO, alpha);
                 }
                 const float m_sub = (m == -INFINITY) ? 0.f : m;
                 // p = 2^(s c - m) on pairs: one packed FMA, two ex2, packed sums in 4 chains
@@ -431,7 +568,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!ok) break;
             ++of;
             tc_fence_after();
-            const float inv_l = 1.f / (l + lc);
+            // General mask: rows past the valid length, or left with no allowed key, give 0 / -inf.
+            const bool dead = MASK && (rq >= it.lq || !(l > 0.f));
+            const float inv_l = dead ? 0.f : 1.f / (l + lc);
             const size_t orow_idx = ((SPLIT ? static_cast<size_t>(it.split) * BH : 0) + it.bh) *
                                         static_cast<size_t>(N) + rq;
 #pragma unroll
@@ -452,6 +591,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     } else {
                         __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(Out) + orow_idx * D;
+                        if (MASK && dead) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = 0u;
+                        }
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             uint4 v;
@@ -464,7 +607,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            if (rq < N) LSE[orow_idx] = (m + log2f(l)) * LN2;
+            if (rq < N) LSE[orow_idx] = (MASK && dead) ? -INFINITY : (m + log2f(l)) * LN2;
             tc_fence_before();
             mbar_arrive(&o_empty[t]);
         }
@@ -473,11 +616,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, bool CAUSAL, bool SPLIT, bool MASK>
 cudaError_t launch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
-                   const CUtensorMap &tmV, void *Out, float *LSE, int S, unsigned *status,
-                   cudaStream_t stream) {
-    auto kern = fwd_kernel<D, CAUSAL, SPLIT>;
+                   const CUtensorMap &tmV, void *Out, float *LSE, int S, const MaskArgs &mk,
+                   unsigned *status, cudaStream_t stream) {
+    auto kern = fwd_kernel<D, CAUSAL, SPLIT, MASK>;
     const int smem = Layout<D>::BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -494,20 +637,20 @@ cudaError_t launch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &
     const int grid = static_cast<int>(std::min<long long>(n_items, num_sms()));
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     kern<<<grid, NUM_THREADS, smem, stream>>>(tmQ, tmK, tmV, Out, LSE, p.Hq, p.Hkv, p.N, BH,
-                                              static_cast<int>(n_items), S, scale_log2, status);
+                                              static_cast<int>(n_items), S, scale_log2, mk, status);
     return cudaGetLastError();
 }
 
-template <bool SPLIT>
+template <bool SPLIT, bool MASK>
 cudaError_t dispatch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
-                     const CUtensorMap &tmV, void *Out, float *LSE, int S, unsigned *status,
-                     cudaStream_t stream) {
+                     const CUtensorMap &tmV, void *Out, float *LSE, int S, const MaskArgs &mk,
+                     unsigned *status, cudaStream_t stream) {
     if (p.d == 128)
-        return p.causal ? launch<128, true, SPLIT>(p, tmQ, tmK, tmV, Out, LSE, S, status, stream)
-                        : launch<128, false, SPLIT>(p, tmQ, tmK, tmV, Out, LSE, S, status, stream);
+        return p.causal ? launch<128, true, SPLIT, MASK>(p, tmQ, tmK, tmV, Out, LSE, S, mk, status, stream)
+                        : launch<128, false, SPLIT, MASK>(p, tmQ, tmK, tmV, Out, LSE, S, mk, status, stream);
     if (p.d == 64)
-        return p.causal ? launch<64, true, SPLIT>(p, tmQ, tmK, tmV, Out, LSE, S, status, stream)
-                        : launch<64, false, SPLIT>(p, tmQ, tmK, tmV, Out, LSE, S, status, stream);
+        return p.causal ? launch<64, true, SPLIT, MASK>(p, tmQ, tmK, tmV, Out, LSE, S, mk, status, stream)
+                        : launch<64, false, SPLIT, MASK>(p, tmQ, tmK, tmV, Out, LSE, S, mk, status, stream);
     return cudaErrorInvalidValue;
 }
 
@@ -516,13 +659,20 @@ cudaError_t dispatch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap
 cudaError_t launch_fwd_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                             const CUtensorMap &tmV, void *O, float *LSE, unsigned *status,
                             cudaStream_t stream) {
-    return fwd::dispatch<false>(p, tmQ, tmK, tmV, O, LSE, 1, status, stream);
+    return fwd::dispatch<false, false>(p, tmQ, tmK, tmV, O, LSE, 1, MaskArgs{}, status, stream);
+}
+
+cudaError_t launch_fwd_masked_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                                   const CUtensorMap &tmV, void *O, float *LSE, const MaskArgs &mk,
+                                   unsigned *status, cudaStream_t stream) {
+    return fwd::dispatch<false, true>(p, tmQ, tmK, tmV, O, LSE, 1, mk, status, stream);
 }
 
 cudaError_t launch_fwd_split_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                                   const CUtensorMap &tmV, float *O_parts, float *LSE_parts,
                                   int num_splits, unsigned *status, cudaStream_t stream) {
-    return fwd::dispatch<true>(p, tmQ, tmK, tmV, O_parts, LSE_parts, num_splits, status, stream);
+    return fwd::dispatch<true, false>(p, tmQ, tmK, tmV, O_parts, LSE_parts, num_splits, MaskArgs{},
+                                      status, stream);
 }
 
 }  // namespace fa

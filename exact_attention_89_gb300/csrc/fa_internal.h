@@ -17,11 +17,25 @@ struct Problem {
     float scale;
 };
 
+// General mask of the masked entry points (device pointers; null members mean "no limit"):
+// per-batch valid query rows and keys, and a 0/1 mask over 128 x 128 tiles [mask_heads, nb, nb].
+struct MaskArgs {
+    const int *q_len = nullptr;
+    const int *k_len = nullptr;
+    const uint8_t *block_mask = nullptr;
+    int mask_heads = 0;
+};
+
 // K1: bf16 forward on tcgen05. Maps are 3-D [d, N, B*H] bf16, box [64, 128, 1], 128B swizzle;
 // O is written with plain stores.
 cudaError_t launch_fwd_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                             const CUtensorMap &tmV, void *O, float *LSE, unsigned *status,
                             cudaStream_t stream);
+
+// K1 under a general mask.
+cudaError_t launch_fwd_masked_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                                   const CUtensorMap &tmV, void *O, float *LSE, const MaskArgs &mk,
+                                   unsigned *status, cudaStream_t stream);
 
 // K1 split-KV variant: num_splits contiguous ranges of key blocks, each giving an fp32 partial
 // O_parts [S, B*Hq, N, d] and LSE_parts [S, B*Hq, N] (-inf for rows with no key in the range).

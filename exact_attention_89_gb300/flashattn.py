@@ -6,7 +6,8 @@ fallback: if ``libflashattn.so`` is missing or the GPU is not sm_103, calls fail
 
 Low-level functions (same names and argument order as ``include/flashattn.h``):
     fa_fwd, fa_bwd, fa_bwd_workspace_bytes, fa_fwd_fp32, fa_bwd_fp32,
-    fa_get_device_status, fa_status_string, fa_bwd_noalloc, fa_fwd_split, fa_merge
+    fa_get_device_status, fa_status_string, fa_bwd_noalloc, fa_fwd_split, fa_merge,
+    fa_fwd_masked
 Convenience wrappers that allocate outputs with torch:
     attention_forward, attention_backward, attention_forward_split
 """
@@ -33,7 +34,10 @@ FA_ERR_DEVICE_BOUNDS = 7
 # Every symbol include/flashattn.h declares.
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_fp32", "fa_bwd_fp32",
             "fa_get_device_status", "fa_status_string", "fa_bwd_noalloc", "fa_fwd_split",
-            "fa_merge")
+            "fa_merge", "fa_fwd_masked")
+
+# Side of the square tiles of a block mask (FA_MASK_BLOCK).
+MASK_BLOCK = 128
 
 # Largest number of key ranges fa_fwd_split / fa_merge accept (FA_MAX_SPLITS).
 MAX_SPLITS = 256
@@ -82,6 +86,8 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_split.restype = i
             L.fa_merge.argtypes = [vp, vp, i, ctypes.c_longlong, i, vp, i, vp, vp]
             L.fa_merge.restype = i
+            L.fa_fwd_masked.argtypes = [vp] * 5 + dims + [vp, vp, vp, i, vp]
+            L.fa_fwd_masked.restype = i
             _lib = L
     return _lib
 
@@ -168,6 +174,22 @@ def fa_merge(O_parts, LSE_parts, O, LSE, stream=None, check: bool = True) -> int
     return _check(st, "fa_merge", check)
 
 
+def _mask_ptrs(q_len, k_len, block_mask):
+    mh = 0 if block_mask is None else int(block_mask.shape[0])
+    return _ptr(q_len), _ptr(k_len), _ptr(block_mask), mh
+
+
+def fa_fwd_masked(Q, K, V, O, LSE, causal: bool, scale: float, q_len=None, k_len=None,
+                  block_mask=None, stream=None, check: bool = True) -> int:
+    """fa_fwd under a general mask: q_len / k_len int32 [B] and block_mask uint8
+    [mask_heads, nb, nb] device tensors (or None)."""
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    st = lib().fa_fwd_masked(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d,
+                             int(bool(causal)), float(scale),
+                             *_mask_ptrs(q_len, k_len, block_mask), _stream(stream))
+    return _check(st, "fa_fwd_masked", check)
+
+
 def fa_fwd_fp32(Q, K, V, O, LSE, causal: bool, scale: float, stream=None, check: bool = True):
     B, Hq, Hkv, N, d = _dims(Q, K)
     st = lib().fa_fwd_fp32(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d,
@@ -217,6 +239,18 @@ def attention_forward_split(Q, K, V, causal: bool, scale: float | None = None,
     fa_merge(O_parts, LSE_parts, O, LSE, stream)
     if return_parts:
         return O, LSE, O_parts, LSE_parts
+    return O, LSE
+
+
+def attention_forward_masked(Q, K, V, causal: bool, scale: float | None = None, q_len=None,
+                             k_len=None, block_mask=None, stream=None):
+    """Allocates O and LSE and runs fa_fwd_masked."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(Q.shape[-1])
+    B, Hq, N, d = Q.shape
+    O = torch.empty_like(Q)
+    LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=Q.device)
+    fa_fwd_masked(Q, K, V, O, LSE, causal, scale, q_len, k_len, block_mask, stream)
     return O, LSE
 
 

@@ -27,6 +27,7 @@ class Workload:
     backward: bool
     q_mult: float = 1.0
     num_splits: int = 1          # key ranges of the split-KV forward (1: the one-pass forward)
+    mask: str = ""               # general-mask recipe (see workload_mask), "" for none
 
     @property
     def scale(self) -> float:
@@ -54,7 +55,40 @@ WORKLOADS = {
     # GB300 has, the case the split-KV forward (num_splits key ranges + merge) is for.
     "splitkv_n32768": Workload("splitkv_n32768", 1, 1, 1, 32768, 128, True, 5, torch.bfloat16,
                                False, num_splits=4),
+    # Padded batch of variable-length sequences (general mask: valid lengths).
+    "varlen_n8192": Workload("varlen_n8192", 8, 16, 16, 8192, 128, True, 6, torch.bfloat16, True,
+                             mask="varlen"),
+    # Block-sparse causal pattern (general mask: tile mask): a local window plus a first tile.
+    "local_n16384": Workload("local_n16384", 1, 16, 16, 16384, 128, True, 7, torch.bfloat16, True,
+                             mask="local_sink"),
 }
+
+MASK_BLOCK = 128        # side of the tiles a block mask covers
+LOCAL_WINDOW_TILES = 8  # local_sink: tiles of keys before (and including) the query's own tile
+
+
+def workload_mask(w: Workload):
+    """(q_len, k_len, block_mask) numpy arrays (int32 [B], int32 [B], uint8 [heads, nb, nb]) of a
+    workload's mask recipe, each None when absent.
+
+    varlen: q_len = k_len, the first sequence full length N, the others uniform in [N/8, N]
+    (seeded).  local_sink: one mask for every head; query tile a sees key tiles
+    a-7 .. a and tile 0."""
+    import numpy as np
+    if not w.mask:
+        return None, None, None
+    if w.mask == "varlen":
+        rng = np.random.default_rng(w.seed)
+        lens = rng.integers(w.N // 8, w.N + 1, size=w.B).astype(np.int32)
+        lens[0] = w.N
+        return lens, lens.copy(), None
+    if w.mask == "local_sink":
+        nb = -(-w.N // MASK_BLOCK)
+        a = np.arange(nb)[:, None]
+        c = np.arange(nb)[None, :]
+        bm = ((c <= a) & (c > a - LOCAL_WINDOW_TILES)) | (c == 0)
+        return None, None, bm.astype(np.uint8)[None]
+    raise ValueError("unknown mask recipe " + w.mask)
 
 
 def make_inputs(B: int, Hq: int, Hkv: int, N: int, d: int, seed: int,

@@ -64,6 +64,32 @@ fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LS
                  int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                  cudaStream_t stream);
 
+/* Side of the square tiles a block mask of fa_fwd_masked / fa_bwd_masked covers. */
+#define FA_MASK_BLOCK 128
+
+/*
+ * Forward under a general mask: valid lengths of a padded batch and a 0/1 mask over tiles, on
+ * top of the causal rule.  The mask acts on whole tiles of Q K^T (FlashAttention DAC'24 reading
+ * note, paper.adslab.icu, "other operators"): tiles a row may not see are skipped, not computed
+ * and zeroed.  Masked pairs have weight 0.
+ *   Q, K, V, O, LSE, sizes, causal, scale: as in fa_fwd (d 64 or 128).
+ *   q_len, k_len: device int32 [B] or NULL.  Batch b's query rows i >= q_len[b] and keys
+ *     j >= k_len[b] are padding (values clamped to [0, N]).  K and V padding rows must hold
+ *     finite values (a zero weight times an infinite value would still give NaN).
+ *   block_mask: device uint8 [mask_heads, nb, nb] or NULL, nb = ceil(N / FA_MASK_BLOCK);
+ *     entry (h, a, c) != 0 lets query rows [a*128, a*128+128) see keys [c*128, c*128+128).
+ *     mask_heads is 1 (one mask for every head), Hq (one per query head, shared by the batch)
+ *     or B*Hq (one per (batch, query head), index b*Hq + hq); it is ignored when block_mask is
+ *     NULL.
+ *   A row with no allowed key, and every padding row, gets O = 0 and LSE = -inf.
+ *   Errors as for fa_fwd, plus FA_ERR_INVALID_ARG for another mask_heads and FA_ERR_MISALIGNED
+ *   for q_len / k_len not 4-byte aligned.  The mask arrays are only read, on `stream`.
+ */
+fa_status fa_fwd_masked(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                        int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                        const int *q_len, const int *k_len, const unsigned char *block_mask,
+                        int mask_heads, cudaStream_t stream);
+
 /* Largest number of key ranges fa_fwd_split and fa_merge accept. */
 #define FA_MAX_SPLITS 256
 

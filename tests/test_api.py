@@ -134,6 +134,22 @@ def test_merge_rejects_invalid_arguments(built_lib):
         assert merge(**{k: MIS}) == E.FA_ERR_MISALIGNED
 
 
+def test_masked_forward_rejects_invalid_arguments(built_lib):
+    L = built_lib.lib()
+    E = built_lib
+
+    def masked(Q=A, ql=None, kl=None, bm=None, mh=0, B=2, Hq=4, Hkv=2, N=300, d=128):
+        return L.fa_fwd_masked(Q, A, A, A, A, B, Hq, Hkv, N, d, 1, 0.1, ql, kl, bm, mh, None)
+
+    assert masked(B=0) == E.FA_ERR_INVALID_ARG
+    assert masked(d=96) == E.FA_ERR_UNSUPPORTED
+    assert masked(Q=MIS) == E.FA_ERR_MISALIGNED
+    assert masked(ql=A + 2) == E.FA_ERR_MISALIGNED
+    assert masked(kl=A + 1) == E.FA_ERR_MISALIGNED
+    for mh in (0, 2, 3, 9):
+        assert masked(bm=A + 1, mh=mh) == E.FA_ERR_INVALID_ARG, mh
+
+
 def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     """The binding never falls back: a missing library is an error, not a CPU path."""
     from exact_attention_89_gb300 import flashattn
