@@ -203,6 +203,47 @@ fa_status fa_fwd_masked(const void *Q, const void *K, const void *V, void *O, fl
     return fa::from_cuda(fa::launch_fwd_masked_bf16(p, tq, tk, tv, O, LSE, mk, di->status, stream));
 }
 
+fa_status fa_bwd_masked(const void *Q, const void *K, const void *V, const void *O,
+                        const void *dO, const float *LSE, void *dQ, void *dK, void *dV, int B,
+                        int Hq, int Hkv, int N, int d, int causal, float scale, const int *q_len,
+                        const int *k_len, const unsigned char *block_mask, int mask_heads,
+                        void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(Hq / Hkv) * ((N + 63) / 64) > fa::MASK_BWD_MAX_STEPS)
+        return FA_ERR_UNSUPPORTED;
+    if (!fa::aligned16(Q) || !fa::aligned16(K) || !fa::aligned16(V) || !fa::aligned16(O) ||
+        !fa::aligned16(dO) || !fa::aligned16(LSE) || !fa::aligned16(dQ) || !fa::aligned16(dK) ||
+        !fa::aligned16(dV))
+        return FA_ERR_MISALIGNED;
+    fa::MaskArgs mk;
+    if ((st = fa::check_mask(B, Hq, q_len, k_len, block_mask, mask_heads, &mk)) != FA_OK) return st;
+    if (!fa::aligned16(workspace) || workspace_bytes < fa_bwd_workspace_bytes(B, Hq, N, d))
+        return FA_ERR_WORKSPACE;
+    fa::DeviceInfo *di = nullptr;
+    if ((st = fa::current_device(&di, true)) != FA_OK) return st;
+    const Problem p{B, Hq, Hkv, N, d, causal ? 1 : 0, scale};
+    const size_t rows = static_cast<size_t>(B) * Hq * N;
+    float *Dvec = static_cast<float *>(workspace);
+    float *dQacc = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                             fa::align256(rows * sizeof(float)));
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+    if (!fa::encode_bf16(&tq, Q, d, N, 1LL * B * Hq, 64) ||
+        !fa::encode_bf16(&tk, K, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tv, V, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tdo, dO, d, N, 1LL * B * Hq, 64) ||
+        !fa::encode_bf16(&tdk, dK, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tdv, dV, d, N, 1LL * B * Hkv, 128))
+        return FA_ERR_CUDA;
+    cudaError_t e = fa::launch_bwd_preprocess_bf16(p, O, dO, Dvec, dQacc, stream);
+    if (e == cudaSuccess)
+        e = fa::launch_bwd_main_masked_bf16(p, tq, tk, tv, tdo, tdk, tdv, LSE, Dvec, dQacc, mk,
+                                            di->status, stream);
+    if (e == cudaSuccess) e = fa::launch_bwd_dq_convert_bf16(p, dQacc, dQ, stream);
+    return fa::from_cuda(e);
+}
+
 fa_status fa_fwd_split(const void *Q, const void *K, const void *V, float *O_parts,
                        float *LSE_parts, int B, int Hq, int Hkv, int N, int d, int causal,
                        float scale, int num_splits, cudaStream_t stream) {

@@ -48,6 +48,8 @@ constexpr int WARP_MMA = 9;
 constexpr uint32_t REGS_GRAD = 256, REGS_DRAIN = 104, REGS_OTHER = 64;
 constexpr int REGS_NEEDED = 128 * (REGS_GRAD + REGS_DRAIN + REGS_OTHER);
 constexpr float LOG2E = 1.4426950408889634f;
+// Steps (query head of the group x query tile) a masked CTA can list in shared memory.
+constexpr int MAX_MASK_STEPS = MASK_BWD_MAX_STEPS;
 
 template <int D>
 struct Layout {
@@ -68,6 +70,9 @@ struct Layout {
     static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
     static constexpr int ABORT_OFF = TMEM_OFF + 8;
     static constexpr int BYTES = ABORT_OFF + 8 + 1024;
+    // General mask: the CTA's list of steps (query head, query tile) its tile mask keeps.
+    static constexpr int LIST_OFF = ABORT_OFF + 16;                  // [2] step count, then entries
+    static constexpr int BYTES_MASK = LIST_OFF + 4 + MAX_MASK_STEPS * 2 + 1024;
 };
 
 constexpr uint32_t T_DK = 0, T_DV = 128, T_BUF = 256;
@@ -78,14 +83,17 @@ __device__ __forceinline__ int first_q_tile(int jb) {
     return CAUSAL ? (jb * BKV) / BQ : 0;
 }
 
-template <int D, int DR, bool CAUSAL>
+// MASK = true: the general mask mk on top of the causal rule.  The CTA lists, before the roles
+// split, the steps whose tile its mask keeps (rows past the valid length and key blocks past it
+// drop out); a key block with no step at all gets dK = dV = 0.
+template <int D, int DR, bool CAUSAL, bool MASK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                     const float *__restrict__ LSE, const float *__restrict__ Dvec,
                     float *__restrict__ dQacc, int Hq, int Hkv, int N, int BHkv, int HC,
-                    float scale, float scale_log2, unsigned *status) {
+                    float scale, float scale_log2, const MaskArgs mk, unsigned *status) {
     // Laid out for d = 128.  With a real head dim DR = 64 the tensor maps are 64 wide, so the
     // second 64-column chunk of every load is TMA zero fill: all products see zero-padded
     // operands and are unchanged; only the dQ reductions and the dK / dV stores use DR.
@@ -124,8 +132,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int b = bkv / Hkv, hk = bkv % Hkv;
     const int nq = (N + BQ - 1) / BQ;
     const int i0 = first_q_tile<CAUSAL>(jb);
-    const int tiles_per_head = nq - i0;
-    const int T = G * tiles_per_head;           // steps of this CTA (>= 1)
+    int lq = N, lk = N;                         // valid query rows / keys of the batch
+    if (MASK) {
+        if (mk.q_len) lq = min(max(__ldg(mk.q_len + b), 0), N);
+        if (mk.k_len) lk = min(max(__ldg(mk.k_len + b), 0), N);
+    }
+    const int tiles_per_head = MASK ? max(0, (lq + BQ - 1) / BQ - i0) : nq - i0;
+    uint16_t *steps = reinterpret_cast<uint16_t *>(smem + L::LIST_OFF + 4);
+    if (MASK && warp == 0) {
+        // steps (g, i) in the unmasked order, kept if the key block is inside the valid length
+        // and the tile mask lets query tile i / 2 of head g see key block jb
+        const int cand = (jb * BKV < lk) ? G * tiles_per_head : 0;
+        int count = 0;
+        for (int c0 = 0; c0 < cand; c0 += 32) {
+            const int c = c0 + lane;
+            bool keep = false;
+            if (c < cand) {
+                keep = true;
+                if (mk.block_mask) {
+                    const int g = c / tiles_per_head, i = i0 + c % tiles_per_head;
+                    const int hq = hk * G + g;
+                    const int h = mk.mask_heads == 1 ? 0 : (mk.mask_heads == BHkv * G ? b * Hq + hq : hq);
+                    keep = __ldg(mk.block_mask + (static_cast<size_t>(h) * nkb + (i * BQ) / BKV) * nkb + jb) != 0;
+                }
+            }
+            const unsigned ball = __ballot_sync(0xffffffffu, keep);
+            if (keep && count + __popc(ball & ((1u << lane) - 1u)) < MAX_MASK_STEPS)
+                steps[count + __popc(ball & ((1u << lane) - 1u))] = static_cast<uint16_t>(c);
+            count += __popc(ball);
+        }
+        if (lane == 0) *reinterpret_cast<int *>(smem + L::LIST_OFF) = min(count, MAX_MASK_STEPS);
+    }
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
@@ -153,6 +190,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // steps of this CTA: every (query head, tile at or below the diagonal), or the listed ones
+    const int T = MASK ? *reinterpret_cast<volatile int *>(smem + L::LIST_OFF) : G * tiles_per_head;
+    auto step_tile = [&](int s, int &g, int &i) {
+        const int e = MASK ? static_cast<int>(steps[s]) : s;
+        g = e / tiles_per_head;
+        i = i0 + e % tiles_per_head;
+    };
+    const int qend = MASK ? lq : N, kend = MASK ? lk : N;   // rows / keys past these are masked
 
     // Each role branch starts with its register budget and ends with its own copy of the final
     // barrier, so no code is shared between budgets.
@@ -163,16 +208,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmdO);
-            mbar_arrive_expect_tx(kv_full, 2 * L::KV_BYTES);
-            for (int ch = 0; ch < D / 64; ++ch) {
-                tma_load_3d(smem + L::K_OFF + ch * L::KV_CHUNK, &tmK, ch * 64, jb * BKV, bkv, kv_full);
-                tma_load_3d(smem + L::V_OFF + ch * L::KV_CHUNK, &tmV, ch * 64, jb * BKV, bkv, kv_full);
+            if (T > 0) {                            // (a masked key block may have no step)
+                mbar_arrive_expect_tx(kv_full, 2 * L::KV_BYTES);
+                for (int ch = 0; ch < D / 64; ++ch) {
+                    tma_load_3d(smem + L::K_OFF + ch * L::KV_CHUNK, &tmK, ch * 64, jb * BKV, bkv, kv_full);
+                    tma_load_3d(smem + L::V_OFF + ch * L::KV_CHUNK, &tmV, ch * 64, jb * BKV, bkv, kv_full);
+                }
             }
             int issued = 0;
             for (int s = 0; s < T; ++s) {
                 const int st = s % NSQ, rnd = s / NSQ;
                 if (!mbar_wait(&q_empty[st], (rnd & 1) ^ 1, abort_flag, status)) break;
-                const int g = s / tiles_per_head, i = i0 + s % tiles_per_head;
+                int g, i;
+                step_tile(s, g, i);
                 const int bhq = b * Hq + hk * G + g;
                 mbar_arrive_expect_tx(&q_full[st], 2 * L::Q_BYTES);
                 uint8_t *qdst = smem + L::QR_OFF + st * 2 * L::Q_BYTES;
@@ -186,7 +234,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (*abort_flag) {
                 for (int s = max(0, issued - NSQ); s < issued; ++s)
                     mbar_drain(&q_full[s % NSQ], (s / NSQ) & 1);
-                mbar_drain(kv_full, 0);
+                if (T > 0) mbar_drain(kv_full, 0);
             }
         }
     } else if (warp == WARP_MMA) {
@@ -222,7 +270,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 mma_commit(&s_full[s & 1]);
             };
-            bool ok = mbar_wait(kv_full, 0, abort_flag, status) &&
+            bool ok = T > 0 && mbar_wait(kv_full, 0, abort_flag, status) &&
                       mbar_wait(&q_full[0], 0, abort_flag, status);
             tc_fence_after();
             if (ok) issue_sp(0);
@@ -284,16 +332,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // step instead of sitting between the MMAs and this step's work.
         auto load_stat = [&](int s) -> float {
             if (s >= T) return 0.f;
-            const int g = s / tiles_per_head, i = i0 + s % tiles_per_head;
+            int g, i;
+            step_tile(s, g, i);
             const int bhq = b * Hq + hk * G + g;
             const int q = i * BQ + (krow & (BQ - 1));
-            if (krow < BQ)
-                return (q < N) ? LSE[static_cast<size_t>(bhq) * N + q] * LOG2E : INFINITY;
-            return (q < N) ? Dvec[static_cast<size_t>(bhq) * N + q] : 0.f;
+            if (krow < BQ) {
+                if (q >= qend) return INFINITY;
+                const float lse = LSE[static_cast<size_t>(bhq) * N + q];
+                // a row with no allowed key (LSE = -inf) gets P = 0 from +inf
+                return (MASK && lse == -INFINITY) ? INFINITY : lse * LOG2E;
+            }
+            return (q < qend) ? Dvec[static_cast<size_t>(bhq) * N + q] : 0.f;
         };
         float v_next = load_stat(0);
         for (int s = 0; s < T; ++s) {
-            const int g = s / tiles_per_head, i = i0 + s % tiles_per_head;
+            int g, i;
+            step_tile(s, g, i);
             const int bhq = b * Hq + hk * G + g;
             const int q0 = i * BQ;
             const int bsel = s & 1;
@@ -310,8 +364,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // P^T in place over the S^T registers, then dS^T with dP^T streamed in halves
                 uint32_t sr[64];
                 tmem_ld_x64(buf + B_ST, sr);
-                const bool need_mask = (CAUSAL && q0 < jb * BKV + BKV) || (q0 + BQ > N) ||
-                                       (jb * BKV + BKV > N);
+                const bool need_mask = (CAUSAL && q0 < jb * BKV + BKV) || (q0 + BQ > qend) ||
+                                       (jb * BKV + BKV > kend);
                 const float4 *l4 = reinterpret_cast<const float4 *>(sbuf);
                 const float4 *d4 = reinterpret_cast<const float4 *>(sbuf + BQ);
                 float pf[64];
@@ -331,7 +385,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < BQ; ++c) {
                         const int q = q0 + c;
-                        if ((CAUSAL && key > q) || q >= N || key >= N) pf[c] = 0.f;
+                        if ((CAUSAL && key > q) || q >= qend || key >= kend) pf[c] = 0.f;
                     }
                 }
                 uint32_t pp[32], dd[32];
@@ -384,6 +438,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t a[32];
                     tmem_ld_x32(tmem + lane_off + tcol + c0, a);
+                    if (MASK && T == 0) {               // no step: TMEM was never written
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) a[k] = 0u;
+                    }
                     uint8_t *rowp = dst + (c0 / 64) * L::KV_CHUNK + krow * 128;
                     const int u0 = (c0 % 64) / 8;
 #pragma unroll
@@ -416,7 +474,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int dcol = wq * 32 + lane;            // column of dQ = TMEM lane of dQ^T
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         for (int s = 0; s < T; ++s) {
-            const int g = s / tiles_per_head, i = i0 + s % tiles_per_head;
+            int g, i;
+            step_tile(s, g, i);
             const int bhq = b * Hq + hk * G + g;
             const int q0 = i * BQ;
             const int bsel = s & 1;
@@ -428,7 +487,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_arrive(&dq_empty[bsel]);
             float *dst = dQacc + (static_cast<size_t>(bhq) * N + q0) * DR + dcol;
             // rows of this tile inside the sequence; with DR = 64 the upper 64 lanes hold zeros
-            const int nvalid = (DR == D || dcol < DR) ? min(BQ, N - q0) : 0;
+            const int nvalid = (DR == D || dcol < DR) ? min(BQ, qend - q0) : 0;
 #pragma unroll
             for (int c = 0; c < BQ; ++c)
                 if (c < nvalid) atomicAdd(dst + static_cast<size_t>(c) * DR, __uint_as_float(a[c]) * scale);
@@ -517,39 +576,62 @@ cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const vo
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
-                                 const CUtensorMap &tmV, const CUtensorMap &tmdO,
-                                 const CUtensorMap &tmdK, const CUtensorMap &tmdV,
-                                 const float *LSE, const float *D, float *dQacc, unsigned *status,
-                                 cudaStream_t stream) {
+namespace bwd {
+template <bool MASK>
+cudaError_t launch_main(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                        const CUtensorMap &tmV, const CUtensorMap &tmdO, const CUtensorMap &tmdK,
+                        const CUtensorMap &tmdV, const float *LSE, const float *D, float *dQacc,
+                        const MaskArgs &mk, unsigned *status, cudaStream_t stream) {
     if (p.d != 128 && p.d != 64) return cudaErrorInvalidValue;
     const int BHkv = p.B * p.Hkv;
-    const long long nkb = (p.N + bwd::BKV - 1) / bwd::BKV;
+    const long long nkb = (p.N + BKV - 1) / BKV;
     // One chunk spans every KV head (key-block-major order): measured slightly faster than
     // chunks of heads sized for L2 residency.
     const int HC = BHkv;
     const long long grid = nkb * BHkv;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    const int smem = bwd::Layout<128>::BYTES;
+    if (MASK && static_cast<long long>(p.Hq / p.Hkv) * ((p.N + BQ - 1) / BQ) > MAX_MASK_STEPS)
+        return cudaErrorInvalidConfiguration;
+    const int smem = MASK ? Layout<128>::BYTES_MASK : Layout<128>::BYTES;
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                           const float *, const float *, float *, int, int, int, int, int, float, float,
-                          unsigned *);
+                          MaskArgs, unsigned *);
     Kern kern;
     if (p.d == 128)
-        kern = p.causal ? bwd::bwd_main_kernel<128, 128, true> : bwd::bwd_main_kernel<128, 128, false>;
+        kern = p.causal ? bwd_main_kernel<128, 128, true, MASK> : bwd_main_kernel<128, 128, false, MASK>;
     else
-        kern = p.causal ? bwd::bwd_main_kernel<128, 64, true> : bwd::bwd_main_kernel<128, 64, false>;
+        kern = p.causal ? bwd_main_kernel<128, 64, true, MASK> : bwd_main_kernel<128, 64, false, MASK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // the in-kernel register split needs at least REGS_NEEDED registers at launch
     cudaFuncAttributes attr{};
     if ((e = cudaFuncGetAttributes(&attr, kern)) != cudaSuccess) return e;
-    if (attr.numRegs * bwd::NUM_THREADS < bwd::REGS_NEEDED) return cudaErrorInvalidConfiguration;
-    kern<<<static_cast<unsigned>(grid), bwd::NUM_THREADS, smem, stream>>>(
+    if (attr.numRegs * NUM_THREADS < REGS_NEEDED) return cudaErrorInvalidConfiguration;
+    kern<<<static_cast<unsigned>(grid), NUM_THREADS, smem, stream>>>(
         tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, HC, p.scale,
-        scale_log2, status);
+        scale_log2, mk, status);
     return cudaGetLastError();
+}
+}  // namespace bwd
+
+cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                                 const CUtensorMap &tmV, const CUtensorMap &tmdO,
+                                 const CUtensorMap &tmdK, const CUtensorMap &tmdV,
+                                 const float *LSE, const float *D, float *dQacc, unsigned *status,
+                                 cudaStream_t stream) {
+    return bwd::launch_main<false>(p, tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, MaskArgs{},
+                                   status, stream);
+}
+
+cudaError_t launch_bwd_main_masked_bf16(const Problem &p, const CUtensorMap &tmQ,
+                                        const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                        const CUtensorMap &tmdO, const CUtensorMap &tmdK,
+                                        const CUtensorMap &tmdV, const float *LSE, const float *D,
+                                        float *dQacc, const MaskArgs &mk, unsigned *status,
+                                        cudaStream_t stream) {
+    return bwd::launch_main<true>(p, tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, mk, status,
+                                  stream);
 }
 
 cudaError_t launch_bwd_dq_convert_bf16(const Problem &p, const float *dQacc, void *dQ,

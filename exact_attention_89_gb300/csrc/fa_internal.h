@@ -59,6 +59,16 @@ cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const
                                  const float *LSE, const float *D, float *dQacc, unsigned *status,
                                  cudaStream_t stream);
 
+// K3 under a general mask.  Needs (Hq / Hkv) * ceil(N / 64) <= MASK_BWD_MAX_STEPS (the CTA's
+// step list lives in shared memory).
+constexpr int MASK_BWD_MAX_STEPS = 16384;
+cudaError_t launch_bwd_main_masked_bf16(const Problem &p, const CUtensorMap &tmQ,
+                                        const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                        const CUtensorMap &tmdO, const CUtensorMap &tmdK,
+                                        const CUtensorMap &tmdV, const float *LSE, const float *D,
+                                        float *dQacc, const MaskArgs &mk, unsigned *status,
+                                        cudaStream_t stream);
+
 // K4: dQ = bf16(dQacc).
 cudaError_t launch_bwd_dq_convert_bf16(const Problem &p, const float *dQacc, void *dQ,
                                        cudaStream_t stream);

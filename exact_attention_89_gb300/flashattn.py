@@ -7,7 +7,7 @@ fallback: if ``libflashattn.so`` is missing or the GPU is not sm_103, calls fail
 Low-level functions (same names and argument order as ``include/flashattn.h``):
     fa_fwd, fa_bwd, fa_bwd_workspace_bytes, fa_fwd_fp32, fa_bwd_fp32,
     fa_get_device_status, fa_status_string, fa_bwd_noalloc, fa_fwd_split, fa_merge,
-    fa_fwd_masked
+    fa_fwd_masked, fa_bwd_masked
 Convenience wrappers that allocate outputs with torch:
     attention_forward, attention_backward, attention_forward_split
 """
@@ -34,7 +34,7 @@ FA_ERR_DEVICE_BOUNDS = 7
 # Every symbol include/flashattn.h declares.
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_fp32", "fa_bwd_fp32",
             "fa_get_device_status", "fa_status_string", "fa_bwd_noalloc", "fa_fwd_split",
-            "fa_merge", "fa_fwd_masked")
+            "fa_merge", "fa_fwd_masked", "fa_bwd_masked")
 
 # Side of the square tiles of a block mask (FA_MASK_BLOCK).
 MASK_BLOCK = 128
@@ -88,6 +88,8 @@ def lib() -> ctypes.CDLL:
             L.fa_merge.restype = i
             L.fa_fwd_masked.argtypes = [vp] * 5 + dims + [vp, vp, vp, i, vp]
             L.fa_fwd_masked.restype = i
+            L.fa_bwd_masked.argtypes = [vp] * 9 + dims + [vp, vp, vp, i, vp, sz, vp]
+            L.fa_bwd_masked.restype = i
             _lib = L
     return _lib
 
@@ -190,6 +192,18 @@ def fa_fwd_masked(Q, K, V, O, LSE, causal: bool, scale: float, q_len=None, k_len
     return _check(st, "fa_fwd_masked", check)
 
 
+def fa_bwd_masked(Q, K, V, O, dO, LSE, dQ, dK, dV, causal: bool, scale: float, workspace,
+                  q_len=None, k_len=None, block_mask=None, stream=None, check: bool = True) -> int:
+    """fa_bwd under the general mask fa_fwd_masked used."""
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().fa_bwd_masked(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ),
+                             _ptr(dK), _ptr(dV), B, Hq, Hkv, N, d, int(bool(causal)),
+                             float(scale), *_mask_ptrs(q_len, k_len, block_mask),
+                             _ptr(workspace), wbytes, _stream(stream))
+    return _check(st, "fa_bwd_masked", check)
+
+
 def fa_fwd_fp32(Q, K, V, O, LSE, causal: bool, scale: float, stream=None, check: bool = True):
     B, Hq, Hkv, N, d = _dims(Q, K)
     st = lib().fa_fwd_fp32(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d,
@@ -252,6 +266,22 @@ def attention_forward_masked(Q, K, V, causal: bool, scale: float | None = None, 
     LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=Q.device)
     fa_fwd_masked(Q, K, V, O, LSE, causal, scale, q_len, k_len, block_mask, stream)
     return O, LSE
+
+
+def attention_backward_masked(Q, K, V, O, dO, LSE, causal: bool, scale: float | None = None,
+                              q_len=None, k_len=None, block_mask=None, workspace=None,
+                              stream=None):
+    """Allocates dQ, dK, dV (and the workspace unless given) and runs fa_bwd_masked."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(Q.shape[-1])
+    B, Hq, N, d = Q.shape
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_bytes(B, Hq, N, d), dtype=torch.uint8,
+                                device=Q.device)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    fa_bwd_masked(Q, K, V, O, dO, LSE, dQ, dK, dV, causal, scale, workspace, q_len, k_len,
+                  block_mask, stream)
+    return dQ, dK, dV
 
 
 def attention_backward(Q, K, V, O, dO, LSE, causal: bool, scale: float | None = None,

@@ -90,6 +90,21 @@ fa_status fa_fwd_masked(const void *Q, const void *K, const void *V, void *O, fl
                         const int *q_len, const int *k_len, const unsigned char *block_mask,
                         int mask_heads, cudaStream_t stream);
 
+/*
+ * Backward under a general mask: the gradients of fa_fwd_masked's output.  Arguments as in
+ * fa_bwd, with O and LSE from fa_fwd_masked on the same mask, plus the mask of fa_fwd_masked.
+ * Padding rows and rows with no allowed key get dQ = 0; padding keys (and keys no row may see)
+ * get dK = dV = 0.  The padding rows of dO must hold finite values.
+ * Also FA_ERR_UNSUPPORTED when (Hq / Hkv) * ceil(N / 64) > 16384 (each key block lists the
+ * (query head, 64-row tile) steps its mask keeps in shared memory).
+ */
+fa_status fa_bwd_masked(const void *Q, const void *K, const void *V, const void *O,
+                        const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                        int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                        const int *q_len, const int *k_len, const unsigned char *block_mask,
+                        int mask_heads, void *workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+
 /* Largest number of key ranges fa_fwd_split and fa_merge accept. */
 #define FA_MAX_SPLITS 256
 

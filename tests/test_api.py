@@ -150,6 +150,29 @@ def test_masked_forward_rejects_invalid_arguments(built_lib):
         assert masked(bm=A + 1, mh=mh) == E.FA_ERR_INVALID_ARG, mh
 
 
+def test_masked_backward_rejects_invalid_arguments(built_lib):
+    L = built_lib.lib()
+    E = built_lib
+
+    def masked(ptrs=None, ql=None, bm=None, mh=0, B=2, Hq=4, Hkv=2, N=300, d=128, ws=A,
+               wbytes=None):
+        ptrs = ptrs or [A] * 9
+        if wbytes is None:
+            wbytes = L.fa_bwd_workspace_bytes(B, Hq, N, d)
+        return L.fa_bwd_masked(*ptrs, B, Hq, Hkv, N, d, 1, 0.1, ql, None, bm, mh, ws, wbytes, None)
+
+    assert masked(B=0) == E.FA_ERR_INVALID_ARG
+    assert masked(d=96) == E.FA_ERR_UNSUPPORTED
+    assert masked(Hq=64, Hkv=1, N=32768) == E.FA_ERR_UNSUPPORTED      # step list too long
+    for k in range(9):
+        ptrs = [A] * 9
+        ptrs[k] = MIS
+        assert masked(ptrs) == E.FA_ERR_MISALIGNED
+    assert masked(ql=A + 2) == E.FA_ERR_MISALIGNED
+    assert masked(bm=A, mh=3) == E.FA_ERR_INVALID_ARG
+    assert masked(wbytes=16) == E.FA_ERR_WORKSPACE
+
+
 def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     """The binding never falls back: a missing library is an error, not a CPU path."""
     from exact_attention_89_gb300 import flashattn
