@@ -37,9 +37,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # "<kernel file>:<sha256 prefix of that file and fa_ptx.cuh>:<workload>"; a key that no longer
 # matches the sources (the kernel changed since the capture) reports null.
 NCU_TRAFFIC = {
-    # fa_bwd on causal_n4096: bwd_main 1.917 GB read + 0.990 GB write, bwd_preprocess 0.210 GB,
-    # bwd_dq_convert 0.164 GB (profiles/bwd_main_kernel_causal_n4096.md)
-    "fa_bwd_sm103a.cu:5648148527b57a99:causal_n4096": 3.28e9,
+    # fa_bwd on causal_n4096: bwd_main 1.917 GB read + 0.986 GB write, bwd_preprocess 0.206 GB,
+    # bwd_dq_convert 0.160 GB (profiles/launches_causal_n4096.md)
+    "fa_bwd_sm103a.cu:10b725014a9bd498:causal_n4096": 3.27e9,
+    # split forward on splitkv_n32768: 25.4 MB read + 0.5 MB write
+    # (profiles/fwd_kernel_split_splitkv_n32768.md)
+    "fa_fwd_sm103a.cu:fbaf7783d9be90e0:splitkv_n32768": 2.59e7,
+    # fa_bwd_masked, three kernels (profiles/masked_local_n16384_varlen_n8192.md)
+    "fa_bwd_sm103a.cu:10b725014a9bd498:local_n16384": 0.994e9,
+    "fa_bwd_sm103a.cu:10b725014a9bd498:varlen_n8192": 25.0e9,
 }
 
 
@@ -48,6 +54,34 @@ def split_key_ranges(N: int, S: int):
     nb = -(-N // 128)
     c = -(-nb // S)
     return [(min(N, s * c * 128), min(N, (s + 1) * c * 128)) for s in range(S)]
+
+
+def allowed_pairs(w, q_len, k_len, block_mask, B=None, heads=None) -> float:
+    """Number of (query, key) pairs a general mask allows, summed over batches and query heads:
+    the work a masked pass does (4 d FLOPs per pair forward).  B / heads restrict the count to
+    the first B batch entries and `heads` query heads (a sampled slice)."""
+    import numpy as np
+    B = w.B if B is None else B
+    Hq = w.Hq if heads is None else heads
+    N, blk = w.N, 128
+    i = np.arange(N)
+    total = 0.0
+    for b in range(B):
+        lq = N if q_len is None else int(min(max(q_len[b], 0), N))
+        lk = N if k_len is None else int(min(max(k_len[b], 0), N))
+        hi = np.minimum(i + 1 if w.causal else np.full(N, N), lk)[:lq]   # keys j < hi per row
+        if block_mask is None:
+            total += Hq * float(np.maximum(hi, 0).sum())
+            continue
+        nb = block_mask.shape[-1]
+        c0 = np.arange(nb) * blk                                           # tile starts
+        per_tile = np.clip(hi[:, None] - c0[None, :], 0, blk)              # [lq, nb]
+        for h in range(Hq):
+            mh = block_mask.shape[0]
+            m = block_mask[0 if mh == 1 else (b * w.Hq + h if mh == w.B * w.Hq else h)]
+            rows_tiles = m[i[:lq] // blk]                                  # [lq, nb]
+            total += float((per_tile * rows_tiles).sum())
+    return total
 
 
 def kernel_sources_hash(kernel_file: str) -> str:
@@ -188,6 +222,45 @@ def cpu_oracle_rows_sample(w, budget_s: float, inputs=None):
             "seconds": t_total, "rows": rows_done}
 
 
+def cpu_oracle_masked_sample(w, budget_s: float, inputs=None):
+    """Masked workloads: times the fp64 oracle's masked forward + backward on whole KV groups
+    (batch entry b, KV head hk), counting the pairs the mask allows in each group."""
+    import torch
+
+    import oracle
+    from exact_attention_89_gb300.inputs import workload_inputs, workload_mask
+    Q, K, V, dO = inputs if inputs is not None else workload_inputs(w)
+    ql, kl, bm = workload_mask(w)
+    G = w.Hq // w.Hkv
+    done, pairs, t_total = 0, 0.0, 0.0
+    while t_total < budget_s or done == 0:
+        b, hk = divmod(done % (w.B * w.Hkv), w.Hkv)
+        sl = slice(hk * G, (hk + 1) * G)
+        q = Q[b:b + 1, sl].to(torch.float64).numpy()
+        k = K[b:b + 1, hk:hk + 1].to(torch.float64).numpy()
+        v = V[b:b + 1, hk:hk + 1].to(torch.float64).numpy()
+        do = dO[b:b + 1, sl].to(torch.float64).numpy()
+        qb = None if ql is None else ql[b:b + 1]
+        kb = None if kl is None else kl[b:b + 1]
+        mb = bm if bm is None or bm.shape[0] == 1 else bm[b * w.Hq + hk * G:b * w.Hq + (hk + 1) * G]
+        m = oracle.Mask(q_len=qb, k_len=kb, block_mask=mb, block=128)
+        t0 = time.perf_counter()
+        oracle.forward_masked(q, k, v, w.causal, w.scale, m)
+        oracle.backward_masked(q, k, v, do, w.causal, w.scale, m)
+        t_total += time.perf_counter() - t0
+        from types import SimpleNamespace
+        sub = SimpleNamespace(B=1, Hq=G, N=w.N, causal=w.causal)
+        pairs += allowed_pairs(sub, qb, kb, mb, B=1, heads=G)
+        done += 1
+    flops = 4.0 * w.d * pairs * 3.5
+    return {"value": flops / t_total / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "%d whole KV group(s) of %s (B%d Hq%d Hkv%d N%d d%d, mask %s), fp64 masked "
+                      "forward+backward, %.1f s" % (done, w.name, w.B, w.Hq, w.Hkv, w.N, w.d,
+                                                    w.mask, t_total),
+            "seconds": t_total}
+
+
 def cpu_oracle_sample(w, budget_s: float, max_heads: int, inputs=None, first_group: int = 0):
     """Times the fp64 oracle (forward + backward of whole KV groups) on the host cores."""
     import torch
@@ -196,6 +269,8 @@ def cpu_oracle_sample(w, budget_s: float, max_heads: int, inputs=None, first_gro
     from exact_attention_89_gb300.inputs import workload_inputs
     if not w.backward:
         return cpu_oracle_rows_sample(w, budget_s, inputs)
+    if w.mask:
+        return cpu_oracle_masked_sample(w, budget_s, inputs)
     Q, K, V, dO = inputs if inputs is not None else workload_inputs(w)
     G = w.Hq // w.Hkv
     heads_done, t_total = 0, 0.0
@@ -300,6 +375,12 @@ def main():
     B, Hq, Hkv, N, d = w.B, w.Hq, w.Hkv, w.N, w.d
     S = w.num_splits
     split = S > 1
+    masked = bool(w.mask)
+    if masked:
+        from exact_attention_89_gb300.inputs import workload_mask
+        ql_h, kl_h, bm_h = workload_mask(w)
+        mq, mkk, mbm = (None if a is None else torch.from_numpy(a).to(dev)
+                        for a in (ql_h, kl_h, bm_h))
     O = torch.empty_like(q)
     LSE = torch.empty(B, Hq, N, dtype=torch.float32, device=dev)
     if w.backward:
@@ -314,6 +395,8 @@ def main():
         # the forward's tensor-core launch
         if split:
             fa.fa_fwd_split(q, k, v, Op, Lp, w.causal, w.scale, S)
+        elif masked:
+            fa.fa_fwd_masked(q, k, v, O, LSE, w.causal, w.scale, mq, mkk, mbm)
         else:
             fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
 
@@ -321,6 +404,8 @@ def main():
         # what follows it in a step: the merge of the partials, or the backward
         if split:
             fa.fa_merge(Op, Lp, O, LSE)
+        elif masked:
+            fa.fa_bwd_masked(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsp, mq, mkk, mbm)
         elif w.backward:
             fa.fa_bwd(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsp)
 
@@ -386,7 +471,11 @@ def main():
     second_ms = sum(b.elapsed_time(c) for _, b, c in ev) / args.steps
     total_ms = max_over_ranks(total_ms, ws, dev)
 
-    flops_step = w.flops_fwd() + (w.flops_bwd() if w.backward else 0.0)
+    # FLOPs: the formula 4 B Hq N^2 d (/2 causal, x2.5 backward), or under a general mask
+    # 4 d per allowed (query, key) pair
+    flops_fwd = (4.0 * d * allowed_pairs(w, ql_h, kl_h, bm_h)) if masked else w.flops_fwd()
+    flops_bwd = 2.5 * flops_fwd if w.backward else 0.0
+    flops_step = flops_fwd + flops_bwd
     value = whole_job_tflops(ws, flops_step, args.steps, total_ms)
 
     # the one-pass forward on the same inputs, for comparison with the split path
@@ -415,9 +504,15 @@ def main():
         qd, kd, vd = dev_in[:3]
         if split:
             res = fa.attention_forward_split(qd, kd, vd, w.causal, w.scale, num_splits=S)
+        elif masked:
+            res = fa.attention_forward_masked(qd, kd, vd, w.causal, w.scale, mq, mkk, mbm)
         else:
             res = fa.attention_forward(qd, kd, vd, w.causal, w.scale)
-        if w.backward:
+        if masked:
+            res = res + fa.attention_backward_masked(qd, kd, vd, res[0], dev_in[3], res[1],
+                                                     w.causal, w.scale, mq, mkk, mbm,
+                                                     workspace=wsp)
+        elif w.backward:
             res = res + fa.attention_backward(qd, kd, vd, res[0], dev_in[3], res[1], w.causal,
                                               w.scale, workspace=wsp)
         for hbuf, dbuf in zip(outs_h, res):
@@ -447,7 +542,7 @@ def main():
     bwd_key = kernel_sources_hash("fa_bwd_sm103a.cu") + ":" + w.name
     peak_source = ("%s burst bf16 (MEASURED_PEAKS.json)" % peaks_src if peaks_src == "measured"
                    else "fallback 1.9 PFLOP/s bf16")
-    fwd_achieved = w.flops_fwd() / (first_ms * 1e-3) / 1e12
+    fwd_achieved = flops_fwd / (first_ms * 1e-3) / 1e12
     if split:
         # the merge reads every LSE part and the O parts of rows with an allowed key in that
         # range, and writes O (bf16) and LSE
@@ -466,15 +561,17 @@ def main():
                               "achieved": merge_gbs, "peak": hbm, "frac": merge_gbs / hbm},
                     "one_pass_fwd_ms": one_pass_ms, "sources": fwd_key}
     elif w.backward:
-        bwd_achieved = w.flops_bwd() / (second_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": "fa_bwd (bwd_main + preprocess + dq_convert)",
+        bwd_achieved = flops_bwd / (second_ms * 1e-3) / 1e12
+        bname, fname = ("fa_bwd_masked", "fa_fwd_masked") if masked else ("fa_bwd", "fa_fwd")
+        roofline = {"bound": "tensor",
+                    "kernel": "%s (bwd_main + preprocess + dq_convert)" % bname,
                     "achieved": bwd_achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": bwd_achieved / peak,
                     "traffic": NCU_TRAFFIC.get(bwd_key), "peak_source": peak_source,
-                    "flops_per_launch": w.flops_bwd(),
-                    "fwd": {"kernel": "fa_fwd", "achieved": fwd_achieved,
+                    "flops_per_launch": flops_bwd,
+                    "fwd": {"kernel": fname, "achieved": fwd_achieved,
                             "frac": fwd_achieved / peak, "ms": first_ms,
-                            "flops_per_launch": w.flops_fwd()},
+                            "flops_per_launch": flops_fwd},
                     "bwd_ms": second_ms, "sources": bwd_key}
     else:
         roofline = {"bound": "tensor", "kernel": "fa_fwd", "achieved": fwd_achieved,
@@ -488,7 +585,7 @@ def main():
 
     if rank == 0:
         if w.backward:
-            what = "fwd+bwd"
+            what = "fwd+bwd" + (" under a general mask (%s)" % w.mask if masked else "")
             l2 = ("inputs larger than L2 (Q,K,V,dO,O = 5 x %.0f MB), no flush"
                   % (q.numel() * 2 / 1e6))
         else:
@@ -504,7 +601,10 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
                            "causal": w.causal, "seed": w.seed, "scale": w.scale,
-                           "num_splits": S, "l2": l2, "parallelism": "replicas x%d" % ws},
+                           "num_splits": S, "mask": w.mask or None,
+                           "flops": "4 d per allowed pair (x3.5 fwd+bwd)" if masked else
+                                    "4 B Hq N^2 d (/2 causal, x3.5 fwd+bwd)",
+                           "l2": l2, "parallelism": "replicas x%d" % ws},
                 "fwd_tflops": fwd_achieved,
                 "fwd_frac_of_peak": fwd_achieved / peak,
                 "fwd_bwd_frac_of_peak": value / ws / peak if w.backward else None,
