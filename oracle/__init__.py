@@ -68,6 +68,19 @@ def _load():
             lib.oracle_backward_dq_rows_masked.argtypes = masked + [_D, _D, _D, _D, ctypes.c_int, _L, _D]
             lib.oracle_backward_dkv_cols_masked.argtypes = masked + [_D, _D, _D, _D, ctypes.c_int, _L,
                                                                      _D, _D]
+            u32, u64, dbl = ctypes.c_uint32, ctypes.c_uint64, ctypes.c_double
+            _U32P = ctypes.POINTER(ctypes.c_uint32)
+            lib.oracle_philox4x32_10.argtypes = [_U32P, _U32P, _U32P]
+            lib.oracle_philox4x32_10.restype = None
+            lib.oracle_dropout_threshold.argtypes = [dbl]
+            lib.oracle_dropout_threshold.restype = u32
+            lib.oracle_dropout_mask.argtypes = [ctypes.c_int, ctypes.c_int, u64, u32, dbl, _U8]
+            drop = [ctypes.c_int] * 6 + [dbl, dbl, u64, u32]
+            lib.oracle_attention_forward_dropout.argtypes = drop + [_D, _D, _D, _D, _D]
+            lib.oracle_attention_backward_dropout.argtypes = drop + [_D, _D, _D, _D, _D, _D, _D]
+            for name in ("oracle_dropout_mask", "oracle_attention_forward_dropout",
+                         "oracle_attention_backward_dropout"):
+                getattr(lib, name).restype = ctypes.c_int
             for name in ("oracle_attention_forward", "oracle_attention_backward",
                          "oracle_forward_rows", "oracle_backward_dq_rows",
                          "oracle_backward_dkv_cols", "oracle_num_threads",
@@ -333,3 +346,54 @@ def backward_dkv_cols_masked(Q, K, V, dO, causal: bool, scale: float, mask: Mask
                                                  _ptr(dV))
     _check(rc, "oracle_backward_dkv_cols_masked")
     return dK, dV
+
+
+# ----------------------------------------------------------------------------- dropout
+def philox4x32_10(counter, key):
+    """Philox4x32-10 (Salmon et al., SC'11) of a 4-word counter and 2-word key -> 4 words."""
+    c = (ctypes.c_uint32 * 4)(*[int(x) & 0xFFFFFFFF for x in counter])
+    k = (ctypes.c_uint32 * 2)(*[int(x) & 0xFFFFFFFF for x in key])
+    out = (ctypes.c_uint32 * 4)()
+    _load().oracle_philox4x32_10(c, k, out)
+    return tuple(int(x) for x in out)
+
+
+def dropout_threshold(p: float) -> int:
+    """floor((1 - p) 2^32): a key is kept when its Philox word is below this."""
+    return int(_load().oracle_dropout_threshold(float(p)))
+
+
+def dropout_mask(BH: int, N: int, seed: int, offset: int, p: float):
+    """Keep decisions Z [BH, N, N] uint8 of every (b*Hq + hq, query, key)."""
+    Z = np.zeros((BH, N, N), dtype=np.uint8)
+    rc = _load().oracle_dropout_mask(BH, N, int(seed), int(offset), float(p), _ptr(Z, _U8))
+    _check(rc, "oracle_dropout_mask")
+    return Z
+
+
+def forward_dropout(Q, K, V, causal: bool, scale: float, p: float, seed: int, offset: int):
+    """Forward with dropout: (O [B, Hq, N, d], LSE [B, Hq, N])."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, Hq, Hkv, N, d = _shape(Q, K)
+    O = np.zeros((B, Hq, N, d))
+    L = np.zeros((B, Hq, N))
+    rc = _load().oracle_attention_forward_dropout(B, Hq, Hkv, N, d, int(bool(causal)),
+                                                  float(scale), float(p), int(seed), int(offset),
+                                                  _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L))
+    _check(rc, "oracle_attention_forward_dropout")
+    return O, L
+
+
+def backward_dropout(Q, K, V, dO, causal: bool, scale: float, p: float, seed: int, offset: int):
+    """Backward with dropout: (dQ [B, Hq, N, d], dK, dV [B, Hkv, N, d])."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, Hq, Hkv, N, d = _shape(Q, K)
+    dQ = np.zeros((B, Hq, N, d))
+    dK = np.zeros((B, Hkv, N, d))
+    dV = np.zeros((B, Hkv, N, d))
+    rc = _load().oracle_attention_backward_dropout(B, Hq, Hkv, N, d, int(bool(causal)),
+                                                   float(scale), float(p), int(seed), int(offset),
+                                                   _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ),
+                                                   _ptr(dK), _ptr(dV))
+    _check(rc, "oracle_attention_backward_dropout")
+    return dQ, dK, dV

@@ -41,6 +41,16 @@
  *    Hq or B * Hq heads.  A row with no allowed key (every row i >= q_len[b], or one whose tiles
  *    are all masked) gets O = 0 and LSE = -inf, and passes no gradient.
  *
+ *  - Dropout (the *_dropout entry points): the reading note ("other operators") lists dropout
+ *    among the operations fused per block.  Read as inverted dropout on the normalised P:
+ *    P~_ij = P_ij Z_ij / (1 - p) with Z_ij in {0, 1}, O = P~ V; LSE is that of the undropped
+ *    P.  Z_ij = 1 ("keep") iff word (j mod 4) of Philox4x32-10 (Salmon, Moraes, Dror and Shaw,
+ *    "Parallel random numbers: as easy as 1, 2, 3", SC'11) at counter (j / 4, i, b * Hq + hq,
+ *    offset) and key (seed mod 2^32, seed / 2^32) is below floor((1 - p) 2^32).  The backward
+ *    follows by the chain rule: dV = P~^T dO, dP~ = dO V^T, dS = P (.) (Z / (1 - p) (.) dP~ - D)
+ *    with D_i = <dO_i, O_i> of the dropped O (since sum_j P_ij Z_ij / (1 - p) <dO_i, v_j> =
+ *    <dO_i, O_i>), dQ = scale dS K, dK = scale dS^T Q.
+ *
  * Layout: every tensor is contiguous [B, H, N, d] fp64 (d fastest); K, V, dK, dV use H = Hkv.
  * LSE is [B, Hq, N].  Causal means key j <= query i (top-left aligned, Nq = Nk = N).
  *
@@ -581,4 +591,176 @@ int oracle_backward_dkv_cols_masked(int B, int Hq, int Hkv, int N, int d, int ca
         make_mask(&M, causal, B, Hq, N, q_len, k_len, block_mask, mask_heads, block))
         return 1;
     return dkv_cols_impl(&M, B, Hq, Hkv, N, d, scale, Q, K, V, dO, ncols, cols, dK_rows, dV_rows);
+}
+
+/* ------------------------------------------------------------------------------- dropout */
+
+/*
+ * Philox4x32-10 (Salmon et al., SC'11): ten rounds; each multiplies words 0 and 2 by the two
+ * round multipliers into 64-bit products, and the new state is
+ *   (hi(M1 x2) ^ x1 ^ k0, lo(M1 x2), hi(M0 x0) ^ x3 ^ k1, lo(M0 x0)),
+ * after which the key is bumped by the two Weyl increments.
+ */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    const uint64_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3], k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = M0 * (uint64_t)x0, p1 = M1 * (uint64_t)x2;
+        const uint32_t y0 = (uint32_t)(p1 >> 32) ^ x1 ^ k0;
+        const uint32_t y1 = (uint32_t)p1;
+        const uint32_t y2 = (uint32_t)(p0 >> 32) ^ x3 ^ k1;
+        const uint32_t y3 = (uint32_t)p0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+        k0 += W0;
+        k1 += W1;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+/* floor((1 - p) 2^32) for 0 < p < 1 (0 for an invalid p). */
+uint32_t oracle_dropout_threshold(double p) {
+    if (!(p > 0.0) || !(p < 1.0)) return 0;
+    const double t = floor((1.0 - p) * 4294967296.0);
+    return t >= 4294967295.0 ? 4294967295u : (uint32_t)t;
+}
+
+static int dropout_keep(uint64_t seed, uint32_t offset, uint32_t thresh, i64 bh, i64 i, i64 j) {
+    const uint32_t ctr[4] = {(uint32_t)(j >> 2), (uint32_t)i, (uint32_t)bh, offset};
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t r[4];
+    oracle_philox4x32_10(ctr, key, r);
+    return r[j & 3] < thresh;
+}
+
+/* The keep decisions Z [BH, N, N] (1 = keep) of every (head, query, key). */
+int oracle_dropout_mask(int BH, int N, uint64_t seed, uint32_t offset, double p,
+                        unsigned char *Z_out) {
+    if (BH < 1 || N < 1) return 1;
+    const uint32_t thresh = oracle_dropout_threshold(p);
+    if (thresh == 0) return 1;
+#pragma omp parallel for schedule(static) collapse(2)
+    for (i64 bh = 0; bh < BH; ++bh)
+        for (i64 i = 0; i < N; ++i)
+            for (i64 j = 0; j < N; ++j)
+                Z_out[(bh * N + i) * N + j] = (unsigned char)dropout_keep(seed, offset, thresh, bh, i, j);
+    return 0;
+}
+
+/* Forward with dropout on every head: O [B, Hq, N, d] = P~ V, LSE [B, Hq, N] of the undropped P. */
+int oracle_attention_forward_dropout(int B, int Hq, int Hkv, int N, int d, int causal,
+                                     double scale, double p, uint64_t seed, uint32_t offset,
+                                     const double *Q, const double *K, const double *V,
+                                     double *O_out, double *LSE_out) {
+    if (check_shape(B, Hq, Hkv, N, d)) return 1;
+    const uint32_t thresh = oracle_dropout_threshold(p);
+    if (thresh == 0) return 1;
+    const int G = Hq / Hkv;
+    const i64 nd = (i64)N * d;
+    const mask_t M = causal_only(causal, B, Hq, N);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *prow = (double *)malloc(sizeof(double) * N);
+        double *ofull = (double *)malloc(sizeof(double) * d);
+#pragma omp for schedule(dynamic, 16) collapse(2)
+        for (i64 bh = 0; bh < (i64)B * Hq; ++bh)
+            for (i64 i = 0; i < N; ++i) {
+                if (!prow || !ofull) { bad = 2; continue; }
+                const i64 b = bh / Hq, hq = bh % Hq, hk = hq / G;
+                const double *k = K + (b * Hkv + hk) * nd, *v = V + (b * Hkv + hk) * nd;
+                LSE_out[bh * N + i] = softmax_row(&M, b, hq, Q + bh * nd + i * d, k, v, i, N, d,
+                                                  scale, prow, ofull);
+                double *o = O_out + bh * nd + i * d;
+                for (int c = 0; c < d; ++c) o[c] = 0.0;
+                for (i64 j = 0; j < N; ++j) {
+                    if (prow[j] == 0.0 || !dropout_keep(seed, offset, thresh, bh, i, j)) continue;
+                    const double w = prow[j] / (1.0 - p);
+                    for (int c = 0; c < d; ++c) o[c] += w * v[j * d + c];
+                }
+            }
+        free(prow); free(ofull);
+    }
+    return bad;
+}
+
+/* Backward with dropout on every KV group: dQ [B, Hq, N, d], dK and dV [B, Hkv, N, d]. */
+int oracle_attention_backward_dropout(int B, int Hq, int Hkv, int N, int d, int causal,
+                                      double scale, double p, uint64_t seed, uint32_t offset,
+                                      const double *Q, const double *K, const double *V,
+                                      const double *dO, double *dQ_out, double *dK_out,
+                                      double *dV_out) {
+    if (check_shape(B, Hq, Hkv, N, d)) return 1;
+    const uint32_t thresh = oracle_dropout_threshold(p);
+    if (thresh == 0) return 1;
+    const int G = Hq / Hkv;
+    const i64 nn = (i64)N * N, nd = (i64)N * d;
+    const mask_t M = causal_only(causal, B, Hq, N);
+    double *P = (double *)malloc(sizeof(double) * nn);     /* P, then dS */
+    double *Mk = (double *)malloc(sizeof(double) * nn);    /* Z / (1 - p) */
+    double *O = (double *)malloc(sizeof(double) * nd);
+    double *D = (double *)malloc(sizeof(double) * N);
+    if (!P || !Mk || !O || !D) { free(P); free(Mk); free(O); free(D); return 2; }
+    for (i64 bk = 0; bk < (i64)B * Hkv; ++bk) {
+        const i64 b = bk / Hkv, hk = bk % Hkv;
+        const double *k = K + bk * nd, *v = V + bk * nd;
+        double *dk = dK_out + bk * nd, *dv = dV_out + bk * nd;
+        memset(dk, 0, sizeof(double) * nd);
+        memset(dv, 0, sizeof(double) * nd);
+        for (int r = 0; r < G; ++r) {
+            const i64 hq = hk * G + r, bh = b * Hq + hq;
+            const double *q = Q + bh * nd, *dor = dO + bh * nd;
+            double *dq = dQ_out + bh * nd;
+            /* forward: P, Z / (1 - p), the dropped O and D_i = <dO_i, O_i> */
+#pragma omp parallel
+            {
+                double *ofull = (double *)malloc(sizeof(double) * d);
+#pragma omp for schedule(dynamic, 16)
+                for (i64 i = 0; i < N; ++i) {
+                    softmax_row(&M, b, hq, q + i * d, k, v, i, N, d, scale, P + i * N,
+                                ofull ? ofull : O + i * d);
+                    double *o = O + i * d;
+                    for (int c = 0; c < d; ++c) o[c] = 0.0;
+                    for (i64 j = 0; j < N; ++j) {
+                        Mk[i * N + j] = dropout_keep(seed, offset, thresh, bh, i, j) ? 1.0 / (1.0 - p) : 0.0;
+                        const double w = P[i * N + j] * Mk[i * N + j];
+                        if (w != 0.0)
+                            for (int c = 0; c < d; ++c) o[c] += w * v[j * d + c];
+                    }
+                    D[i] = dot(dor + i * d, o, d);
+                }
+                free(ofull);
+            }
+            /* dV_j += sum_i P~_ij dO_i */
+#pragma omp parallel for schedule(dynamic, 16)
+            for (i64 j = 0; j < N; ++j)
+                for (i64 i = 0; i < N; ++i) {
+                    const double w = P[i * N + j] * Mk[i * N + j];
+                    if (w != 0.0)
+                        for (int c = 0; c < d; ++c) dv[j * d + c] += w * dor[i * d + c];
+                }
+            /* dS_ij = P_ij (Z_ij / (1 - p) <dO_i, v_j> - D_i), over P; dQ_i = scale sum_j dS_ij k_j */
+#pragma omp parallel for schedule(dynamic, 16)
+            for (i64 i = 0; i < N; ++i) {
+                double *row = P + i * N;
+                for (int c = 0; c < d; ++c) dq[i * d + c] = 0.0;
+                for (i64 j = 0; j < N; ++j) {
+                    if (row[j] == 0.0) continue;
+                    row[j] = row[j] * (Mk[i * N + j] * dot(dor + i * d, v + j * d, d) - D[i]);
+                    for (int c = 0; c < d; ++c) dq[i * d + c] += row[j] * k[j * d + c];
+                }
+                for (int c = 0; c < d; ++c) dq[i * d + c] *= scale;
+            }
+            /* dK_j += scale sum_i dS_ij q_i */
+#pragma omp parallel for schedule(dynamic, 16)
+            for (i64 j = 0; j < N; ++j)
+                for (i64 i = 0; i < N; ++i) {
+                    const double ds = P[i * N + j];
+                    if (ds != 0.0)
+                        for (int c = 0; c < d; ++c) dk[j * d + c] += scale * ds * q[i * d + c];
+                }
+        }
+    }
+    free(P); free(Mk); free(O); free(D);
+    return 0;
 }
