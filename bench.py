@@ -85,10 +85,10 @@ def allowed_pairs(w, q_len, k_len, block_mask, B=None, heads=None) -> float:
 
 
 def kernel_sources_hash(kernel_file: str) -> str:
-    """Key prefix for NCU_TRAFFIC: the kernel's source file and the device primitives it uses."""
+    """Key prefix for NCU_TRAFFIC: the kernel's source file and the device headers it uses."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_89_gb300", "csrc")
-    for fn in (kernel_file, "fa_ptx.cuh"):
+    for fn in (kernel_file, "fa_ptx.cuh", "fa_philox.cuh"):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return "%s:%s" % (kernel_file, h.hexdigest()[:16])
@@ -261,6 +261,31 @@ def cpu_oracle_masked_sample(w, budget_s: float, inputs=None):
             "seconds": t_total}
 
 
+def cpu_oracle_dropout_sample(w, budget_s: float, inputs=None):
+    """Dropout workloads: times the fp64 oracle's dropout forward + backward on the first
+    (batch, query head) slice, whose global head index the oracle reproduces on the slice."""
+    import torch
+
+    import oracle
+    from exact_attention_89_gb300.inputs import workload_inputs
+    Q, K, V, dO = inputs if inputs is not None else workload_inputs(w)
+    sl = (slice(0, 1), slice(0, 1))
+    q, k, v, do = (t[sl].to(torch.float64).numpy() for t in (Q, K, V, dO))
+    done, t_total = 0, 0.0
+    while t_total < budget_s or done == 0:
+        t0 = time.perf_counter()
+        oracle.forward_dropout(q, k, v, w.causal, w.scale, w.dropout, w.seed, 0)
+        oracle.backward_dropout(q, k, v, do, w.causal, w.scale, w.dropout, w.seed, 0)
+        t_total += time.perf_counter() - t0
+        done += 1
+    per_head = (w.flops_fwd() + w.flops_bwd()) / (w.B * w.Hq)
+    return {"value": per_head * done / t_total / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d pass(es) over head 0 of %s (N%d d%d causal, dropout %.2f), fp64 "
+                      "forward+backward, %.1f s" % (done, w.name, w.N, w.d, w.dropout, t_total),
+            "seconds": t_total}
+
+
 def cpu_oracle_sample(w, budget_s: float, max_heads: int, inputs=None, first_group: int = 0):
     """Times the fp64 oracle (forward + backward of whole KV groups) on the host cores."""
     import torch
@@ -271,6 +296,8 @@ def cpu_oracle_sample(w, budget_s: float, max_heads: int, inputs=None, first_gro
         return cpu_oracle_rows_sample(w, budget_s, inputs)
     if w.mask:
         return cpu_oracle_masked_sample(w, budget_s, inputs)
+    if w.dropout:
+        return cpu_oracle_dropout_sample(w, budget_s, inputs)
     Q, K, V, dO = inputs if inputs is not None else workload_inputs(w)
     G = w.Hq // w.Hkv
     heads_done, t_total = 0, 0.0
@@ -397,6 +424,8 @@ def main():
             fa.fa_fwd_split(q, k, v, Op, Lp, w.causal, w.scale, S)
         elif masked:
             fa.fa_fwd_masked(q, k, v, O, LSE, w.causal, w.scale, mq, mkk, mbm)
+        elif w.dropout:
+            fa.fa_fwd_dropout(q, k, v, O, LSE, w.causal, w.scale, w.dropout, w.seed, 0)
         else:
             fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
 
@@ -406,6 +435,9 @@ def main():
             fa.fa_merge(Op, Lp, O, LSE)
         elif masked:
             fa.fa_bwd_masked(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsp, mq, mkk, mbm)
+        elif w.dropout:
+            fa.fa_bwd_dropout(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, w.dropout,
+                              w.seed, 0, wsp)
         elif w.backward:
             fa.fa_bwd(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsp)
 
@@ -506,12 +538,18 @@ def main():
             res = fa.attention_forward_split(qd, kd, vd, w.causal, w.scale, num_splits=S)
         elif masked:
             res = fa.attention_forward_masked(qd, kd, vd, w.causal, w.scale, mq, mkk, mbm)
+        elif w.dropout:
+            res = fa.attention_forward_dropout(qd, kd, vd, w.causal, w.scale, w.dropout, w.seed)
         else:
             res = fa.attention_forward(qd, kd, vd, w.causal, w.scale)
         if masked:
             res = res + fa.attention_backward_masked(qd, kd, vd, res[0], dev_in[3], res[1],
                                                      w.causal, w.scale, mq, mkk, mbm,
                                                      workspace=wsp)
+        elif w.dropout:
+            res = res + fa.attention_backward_dropout(qd, kd, vd, res[0], dev_in[3], res[1],
+                                                      w.causal, w.scale, w.dropout, w.seed,
+                                                      workspace=wsp)
         elif w.backward:
             res = res + fa.attention_backward(qd, kd, vd, res[0], dev_in[3], res[1], w.causal,
                                               w.scale, workspace=wsp)
@@ -562,7 +600,8 @@ def main():
                     "one_pass_fwd_ms": one_pass_ms, "sources": fwd_key}
     elif w.backward:
         bwd_achieved = flops_bwd / (second_ms * 1e-3) / 1e12
-        bname, fname = ("fa_bwd_masked", "fa_fwd_masked") if masked else ("fa_bwd", "fa_fwd")
+        bname, fname = (("fa_bwd_masked", "fa_fwd_masked") if masked else
+                        ("fa_bwd_dropout", "fa_fwd_dropout") if w.dropout else ("fa_bwd", "fa_fwd"))
         roofline = {"bound": "tensor",
                     "kernel": "%s (bwd_main + preprocess + dq_convert)" % bname,
                     "achieved": bwd_achieved, "peak": peak, "unit": "TFLOP/s",
@@ -585,7 +624,8 @@ def main():
 
     if rank == 0:
         if w.backward:
-            what = "fwd+bwd" + (" under a general mask (%s)" % w.mask if masked else "")
+            what = "fwd+bwd" + (" under a general mask (%s)" % w.mask if masked else
+                                " with dropout p=%g" % w.dropout if w.dropout else "")
             l2 = ("inputs larger than L2 (Q,K,V,dO,O = 5 x %.0f MB), no flush"
                   % (q.numel() * 2 / 1e6))
         else:

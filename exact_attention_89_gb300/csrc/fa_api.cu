@@ -175,10 +175,104 @@ fa_status check_mask(int B, int Hq, const int *q_len, const int *k_len,
     mk->mask_heads = block_mask ? mask_heads : 0;
     return FA_OK;
 }
+// Host checks of a dropout probability; fills the kernels' DropoutArgs (p = 0: no dropout).
+fa_status make_dropout(float p, unsigned long long seed, unsigned offset, DropoutArgs *dr,
+                       bool *active) {
+    if (!(p >= 0.f) || !(p < 1.f)) return FA_ERR_INVALID_ARG;   // also rejects NaN
+    *active = p > 0.f;
+    const double t = std::floor((1.0 - static_cast<double>(p)) * 4294967296.0);
+    set_round_keys(dr, seed);
+    dr->offset = offset;
+    dr->thresh = t >= 4294967295.0 ? 0xFFFFFFFFu : static_cast<uint32_t>(t);
+    dr->rscale = static_cast<float>(1.0 / (1.0 - static_cast<double>(p)));
+    return FA_OK;
+}
 }  // namespace
 }  // namespace fa
 
 extern "C" {
+
+fa_status fa_fwd_dropout(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                         int Hq, int Hkv, int N, int d, int causal, float scale, float p_drop,
+                         unsigned long long seed, unsigned offset, cudaStream_t stream) {
+    fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    fa::DropoutArgs dr;
+    bool active = false;
+    if ((st = fa::make_dropout(p_drop, seed, offset, &dr, &active)) != FA_OK) return st;
+    if (!active) return fa_fwd(Q, K, V, O, LSE, B, Hq, Hkv, N, d, causal, scale, stream);
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!fa::aligned16(Q) || !fa::aligned16(K) || !fa::aligned16(V) || !fa::aligned16(O) ||
+        !fa::aligned16(LSE))
+        return FA_ERR_MISALIGNED;
+    fa::DeviceInfo *di = nullptr;
+    if ((st = fa::current_device(&di, true)) != FA_OK) return st;
+    const Problem p{B, Hq, Hkv, N, d, causal ? 1 : 0, scale};
+    CUtensorMap tq, tk, tv;
+    if (!fa::encode_bf16(&tq, Q, d, N, 1LL * B * Hq, 128) ||
+        !fa::encode_bf16(&tk, K, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tv, V, d, N, 1LL * B * Hkv, 128))
+        return FA_ERR_CUDA;
+    return fa::from_cuda(fa::launch_fwd_dropout_bf16(p, tq, tk, tv, O, LSE, dr, di->status, stream));
+}
+
+fa_status fa_bwd_dropout(const void *Q, const void *K, const void *V, const void *O,
+                         const void *dO, const float *LSE, void *dQ, void *dK, void *dV, int B,
+                         int Hq, int Hkv, int N, int d, int causal, float scale, float p_drop,
+                         unsigned long long seed, unsigned offset, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+    fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    fa::DropoutArgs dr;
+    bool active = false;
+    if ((st = fa::make_dropout(p_drop, seed, offset, &dr, &active)) != FA_OK) return st;
+    if (!active)
+        return fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, N, d, causal, scale, workspace,
+                      workspace_bytes, stream);
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!fa::aligned16(Q) || !fa::aligned16(K) || !fa::aligned16(V) || !fa::aligned16(O) ||
+        !fa::aligned16(dO) || !fa::aligned16(LSE) || !fa::aligned16(dQ) || !fa::aligned16(dK) ||
+        !fa::aligned16(dV))
+        return FA_ERR_MISALIGNED;
+    if (!fa::aligned16(workspace) || workspace_bytes < fa_bwd_workspace_bytes(B, Hq, N, d))
+        return FA_ERR_WORKSPACE;
+    fa::DeviceInfo *di = nullptr;
+    if ((st = fa::current_device(&di, true)) != FA_OK) return st;
+    const Problem p{B, Hq, Hkv, N, d, causal ? 1 : 0, scale};
+    const size_t rows = static_cast<size_t>(B) * Hq * N;
+    float *Dvec = static_cast<float *>(workspace);
+    float *dQacc = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                             fa::align256(rows * sizeof(float)));
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+    if (!fa::encode_bf16(&tq, Q, d, N, 1LL * B * Hq, 64) ||
+        !fa::encode_bf16(&tk, K, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tv, V, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tdo, dO, d, N, 1LL * B * Hq, 64) ||
+        !fa::encode_bf16(&tdk, dK, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tdv, dV, d, N, 1LL * B * Hkv, 128))
+        return FA_ERR_CUDA;
+    cudaError_t e = fa::launch_bwd_preprocess_bf16(p, O, dO, Dvec, dQacc, stream);
+    if (e == cudaSuccess)
+        e = fa::launch_bwd_main_dropout_bf16(p, tq, tk, tv, tdo, tdk, tdv, LSE, Dvec, dQacc, dr,
+                                             di->status, stream);
+    if (e == cudaSuccess) e = fa::launch_bwd_dq_convert_bf16(p, dQacc, dQ, stream);
+    return fa::from_cuda(e);
+}
+
+fa_status fa_dropout_mask(int BH, int N, float p_drop, unsigned long long seed, unsigned offset,
+                          unsigned char *Z, cudaStream_t stream) {
+    if (BH < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    fa::DropoutArgs dr;
+    bool active = false;
+    fa_status st = fa::make_dropout(p_drop, seed, offset, &dr, &active);
+    if (st != FA_OK) return st;
+    if (Z == nullptr) return FA_ERR_MISALIGNED;
+    fa::DeviceInfo *di = nullptr;
+    if ((st = fa::current_device(&di, true)) != FA_OK) return st;
+    const size_t bytes = static_cast<size_t>(BH) * N * N;
+    if (!active) return fa::from_cuda(cudaMemsetAsync(Z, 1, bytes, stream));
+    return fa::from_cuda(fa::launch_dropout_mask(dr, BH, N, Z, stream));
+}
 
 fa_status fa_fwd_masked(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
                         int Hq, int Hkv, int N, int d, int causal, float scale, const int *q_len,

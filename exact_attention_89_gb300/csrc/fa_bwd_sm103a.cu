@@ -33,6 +33,7 @@
 #include <cmath>
 
 #include "fa_internal.h"
+#include "fa_philox.cuh"
 #include "fa_ptx.cuh"
 
 namespace fa {
@@ -86,14 +87,19 @@ __device__ __forceinline__ int first_q_tile(int jb) {
 // MASK = true: the general mask mk on top of the causal rule.  The CTA lists, before the roles
 // split, the steps whose tile its mask keeps (rows past the valid length and key blocks past it
 // drop out); a key block with no step at all gets dK = dV = 0.
-template <int D, int DR, bool CAUSAL, bool MASK>
+// DROP = true: dropout on P (fa_philox.cuh has the keep rule): dV takes P Z / (1 - p) and
+// dS = P (Z / (1 - p) dP - D); the keep words of a quad of key rows come from one Philox call
+// per query, spread over the quad's four lanes and exchanged by shuffles.
+template <int D, int DR, bool CAUSAL, bool MASK, bool DROP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                     const float *__restrict__ LSE, const float *__restrict__ Dvec,
                     float *__restrict__ dQacc, int Hq, int Hkv, int N, int BHkv, int HC,
-                    float scale, float scale_log2, const MaskArgs mk, unsigned *status) {
+                    float scale, float scale_log2, const MaskArgs mk, const DropoutArgs drop,
+                    unsigned *status) {
+    static_assert(!(MASK && DROP), "one variant at a time");
     // Laid out for d = 128.  With a real head dim DR = 64 the tensor maps are 64 wide, so the
     // second 64-column chunk of every load is TMA zero fill: all products see zero-padded
     // operands and are unchanged; only the dQ reductions and the dK / dV stores use DR.
@@ -389,12 +395,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 uint32_t pp[32], dd[32];
+                uint64_t keep = ~0ull;                  // bit c: query q0 + c keeps this key
+                if constexpr (DROP) {
+                    // one Philox call per query of the quad's 4t + (lane & 3), then a 4 x 4
+                    // transpose: round k takes from lane (lane ^ k) the word of this lane's key
+                    const int qd = lane & 3;
+                    const uint32_t mkey = static_cast<uint32_t>(key) >> 2;
+                    keep = 0ull;
+#pragma unroll 4
+                    for (int t = 0; t < BQ / 4; ++t) {
+                        const uint4 w = dropout_words(drop, mkey, static_cast<uint32_t>(q0 + 4 * t + qd),
+                                                      static_cast<uint32_t>(bhq));
 #pragma unroll
-                for (int c = 0; c < BQ; c += 2) pp[c >> 1] = pack_bf16x2(pf[c], pf[c + 1]);
+                        for (int k = 0; k < 4; ++k) {
+                            const int sel = qd ^ k;
+                            const uint32_t mine = sel == 0 ? w.x : sel == 1 ? w.y : sel == 2 ? w.z : w.w;
+                            const uint32_t got = k == 0 ? mine : __shfl_xor_sync(0xffffffffu, mine, k);
+                            keep |= static_cast<uint64_t>(got < drop.thresh) << (4 * t + (qd ^ k));
+                        }
+                    }
+                }
+                auto kept = [&](int c) -> bool { return !DROP || ((keep >> c) & 1ull); };
+#pragma unroll
+                for (int c = 0; c < BQ; c += 2) {
+                    if constexpr (DROP)
+                        pp[c >> 1] = pack_bf16x2(kept(c) ? pf[c] * drop.rscale : 0.f,
+                                                 kept(c + 1) ? pf[c + 1] * drop.rscale : 0.f);
+                    else
+                        pp[c >> 1] = pack_bf16x2(pf[c], pf[c + 1]);
+                }
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t dr[32];
                     tmem_ld_x32(buf + B_DPT + 32 * h, dr);
+                    if constexpr (DROP) {
+                        // dP of a dropped pair does not reach P; a kept one is scaled by 1/(1-p)
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            dr[c] = __float_as_uint(kept(32 * h + c) ? __uint_as_float(dr[c]) * drop.rscale : 0.f);
+                    }
 #pragma unroll
                     for (int c = 0; c < 32; c += 4) {
                         const float4 dv = d4[(32 * h + c) >> 2];
@@ -577,11 +616,12 @@ cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const vo
 }
 
 namespace bwd {
-template <bool MASK>
+template <bool MASK, bool DROP>
 cudaError_t launch_main(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                         const CUtensorMap &tmV, const CUtensorMap &tmdO, const CUtensorMap &tmdK,
                         const CUtensorMap &tmdV, const float *LSE, const float *D, float *dQacc,
-                        const MaskArgs &mk, unsigned *status, cudaStream_t stream) {
+                        const MaskArgs &mk, const DropoutArgs &dr, unsigned *status,
+                        cudaStream_t stream) {
     if (p.d != 128 && p.d != 64) return cudaErrorInvalidValue;
     const int BHkv = p.B * p.Hkv;
     const long long nkb = (p.N + BKV - 1) / BKV;
@@ -596,12 +636,14 @@ cudaError_t launch_main(const Problem &p, const CUtensorMap &tmQ, const CUtensor
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                           const float *, const float *, float *, int, int, int, int, int, float, float,
-                          MaskArgs, unsigned *);
+                          MaskArgs, DropoutArgs, unsigned *);
     Kern kern;
     if (p.d == 128)
-        kern = p.causal ? bwd_main_kernel<128, 128, true, MASK> : bwd_main_kernel<128, 128, false, MASK>;
+        kern = p.causal ? bwd_main_kernel<128, 128, true, MASK, DROP>
+                        : bwd_main_kernel<128, 128, false, MASK, DROP>;
     else
-        kern = p.causal ? bwd_main_kernel<128, 64, true, MASK> : bwd_main_kernel<128, 64, false, MASK>;
+        kern = p.causal ? bwd_main_kernel<128, 64, true, MASK, DROP>
+                        : bwd_main_kernel<128, 64, false, MASK, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // the in-kernel register split needs at least REGS_NEEDED registers at launch
@@ -610,7 +652,7 @@ cudaError_t launch_main(const Problem &p, const CUtensorMap &tmQ, const CUtensor
     if (attr.numRegs * NUM_THREADS < REGS_NEEDED) return cudaErrorInvalidConfiguration;
     kern<<<static_cast<unsigned>(grid), NUM_THREADS, smem, stream>>>(
         tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, HC, p.scale,
-        scale_log2, mk, status);
+        scale_log2, mk, dr, status);
     return cudaGetLastError();
 }
 }  // namespace bwd
@@ -620,8 +662,8 @@ cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const
                                  const CUtensorMap &tmdK, const CUtensorMap &tmdV,
                                  const float *LSE, const float *D, float *dQacc, unsigned *status,
                                  cudaStream_t stream) {
-    return bwd::launch_main<false>(p, tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, MaskArgs{},
-                                   status, stream);
+    return bwd::launch_main<false, false>(p, tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc,
+                                          MaskArgs{}, DropoutArgs{}, status, stream);
 }
 
 cudaError_t launch_bwd_main_masked_bf16(const Problem &p, const CUtensorMap &tmQ,
@@ -630,8 +672,18 @@ cudaError_t launch_bwd_main_masked_bf16(const Problem &p, const CUtensorMap &tmQ
                                         const CUtensorMap &tmdV, const float *LSE, const float *D,
                                         float *dQacc, const MaskArgs &mk, unsigned *status,
                                         cudaStream_t stream) {
-    return bwd::launch_main<true>(p, tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, mk, status,
-                                  stream);
+    return bwd::launch_main<true, false>(p, tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc, mk,
+                                         DropoutArgs{}, status, stream);
+}
+
+cudaError_t launch_bwd_main_dropout_bf16(const Problem &p, const CUtensorMap &tmQ,
+                                         const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                         const CUtensorMap &tmdO, const CUtensorMap &tmdK,
+                                         const CUtensorMap &tmdV, const float *LSE, const float *D,
+                                         float *dQacc, const DropoutArgs &dr, unsigned *status,
+                                         cudaStream_t stream) {
+    return bwd::launch_main<false, true>(p, tmQ, tmK, tmV, tmdO, tmdK, tmdV, LSE, D, dQacc,
+                                         MaskArgs{}, dr, status, stream);
 }
 
 cudaError_t launch_bwd_dq_convert_bf16(const Problem &p, const float *dQacc, void *dQ,

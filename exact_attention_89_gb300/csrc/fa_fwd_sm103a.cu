@@ -30,6 +30,7 @@
 #include <cmath>
 
 #include "fa_internal.h"
+#include "fa_philox.cuh"
 #include "fa_ptx.cuh"
 
 namespace fa {
@@ -178,13 +179,15 @@ __device__ __forceinline__ int item_index(int r) {
 // LSE_parts [S, B*Hq, N] (LSE = -inf where a row has no allowed key in the range).
 // MASK = true: the general mask mk on top of the causal rule; rows with no allowed key (and rows
 // past the batch's valid length) get O = 0 and LSE = -inf.
-template <int D, bool CAUSAL, bool SPLIT, bool MASK>
+// DROP = true: dropout on P (fa_philox.cuh has the keep rule): the weights P V applies are the
+// kept ones, l sums all of them, and O is scaled by 1 / (1 - p).
+template <int D, bool CAUSAL, bool SPLIT, bool MASK, bool DROP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, void *__restrict__ Out,
                float *__restrict__ LSE, int Hq, int Hkv, int N, int BH, int n_items, int S,
-               float scale_log2, const MaskArgs mk, unsigned *status) {
-    static_assert(!(SPLIT && MASK), "the split-KV forward takes no general mask");
+               float scale_log2, const MaskArgs mk, const DropoutArgs dr, unsigned *status) {
+    static_assert(int(SPLIT) + int(MASK) + int(DROP) <= 1, "one variant at a time");
     constexpr bool SKIP_EMPTY = SPLIT || MASK;      // items may have no key block at all
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -534,13 +537,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if ((MASK ? jj : j) > 0) rescale_o_row<D>(tO, alpha);
                 }
                 const float m_sub = (m == -INFINITY) ? 0.f : m;
+                uint32_t p[64];
+                if constexpr (DROP) {
+                    // p = 2^(s c - m) for four keys at a time, with the keep words of those four
+                    // keys from one Philox call; l sums every weight, lc the rounding residuals
+                    // of the kept ones (the weights P V applies)
+                    const uint32_t m0 = static_cast<uint32_t>(kbase) >> 2;
+                    float lsum = 0.f, lres = 0.f;
+#pragma unroll
+                    for (int c4 = 0; c4 < 32; ++c4) {
+                        const uint4 w = dropout_words(dr, m0 + c4, static_cast<uint32_t>(rq),
+                                                      static_cast<uint32_t>(it.bh));
+                        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+                        float pk[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float pv = ex2_approx(fmaf(s[4 * c4 + q], scale_log2, -m_sub));
+                            lsum += pv;
+                            pk[q] = words[q] < dr.thresh ? pv : 0.f;
+                            lres += __bfloat162float(__float2bfloat16_rn(pk[q])) - pk[q];
+                        }
+                        p[2 * c4] = pack_bf16x2(pk[0], pk[1]);
+                        p[2 * c4 + 1] = pack_bf16x2(pk[2], pk[3]);
+                    }
+                    l += lsum;
+                    lc += lres;
+                } else {
                 // p = 2^(s c - m) on pairs: one packed FMA, two ex2, packed sums in 4 chains
                 const uint64_t c2 = f2_pack(scale_log2, scale_log2);
                 const uint64_t nm2 = f2_pack(-m_sub, -m_sub);
                 uint64_t acc[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) acc[k] = 0ull;
-                uint32_t p[64];
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const float2 x = f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), c2, nm2));
@@ -556,6 +584,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const float ptop = ex2_approx(fmaf(mx, scale_log2, -m_sub));
                     lc += __bfloat162float(__float2bfloat16_rn(ptop)) - ptop;
                 }
+                }
                 tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
                 tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
                 tmem_wait_st();
@@ -570,7 +599,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             // General mask: rows past the valid length, or left with no allowed key, give 0 / -inf.
             const bool dead = MASK && (rq >= it.lq || !(l > 0.f));
-            const float inv_l = dead ? 0.f : 1.f / (l + lc);
+            const float inv_l = dead ? 0.f : (DROP ? dr.rscale : 1.f) / (l + lc);
             const size_t orow_idx = ((SPLIT ? static_cast<size_t>(it.split) * BH : 0) + it.bh) *
                                         static_cast<size_t>(N) + rq;
 #pragma unroll
@@ -616,11 +645,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int D, bool CAUSAL, bool SPLIT, bool MASK>
+template <int D, bool CAUSAL, bool SPLIT, bool MASK, bool DROP>
 cudaError_t launch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                    const CUtensorMap &tmV, void *Out, float *LSE, int S, const MaskArgs &mk,
-                   unsigned *status, cudaStream_t stream) {
-    auto kern = fwd_kernel<D, CAUSAL, SPLIT, MASK>;
+                   const DropoutArgs &dr, unsigned *status, cudaStream_t stream) {
+    auto kern = fwd_kernel<D, CAUSAL, SPLIT, MASK, DROP>;
     const int smem = Layout<D>::BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -637,20 +666,22 @@ cudaError_t launch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &
     const int grid = static_cast<int>(std::min<long long>(n_items, num_sms()));
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     kern<<<grid, NUM_THREADS, smem, stream>>>(tmQ, tmK, tmV, Out, LSE, p.Hq, p.Hkv, p.N, BH,
-                                              static_cast<int>(n_items), S, scale_log2, mk, status);
+                                              static_cast<int>(n_items), S, scale_log2, mk, dr, status);
     return cudaGetLastError();
 }
 
-template <bool SPLIT, bool MASK>
+template <bool SPLIT, bool MASK, bool DROP>
 cudaError_t dispatch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                      const CUtensorMap &tmV, void *Out, float *LSE, int S, const MaskArgs &mk,
-                     unsigned *status, cudaStream_t stream) {
+                     const DropoutArgs &dr, unsigned *status, cudaStream_t stream) {
     if (p.d == 128)
-        return p.causal ? launch<128, true, SPLIT, MASK>(p, tmQ, tmK, tmV, Out, LSE, S, mk, status, stream)
-                        : launch<128, false, SPLIT, MASK>(p, tmQ, tmK, tmV, Out, LSE, S, mk, status, stream);
+        return p.causal
+                   ? launch<128, true, SPLIT, MASK, DROP>(p, tmQ, tmK, tmV, Out, LSE, S, mk, dr, status, stream)
+                   : launch<128, false, SPLIT, MASK, DROP>(p, tmQ, tmK, tmV, Out, LSE, S, mk, dr, status, stream);
     if (p.d == 64)
-        return p.causal ? launch<64, true, SPLIT, MASK>(p, tmQ, tmK, tmV, Out, LSE, S, mk, status, stream)
-                        : launch<64, false, SPLIT, MASK>(p, tmQ, tmK, tmV, Out, LSE, S, mk, status, stream);
+        return p.causal
+                   ? launch<64, true, SPLIT, MASK, DROP>(p, tmQ, tmK, tmV, Out, LSE, S, mk, dr, status, stream)
+                   : launch<64, false, SPLIT, MASK, DROP>(p, tmQ, tmK, tmV, Out, LSE, S, mk, dr, status, stream);
     return cudaErrorInvalidValue;
 }
 
@@ -659,20 +690,29 @@ cudaError_t dispatch(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap
 cudaError_t launch_fwd_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                             const CUtensorMap &tmV, void *O, float *LSE, unsigned *status,
                             cudaStream_t stream) {
-    return fwd::dispatch<false, false>(p, tmQ, tmK, tmV, O, LSE, 1, MaskArgs{}, status, stream);
+    return fwd::dispatch<false, false, false>(p, tmQ, tmK, tmV, O, LSE, 1, MaskArgs{},
+                                              DropoutArgs{}, status, stream);
 }
 
 cudaError_t launch_fwd_masked_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                                    const CUtensorMap &tmV, void *O, float *LSE, const MaskArgs &mk,
                                    unsigned *status, cudaStream_t stream) {
-    return fwd::dispatch<false, true>(p, tmQ, tmK, tmV, O, LSE, 1, mk, status, stream);
+    return fwd::dispatch<false, true, false>(p, tmQ, tmK, tmV, O, LSE, 1, mk, DropoutArgs{},
+                                             status, stream);
 }
 
 cudaError_t launch_fwd_split_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                                   const CUtensorMap &tmV, float *O_parts, float *LSE_parts,
                                   int num_splits, unsigned *status, cudaStream_t stream) {
-    return fwd::dispatch<true, false>(p, tmQ, tmK, tmV, O_parts, LSE_parts, num_splits, MaskArgs{},
-                                      status, stream);
+    return fwd::dispatch<true, false, false>(p, tmQ, tmK, tmV, O_parts, LSE_parts, num_splits,
+                                             MaskArgs{}, DropoutArgs{}, status, stream);
+}
+
+cudaError_t launch_fwd_dropout_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                                    const CUtensorMap &tmV, void *O, float *LSE,
+                                    const DropoutArgs &dr, unsigned *status, cudaStream_t stream) {
+    return fwd::dispatch<false, false, true>(p, tmQ, tmK, tmV, O, LSE, 1, MaskArgs{}, dr, status,
+                                             stream);
 }
 
 }  // namespace fa

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fa_philox.cuh"
 #include "flashattn.h"
 
 namespace fa {
@@ -37,6 +38,15 @@ cudaError_t launch_fwd_masked_bf16(const Problem &p, const CUtensorMap &tmQ, con
                                    const CUtensorMap &tmV, void *O, float *LSE, const MaskArgs &mk,
                                    unsigned *status, cudaStream_t stream);
 
+// K1 with dropout on P (keep rule in fa_philox.cuh).
+cudaError_t launch_fwd_dropout_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                                    const CUtensorMap &tmV, void *O, float *LSE,
+                                    const DropoutArgs &dr, unsigned *status, cudaStream_t stream);
+
+// Keep decisions Z [BH, N, N] bytes (1 = keep).
+cudaError_t launch_dropout_mask(const DropoutArgs &dr, long long BH, int N, unsigned char *Z,
+                                cudaStream_t stream);
+
 // K1 split-KV variant: num_splits contiguous ranges of key blocks, each giving an fp32 partial
 // O_parts [S, B*Hq, N, d] and LSE_parts [S, B*Hq, N] (-inf for rows with no key in the range).
 cudaError_t launch_fwd_split_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
@@ -68,6 +78,14 @@ cudaError_t launch_bwd_main_masked_bf16(const Problem &p, const CUtensorMap &tmQ
                                         const CUtensorMap &tmdV, const float *LSE, const float *D,
                                         float *dQacc, const MaskArgs &mk, unsigned *status,
                                         cudaStream_t stream);
+
+// K3 with dropout on P.
+cudaError_t launch_bwd_main_dropout_bf16(const Problem &p, const CUtensorMap &tmQ,
+                                         const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                         const CUtensorMap &tmdO, const CUtensorMap &tmdK,
+                                         const CUtensorMap &tmdV, const float *LSE, const float *D,
+                                         float *dQacc, const DropoutArgs &dr, unsigned *status,
+                                         cudaStream_t stream);
 
 // K4: dQ = bf16(dQacc).
 cudaError_t launch_bwd_dq_convert_bf16(const Problem &p, const float *dQacc, void *dQ,

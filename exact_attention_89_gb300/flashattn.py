@@ -7,7 +7,7 @@ fallback: if ``libflashattn.so`` is missing or the GPU is not sm_103, calls fail
 Low-level functions (same names and argument order as ``include/flashattn.h``):
     fa_fwd, fa_bwd, fa_bwd_workspace_bytes, fa_fwd_fp32, fa_bwd_fp32,
     fa_get_device_status, fa_status_string, fa_bwd_noalloc, fa_fwd_split, fa_merge,
-    fa_fwd_masked, fa_bwd_masked
+    fa_fwd_masked, fa_bwd_masked, fa_fwd_dropout, fa_bwd_dropout, fa_dropout_mask
 Convenience wrappers that allocate outputs with torch:
     attention_forward, attention_backward, attention_forward_split
 """
@@ -34,7 +34,8 @@ FA_ERR_DEVICE_BOUNDS = 7
 # Every symbol include/flashattn.h declares.
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_fp32", "fa_bwd_fp32",
             "fa_get_device_status", "fa_status_string", "fa_bwd_noalloc", "fa_fwd_split",
-            "fa_merge", "fa_fwd_masked", "fa_bwd_masked")
+            "fa_merge", "fa_fwd_masked", "fa_bwd_masked", "fa_fwd_dropout", "fa_bwd_dropout",
+            "fa_dropout_mask")
 
 # Side of the square tiles of a block mask (FA_MASK_BLOCK).
 MASK_BLOCK = 128
@@ -90,6 +91,13 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_masked.restype = i
             L.fa_bwd_masked.argtypes = [vp] * 9 + dims + [vp, vp, vp, i, vp, sz, vp]
             L.fa_bwd_masked.restype = i
+            u64, u32 = ctypes.c_ulonglong, ctypes.c_uint
+            L.fa_fwd_dropout.argtypes = [vp] * 5 + dims + [f, u64, u32, vp]
+            L.fa_fwd_dropout.restype = i
+            L.fa_bwd_dropout.argtypes = [vp] * 9 + dims + [f, u64, u32, vp, sz, vp]
+            L.fa_bwd_dropout.restype = i
+            L.fa_dropout_mask.argtypes = [i, i, f, u64, u32, vp, vp]
+            L.fa_dropout_mask.restype = i
             _lib = L
     return _lib
 
@@ -204,6 +212,37 @@ def fa_bwd_masked(Q, K, V, O, dO, LSE, dQ, dK, dV, causal: bool, scale: float, w
     return _check(st, "fa_bwd_masked", check)
 
 
+def fa_fwd_dropout(Q, K, V, O, LSE, causal: bool, scale: float, p_drop: float, seed: int,
+                   offset: int = 0, stream=None, check: bool = True) -> int:
+    """fa_fwd with dropout on P (keep decisions from Philox4x32-10 at (seed, offset))."""
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    st = lib().fa_fwd_dropout(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d,
+                              int(bool(causal)), float(scale), float(p_drop), int(seed),
+                              int(offset), _stream(stream))
+    return _check(st, "fa_fwd_dropout", check)
+
+
+def fa_bwd_dropout(Q, K, V, O, dO, LSE, dQ, dK, dV, causal: bool, scale: float, p_drop: float,
+                   seed: int, offset: int, workspace, stream=None, check: bool = True) -> int:
+    """Backward of fa_fwd_dropout with the same (p_drop, seed, offset)."""
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().fa_bwd_dropout(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ),
+                              _ptr(dK), _ptr(dV), B, Hq, Hkv, N, d, int(bool(causal)),
+                              float(scale), float(p_drop), int(seed), int(offset),
+                              _ptr(workspace), wbytes, _stream(stream))
+    return _check(st, "fa_bwd_dropout", check)
+
+
+def fa_dropout_mask(Z, p_drop: float, seed: int, offset: int = 0, stream=None,
+                    check: bool = True) -> int:
+    """Z: uint8 device tensor [BH, N, N] <- the keep decisions (1 = keep)."""
+    BH, N = Z.shape[0], Z.shape[-1]
+    st = lib().fa_dropout_mask(int(BH), int(N), float(p_drop), int(seed), int(offset), _ptr(Z),
+                               _stream(stream))
+    return _check(st, "fa_dropout_mask", check)
+
+
 def fa_fwd_fp32(Q, K, V, O, LSE, causal: bool, scale: float, stream=None, check: bool = True):
     B, Hq, Hkv, N, d = _dims(Q, K)
     st = lib().fa_fwd_fp32(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d,
@@ -281,6 +320,34 @@ def attention_backward_masked(Q, K, V, O, dO, LSE, causal: bool, scale: float | 
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     fa_bwd_masked(Q, K, V, O, dO, LSE, dQ, dK, dV, causal, scale, workspace, q_len, k_len,
                   block_mask, stream)
+    return dQ, dK, dV
+
+
+def attention_forward_dropout(Q, K, V, causal: bool, scale: float | None, p_drop: float,
+                              seed: int, offset: int = 0, stream=None):
+    """Allocates O and LSE and runs fa_fwd_dropout."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(Q.shape[-1])
+    B, Hq, N, d = Q.shape
+    O = torch.empty_like(Q)
+    LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=Q.device)
+    fa_fwd_dropout(Q, K, V, O, LSE, causal, scale, p_drop, seed, offset, stream)
+    return O, LSE
+
+
+def attention_backward_dropout(Q, K, V, O, dO, LSE, causal: bool, scale: float | None,
+                               p_drop: float, seed: int, offset: int = 0, workspace=None,
+                               stream=None):
+    """Allocates dQ, dK, dV (and the workspace unless given) and runs fa_bwd_dropout."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(Q.shape[-1])
+    B, Hq, N, d = Q.shape
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_bytes(B, Hq, N, d), dtype=torch.uint8,
+                                device=Q.device)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    fa_bwd_dropout(Q, K, V, O, dO, LSE, dQ, dK, dV, causal, scale, p_drop, seed, offset,
+                   workspace, stream)
     return dQ, dK, dV
 
 

@@ -28,6 +28,7 @@ class Workload:
     q_mult: float = 1.0
     num_splits: int = 1          # key ranges of the split-KV forward (1: the one-pass forward)
     mask: str = ""               # general-mask recipe (see workload_mask), "" for none
+    dropout: float = 0.0         # dropout probability on P (keep decisions seeded by `seed`)
 
     @property
     def scale(self) -> float:
@@ -43,7 +44,8 @@ class Workload:
         return 2.5 * self.flops_fwd()
 
 
-# The five workloads of the method's evaluation plan, and one for the split-KV forward.
+# The five workloads of the method's evaluation plan, then workloads for the split-KV forward, the
+# general masks and dropout.
 WORKLOADS = {
     "tiny_fp32": Workload("tiny_fp32", 1, 1, 1, 256, 64, False, 0, torch.float32, True),
     "fwd_d64": Workload("fwd_d64", 4, 16, 16, 1024, 64, False, 1, torch.bfloat16, False),
@@ -61,6 +63,9 @@ WORKLOADS = {
     # Block-sparse causal pattern (general mask: tile mask): a local window plus a first tile.
     "local_n16384": Workload("local_n16384", 1, 16, 16, 16384, 128, True, 7, torch.bfloat16, True,
                              mask="local_sink"),
+    # The bench workload's shape with dropout p = 0.1 on P.
+    "dropout_n4096": Workload("dropout_n4096", 2, 32, 32, 4096, 128, True, 8, torch.bfloat16, True,
+                              dropout=0.1),
 }
 
 MASK_BLOCK = 128        # side of the tiles a block mask covers

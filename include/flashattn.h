@@ -105,6 +105,45 @@ fa_status fa_bwd_masked(const void *Q, const void *K, const void *V, const void 
                         int mask_heads, void *workspace, size_t workspace_bytes,
                         cudaStream_t stream);
 
+/*
+ * Forward with dropout on the attention weights.  The FlashAttention DAC'24 reading note
+ * (paper.adslab.icu, "other operators") lists dropout among the operations applied per block;
+ * here it is inverted dropout on the normalised P: O = (P (.) Z / (1 - p)) V, LSE of the
+ * undropped P.  Z (1 = keep) is a pure function of (seed, offset, head, query, key):
+ *   element (i, j) of head b*Hq + hq is kept iff word (j mod 4) of Philox4x32-10 (Salmon et al.,
+ *   "Parallel random numbers: as easy as 1, 2, 3", SC'11) with counter (j/4, i, b*Hq + hq,
+ *   offset) and key (seed mod 2^32, seed / 2^32) is below floor((1 - p) 2^32).
+ * The backward recomputes the same Z from the same (seed, offset); nothing is stored.
+ *   Arguments as fa_fwd, plus 0 <= p_drop < 1 (0: exactly fa_fwd), seed, offset (give each
+ *   call its own offset, or seed, to draw a fresh mask).  FA_ERR_INVALID_ARG for p_drop outside
+ *   [0, 1) or NaN.
+ */
+fa_status fa_fwd_dropout(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                         int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                         float p_drop, unsigned long long seed, unsigned offset,
+                         cudaStream_t stream);
+
+/*
+ * Backward of fa_fwd_dropout (same p_drop, seed, offset; O and LSE from it):
+ * dV = (P (.) Z / (1 - p))^T dO, dS = P (.) (Z / (1 - p) (.) dO V^T - D) with D = rowsum(dO (.) O),
+ * dQ = scale dS K, dK = scale dS^T Q.  Arguments and errors as fa_bwd plus those of
+ * fa_fwd_dropout.
+ */
+fa_status fa_bwd_dropout(const void *Q, const void *K, const void *V, const void *O,
+                         const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                         int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                         float p_drop, unsigned long long seed, unsigned offset,
+                         void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * The keep decisions Z of fa_fwd_dropout written out: Z [BH, N, N] device bytes (1 = keep) for
+ * heads bh = 0 .. BH-1, computed by the same device code the kernels use.  For checking and
+ * debugging; p_drop = 0 writes all ones.  Errors: FA_ERR_INVALID_ARG (sizes, p_drop),
+ * FA_ERR_MISALIGNED (Z NULL), FA_ERR_CUDA.
+ */
+fa_status fa_dropout_mask(int BH, int N, float p_drop, unsigned long long seed, unsigned offset,
+                          unsigned char *Z, cudaStream_t stream);
+
 /* Largest number of key ranges fa_fwd_split and fa_merge accept. */
 #define FA_MAX_SPLITS 256
 

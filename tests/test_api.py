@@ -173,6 +173,22 @@ def test_masked_backward_rejects_invalid_arguments(built_lib):
     assert masked(wbytes=16) == E.FA_ERR_WORKSPACE
 
 
+def test_dropout_entry_points_reject_invalid_arguments(built_lib):
+    L = built_lib.lib()
+    E = built_lib
+    for pd in (-0.1, 1.0, 1.5, math.nan):
+        assert L.fa_fwd_dropout(A, A, A, A, A, 1, 2, 1, 64, 128, 1, 0.1, pd, 1, 0, None) == E.FA_ERR_INVALID_ARG
+        assert L.fa_bwd_dropout(*([A] * 9), 1, 2, 1, 64, 128, 1, 0.1, pd, 1, 0, A,
+                                L.fa_bwd_workspace_bytes(1, 2, 64, 128), None) == E.FA_ERR_INVALID_ARG
+        assert L.fa_dropout_mask(2, 64, pd, 1, 0, A, None) == E.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_dropout(A, A, A, A, A, 0, 2, 1, 64, 128, 1, 0.1, 0.1, 1, 0, None) == E.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_dropout(A, A, A, A, A, 1, 2, 1, 64, 96, 1, 0.1, 0.1, 1, 0, None) == E.FA_ERR_UNSUPPORTED
+    assert L.fa_fwd_dropout(MIS, A, A, A, A, 1, 2, 1, 64, 128, 1, 0.1, 0.1, 1, 0, None) == E.FA_ERR_MISALIGNED
+    assert L.fa_bwd_dropout(*([A] * 9), 1, 2, 1, 64, 128, 1, 0.1, 0.1, 1, 0, A, 16, None) == E.FA_ERR_WORKSPACE
+    assert L.fa_dropout_mask(0, 64, 0.1, 1, 0, A, None) == E.FA_ERR_INVALID_ARG
+    assert L.fa_dropout_mask(2, 64, 0.1, 1, 0, None, None) == E.FA_ERR_MISALIGNED
+
+
 def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     """The binding never falls back: a missing library is an error, not a CPU path."""
     from exact_attention_89_gb300 import flashattn
