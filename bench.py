@@ -416,6 +416,9 @@ def main():
     if split:
         Op = torch.empty(S, B, Hq, N, d, dtype=torch.float32, device=dev)
         Lp = torch.empty(S, B, Hq, N, dtype=torch.float32, device=dev)
+    if w.kv_outer:
+        kws = torch.empty(fa.fa_fwd_kvouter_workspace_bytes(B, Hq, N, d), dtype=torch.uint8,
+                          device=dev)
     stream = torch.cuda.current_stream()
 
     def fwd_first():
@@ -426,6 +429,8 @@ def main():
             fa.fa_fwd_masked(q, k, v, O, LSE, w.causal, w.scale, mq, mkk, mbm)
         elif w.dropout:
             fa.fa_fwd_dropout(q, k, v, O, LSE, w.causal, w.scale, w.dropout, w.seed, 0)
+        elif w.kv_outer:
+            fa.fa_fwd_kvouter(q, k, v, O, LSE, w.causal, w.scale, kws)
         else:
             fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
 
@@ -512,7 +517,7 @@ def main():
 
     # the one-pass forward on the same inputs, for comparison with the split path
     one_pass_ms = None
-    if split and not args.no_extras:
+    if (split or w.kv_outer) and not args.no_extras:
         for _ in range(3):
             fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
         o_s = torch.cuda.Event(enable_timing=True)
@@ -540,6 +545,8 @@ def main():
             res = fa.attention_forward_masked(qd, kd, vd, w.causal, w.scale, mq, mkk, mbm)
         elif w.dropout:
             res = fa.attention_forward_dropout(qd, kd, vd, w.causal, w.scale, w.dropout, w.seed)
+        elif w.kv_outer:
+            res = fa.attention_forward_kvouter(qd, kd, vd, w.causal, w.scale, workspace=kws)
         else:
             res = fa.attention_forward(qd, kd, vd, w.causal, w.scale)
         if masked:
@@ -613,10 +620,16 @@ def main():
                             "flops_per_launch": flops_fwd},
                     "bwd_ms": second_ms, "sources": bwd_key}
     else:
-        roofline = {"bound": "tensor", "kernel": "fa_fwd", "achieved": fwd_achieved,
+        roofline = {"bound": "tensor", "kernel": "fa_fwd_kvouter" if w.kv_outer else "fa_fwd",
+                    "achieved": fwd_achieved,
                     "peak": peak, "unit": "TFLOP/s", "frac": fwd_achieved / peak,
                     "traffic": NCU_TRAFFIC.get(fwd_key), "peak_source": peak_source,
-                    "flops_per_launch": w.flops_fwd(), "ms": first_ms, "sources": fwd_key}
+                    "flops_per_launch": w.flops_fwd(), "ms": first_ms,
+                    "one_pass_fwd_ms": one_pass_ms,
+                    "sources": (kernel_sources_hash("fa_fwd_kvouter_sm103a.cu") + ":" + w.name
+                                if w.kv_outer else fwd_key)}
+        if w.kv_outer:
+            roofline["traffic"] = NCU_TRAFFIC.get(roofline["sources"])
     cpu = None
     if rank == 0 and ws == 1 and args.cpu_budget > 0 and not args.no_extras:
         r = cpu_oracle_sample(w, args.cpu_budget, w.B * w.Hq)
@@ -629,7 +642,8 @@ def main():
             l2 = ("inputs larger than L2 (Q,K,V,dO,O = 5 x %.0f MB), no flush"
                   % (q.numel() * 2 / 1e6))
         else:
-            what = "fwd (split-KV x%d + merge)" % S if split else "fwd"
+            what = ("fwd (split-KV x%d + merge)" % S if split else
+                    "fwd, key/value-outer order" if w.kv_outer else "fwd")
             l2 = ("Q,K,V,O = 4 x %.0f MB%s; no flush" % (
                 q.numel() * 2 / 1e6,
                 " + fp32 partials %.0f MB" % (Op.numel() * 4 / 1e6) if split else ""))
@@ -642,8 +656,9 @@ def main():
                 "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
                            "causal": w.causal, "seed": w.seed, "scale": w.scale,
                            "num_splits": S, "mask": w.mask or None,
-                           "flops": "4 d per allowed pair (x3.5 fwd+bwd)" if masked else
-                                    "4 B Hq N^2 d (/2 causal, x3.5 fwd+bwd)",
+                           "flops": ("4 d per allowed pair" if masked else
+                                     "4 B Hq N^2 d (/2 causal)") +
+                                    (" (x3.5 fwd+bwd)" if w.backward else " (forward)"),
                            "l2": l2, "parallelism": "replicas x%d" % ws},
                 "fwd_tflops": fwd_achieved,
                 "fwd_frac_of_peak": fwd_achieved / peak,

@@ -338,6 +338,35 @@ fa_status fa_bwd_masked(const void *Q, const void *K, const void *V, const void 
     return fa::from_cuda(e);
 }
 
+size_t fa_fwd_kvouter_workspace_bytes(int B, int Hq, int N, int d) {
+    if (B < 1 || Hq < 1 || N < 1 || d < 1) return 0;
+    return fa::kvouter_workspace_bytes(static_cast<long long>(B) * Hq, N, d);
+}
+
+fa_status fa_fwd_kvouter(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                         int Hq, int Hkv, int N, int d, int causal, float scale, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+    fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (!fa::aligned16(Q) || !fa::aligned16(K) || !fa::aligned16(V) || !fa::aligned16(O) ||
+        !fa::aligned16(LSE))
+        return FA_ERR_MISALIGNED;
+    if (!fa::aligned16(workspace) || workspace_bytes < fa_fwd_kvouter_workspace_bytes(B, Hq, N, d))
+        return FA_ERR_WORKSPACE;
+    fa::DeviceInfo *di = nullptr;
+    if ((st = fa::current_device(&di, true)) != FA_OK) return st;
+    const Problem p{B, Hq, Hkv, N, d, causal ? 1 : 0, scale};
+    CUtensorMap tq, tk, tv;
+    if (!fa::encode_bf16(&tq, Q, d, N, 1LL * B * Hq, 128) ||
+        !fa::encode_bf16(&tk, K, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tv, V, d, N, 1LL * B * Hkv, 128))
+        return FA_ERR_CUDA;
+    return fa::from_cuda(fa::launch_fwd_kvouter_bf16(p, tq, tk, tv, O, LSE,
+                                                     static_cast<float *>(workspace), di->status,
+                                                     stream));
+}
+
 fa_status fa_fwd_split(const void *Q, const void *K, const void *V, float *O_parts,
                        float *LSE_parts, int B, int Hq, int Hkv, int N, int d, int causal,
                        float scale, int num_splits, cudaStream_t stream) {

@@ -57,6 +57,13 @@ cudaError_t launch_fwd_split_bf16(const Problem &p, const CUtensorMap &tmQ, cons
 cudaError_t launch_merge(const float *O_parts, const float *LSE_parts, int S, long long rows, int d,
                          void *O, bool out_bf16, float *LSE, cudaStream_t stream);
 
+// K8: the forward in the key/value-outer order (IO ablation); d = 128.  Workspace: fp32 running
+// O [B*Hq, N, d] then m, l, lc [3][B*Hq, N].
+size_t kvouter_workspace_bytes(long long BH, int N, int d);
+cudaError_t launch_fwd_kvouter_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                                    const CUtensorMap &tmV, void *O, float *LSE, float *workspace,
+                                    unsigned *status, cudaStream_t stream);
+
 // K2: D = rowsum(dO * O) in fp32 and zeroing of the fp32 dQ accumulator.
 cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const void *dO, float *D,
                                        float *dQacc, cudaStream_t stream);

@@ -7,7 +7,8 @@ fallback: if ``libflashattn.so`` is missing or the GPU is not sm_103, calls fail
 Low-level functions (same names and argument order as ``include/flashattn.h``):
     fa_fwd, fa_bwd, fa_bwd_workspace_bytes, fa_fwd_fp32, fa_bwd_fp32,
     fa_get_device_status, fa_status_string, fa_bwd_noalloc, fa_fwd_split, fa_merge,
-    fa_fwd_masked, fa_bwd_masked, fa_fwd_dropout, fa_bwd_dropout, fa_dropout_mask
+    fa_fwd_masked, fa_bwd_masked, fa_fwd_dropout, fa_bwd_dropout, fa_dropout_mask,
+    fa_fwd_kvouter, fa_fwd_kvouter_workspace_bytes
 Convenience wrappers that allocate outputs with torch:
     attention_forward, attention_backward, attention_forward_split
 """
@@ -35,7 +36,7 @@ FA_ERR_DEVICE_BOUNDS = 7
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_fp32", "fa_bwd_fp32",
             "fa_get_device_status", "fa_status_string", "fa_bwd_noalloc", "fa_fwd_split",
             "fa_merge", "fa_fwd_masked", "fa_bwd_masked", "fa_fwd_dropout", "fa_bwd_dropout",
-            "fa_dropout_mask")
+            "fa_dropout_mask", "fa_fwd_kvouter", "fa_fwd_kvouter_workspace_bytes")
 
 # Side of the square tiles of a block mask (FA_MASK_BLOCK).
 MASK_BLOCK = 128
@@ -98,6 +99,10 @@ def lib() -> ctypes.CDLL:
             L.fa_bwd_dropout.restype = i
             L.fa_dropout_mask.argtypes = [i, i, f, u64, u32, vp, vp]
             L.fa_dropout_mask.restype = i
+            L.fa_fwd_kvouter.argtypes = [vp] * 5 + dims + [vp, sz, vp]
+            L.fa_fwd_kvouter.restype = i
+            L.fa_fwd_kvouter_workspace_bytes.argtypes = [i, i, i, i]
+            L.fa_fwd_kvouter_workspace_bytes.restype = sz
             _lib = L
     return _lib
 
@@ -243,6 +248,21 @@ def fa_dropout_mask(Z, p_drop: float, seed: int, offset: int = 0, stream=None,
     return _check(st, "fa_dropout_mask", check)
 
 
+def fa_fwd_kvouter_workspace_bytes(B: int, Hq: int, N: int, d: int) -> int:
+    return int(lib().fa_fwd_kvouter_workspace_bytes(B, Hq, N, d))
+
+
+def fa_fwd_kvouter(Q, K, V, O, LSE, causal: bool, scale: float, workspace, stream=None,
+                   check: bool = True) -> int:
+    """The forward in the key/value-outer loop order (same O and LSE as fa_fwd)."""
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().fa_fwd_kvouter(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d,
+                              int(bool(causal)), float(scale), _ptr(workspace), wbytes,
+                              _stream(stream))
+    return _check(st, "fa_fwd_kvouter", check)
+
+
 def fa_fwd_fp32(Q, K, V, O, LSE, causal: bool, scale: float, stream=None, check: bool = True):
     B, Hq, Hkv, N, d = _dims(Q, K)
     st = lib().fa_fwd_fp32(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d,
@@ -349,6 +369,21 @@ def attention_backward_dropout(Q, K, V, O, dO, LSE, causal: bool, scale: float |
     fa_bwd_dropout(Q, K, V, O, dO, LSE, dQ, dK, dV, causal, scale, p_drop, seed, offset,
                    workspace, stream)
     return dQ, dK, dV
+
+
+def attention_forward_kvouter(Q, K, V, causal: bool, scale: float | None = None,
+                              workspace=None, stream=None):
+    """Allocates O, LSE (and the workspace unless given) and runs fa_fwd_kvouter."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(Q.shape[-1])
+    B, Hq, N, d = Q.shape
+    if workspace is None:
+        workspace = torch.empty(fa_fwd_kvouter_workspace_bytes(B, Hq, N, d), dtype=torch.uint8,
+                                device=Q.device)
+    O = torch.empty_like(Q)
+    LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=Q.device)
+    fa_fwd_kvouter(Q, K, V, O, LSE, causal, scale, workspace, stream)
+    return O, LSE
 
 
 def attention_backward(Q, K, V, O, dO, LSE, causal: bool, scale: float | None = None,

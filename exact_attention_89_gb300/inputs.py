@@ -29,6 +29,7 @@ class Workload:
     num_splits: int = 1          # key ranges of the split-KV forward (1: the one-pass forward)
     mask: str = ""               # general-mask recipe (see workload_mask), "" for none
     dropout: float = 0.0         # dropout probability on P (keep decisions seeded by `seed`)
+    kv_outer: bool = False       # forward in the key/value-outer loop order (IO ablation)
 
     @property
     def scale(self) -> float:
@@ -66,6 +67,9 @@ WORKLOADS = {
     # The bench workload's shape with dropout p = 0.1 on P.
     "dropout_n4096": Workload("dropout_n4096", 2, 32, 32, 4096, 128, True, 8, torch.bfloat16, True,
                               dropout=0.1),
+    # The bench workload's shape, forward only, in the key/value-outer loop order.
+    "kvouter_n4096": Workload("kvouter_n4096", 2, 32, 32, 4096, 128, True, 2, torch.bfloat16, False,
+                              kv_outer=True),
 }
 
 MASK_BLOCK = 128        # side of the tiles a block mask covers

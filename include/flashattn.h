@@ -144,6 +144,22 @@ fa_status fa_bwd_dropout(const void *Q, const void *K, const void *V, const void
 fa_status fa_dropout_mask(int BH, int N, float p_drop, unsigned long long seed, unsigned offset,
                           unsigned char *Z, cudaStream_t stream);
 
+/*
+ * Forward in the key/value-outer loop order, for measuring the IO cost of that order: the
+ * FlashAttention DAC'24 reading note (paper.adslab.icu, Methods) reads every K/V element from
+ * HBM once, with the outer loop over key/value blocks and the inner one over query blocks, and
+ * each query block's running O, m and l written back and re-read per key/value block.  Same
+ * result as fa_fwd (O bf16, LSE); one CTA per (batch, query head).
+ *   Arguments as fa_fwd; d must be 128.  workspace: caller-owned device scratch of at least
+ *   fa_fwd_kvouter_workspace_bytes(B, Hq, N, d) bytes, 16-byte aligned (fp32 running O and the
+ *   per-row statistics); contents on entry do not matter.  Errors as fa_fwd plus
+ *   FA_ERR_WORKSPACE.
+ */
+size_t fa_fwd_kvouter_workspace_bytes(int B, int Hq, int N, int d);
+fa_status fa_fwd_kvouter(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                         int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                         void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Largest number of key ranges fa_fwd_split and fa_merge accept. */
 #define FA_MAX_SPLITS 256
 

@@ -189,6 +189,22 @@ def test_dropout_entry_points_reject_invalid_arguments(built_lib):
     assert L.fa_dropout_mask(2, 64, 0.1, 1, 0, None, None) == E.FA_ERR_MISALIGNED
 
 
+def test_kvouter_forward_rejects_invalid_arguments(built_lib):
+    L = built_lib.lib()
+    E = built_lib
+    need = L.fa_fwd_kvouter_workspace_bytes(1, 2, 64, 128)
+    assert need == 2 * 64 * 128 * 4 + 3 * 2 * 64 * 4
+    assert L.fa_fwd_kvouter_workspace_bytes(0, 2, 64, 128) == 0
+
+    def kvo(Q=A, B=1, d=128, ws=A, wbytes=need):
+        return L.fa_fwd_kvouter(Q, A, A, A, A, B, 2, 1, 64, d, 1, 0.1, ws, wbytes, None)
+    assert kvo(B=0) == E.FA_ERR_INVALID_ARG
+    assert kvo(d=64) == E.FA_ERR_UNSUPPORTED
+    assert kvo(Q=MIS) == E.FA_ERR_MISALIGNED
+    assert kvo(wbytes=need - 1) == E.FA_ERR_WORKSPACE
+    assert kvo(ws=MIS) == E.FA_ERR_WORKSPACE
+
+
 def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     """The binding never falls back: a missing library is an error, not a CPU path."""
     from exact_attention_89_gb300 import flashattn
