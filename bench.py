@@ -419,6 +419,9 @@ def main():
     if w.kv_outer:
         kws = torch.empty(fa.fa_fwd_kvouter_workspace_bytes(B, Hq, N, d), dtype=torch.uint8,
                           device=dev)
+    if w.tensor_fp32:
+        kws = torch.empty(fa.fa_fwd_fp32_tc_workspace_bytes(B, Hq, Hkv, N, d), dtype=torch.uint8,
+                          device=dev)
     stream = torch.cuda.current_stream()
 
     def fwd_first():
@@ -431,6 +434,8 @@ def main():
             fa.fa_fwd_dropout(q, k, v, O, LSE, w.causal, w.scale, w.dropout, w.seed, 0)
         elif w.kv_outer:
             fa.fa_fwd_kvouter(q, k, v, O, LSE, w.causal, w.scale, kws)
+        elif w.tensor_fp32:
+            fa.fa_fwd_fp32_tc(q, k, v, O, LSE, w.causal, w.scale, kws)
         else:
             fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
 
@@ -517,14 +522,16 @@ def main():
 
     # the one-pass forward on the same inputs, for comparison with the split path
     one_pass_ms = None
-    if (split or w.kv_outer) and not args.no_extras:
+    if (split or w.kv_outer or w.tensor_fp32) and not args.no_extras:
+        # the comparison forward: the query-outer bf16 one, or the fp32 one on the CUDA cores
+        ref_fwd = fa.fa_fwd_fp32 if w.tensor_fp32 else fa.fa_fwd
         for _ in range(3):
-            fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
+            ref_fwd(q, k, v, O, LSE, w.causal, w.scale)
         o_s = torch.cuda.Event(enable_timing=True)
         o_e = torch.cuda.Event(enable_timing=True)
         o_s.record(stream)
         for _ in range(args.steps):
-            fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
+            ref_fwd(q, k, v, O, LSE, w.causal, w.scale)
         o_e.record(stream)
         torch.cuda.synchronize()
         one_pass_ms = o_s.elapsed_time(o_e) / args.steps
@@ -547,6 +554,8 @@ def main():
             res = fa.attention_forward_dropout(qd, kd, vd, w.causal, w.scale, w.dropout, w.seed)
         elif w.kv_outer:
             res = fa.attention_forward_kvouter(qd, kd, vd, w.causal, w.scale, workspace=kws)
+        elif w.tensor_fp32:
+            res = fa.attention_forward_fp32_tc(qd, kd, vd, w.causal, w.scale, workspace=kws)
         else:
             res = fa.attention_forward(qd, kd, vd, w.causal, w.scale)
         if masked:
@@ -620,16 +629,27 @@ def main():
                             "flops_per_launch": flops_fwd},
                     "bwd_ms": second_ms, "sources": bwd_key}
     else:
-        roofline = {"bound": "tensor", "kernel": "fa_fwd_kvouter" if w.kv_outer else "fa_fwd",
+        roofline = {"bound": "tensor",
+                    "kernel": ("fa_fwd_kvouter" if w.kv_outer else
+                               "fa_fwd_fp32_tc (split + attn)" if w.tensor_fp32 else "fa_fwd"),
                     "achieved": fwd_achieved,
                     "peak": peak, "unit": "TFLOP/s", "frac": fwd_achieved / peak,
                     "traffic": NCU_TRAFFIC.get(fwd_key), "peak_source": peak_source,
                     "flops_per_launch": w.flops_fwd(), "ms": first_ms,
                     "one_pass_fwd_ms": one_pass_ms,
                     "sources": (kernel_sources_hash("fa_fwd_kvouter_sm103a.cu") + ":" + w.name
-                                if w.kv_outer else fwd_key)}
-        if w.kv_outer:
+                                if w.kv_outer else
+                                kernel_sources_hash("fa_fwd_tf32x3_sm103a.cu") + ":" + w.name
+                                if w.tensor_fp32 else fwd_key)}
+        if w.kv_outer or w.tensor_fp32:
             roofline["traffic"] = NCU_TRAFFIC.get(roofline["sources"])
+        if w.tensor_fp32:
+            # three TF32 products per product: the TF32 dense peak (bf16 / 2 nominal) x 1/3
+            roofline.update({"peak": peak / 2, "peak_source": peak_source + " x 1/2 (TF32 rate)",
+                             "frac": fwd_achieved * 3 / (peak / 2),
+                             "note": "achieved counts the method's FLOPs once; frac counts the "
+                                     "three TF32 products against the TF32 peak",
+                             "simt_fp32_fwd_ms": one_pass_ms})
     cpu = None
     if rank == 0 and ws == 1 and args.cpu_budget > 0 and not args.no_extras:
         r = cpu_oracle_sample(w, args.cpu_budget, w.B * w.Hq)
@@ -643,16 +663,19 @@ def main():
                   % (q.numel() * 2 / 1e6))
         else:
             what = ("fwd (split-KV x%d + merge)" % S if split else
-                    "fwd, key/value-outer order" if w.kv_outer else "fwd")
+                    "fwd, key/value-outer order" if w.kv_outer else
+                    "fwd fp32 on tensor cores (3xTF32)" if w.tensor_fp32 else "fwd")
             l2 = ("Q,K,V,O = 4 x %.0f MB%s; no flush" % (
                 q.numel() * 2 / 1e6,
                 " + fp32 partials %.0f MB" % (Op.numel() * 4 / 1e6) if split else ""))
-        line = {"metric": "attention TFLOP/s %s, bf16 d=%d %s"
-                          % (what, d, "causal" if w.causal else "non-causal"),
+        line = {"metric": "attention TFLOP/s %s, %s d=%d %s"
+                          % (what, "fp32" if w.tensor_fp32 else "bf16", d,
+                             "causal" if w.causal else "non-causal"),
                 "value": value,
                 "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32" if w.tensor_fp32 else "bf16", "data": "synthetic",
                 "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
                            "causal": w.causal, "seed": w.seed, "scale": w.scale,
                            "num_splits": S, "mask": w.mask or None,

@@ -98,6 +98,21 @@ bool encode_bf16(CUtensorMap *m, const void *base, int d, int N, long long BH, i
 
 fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
+// 3-D fp32 view [inner, rows, planes] of a contiguous tensor, box [32, box_rows, 1], 128B swizzle.
+bool encode_f32(CUtensorMap *m, const void *base, long long inner, long long rows, long long planes,
+                int box_rows) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(planes)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 4,
+                             static_cast<cuuint64_t>(inner) * static_cast<cuuint64_t>(rows) * 4};
+    cuuint32_t box[3] = {32, static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 int num_sms() {
@@ -365,6 +380,42 @@ fa_status fa_fwd_kvouter(const void *Q, const void *K, const void *V, void *O, f
     return fa::from_cuda(fa::launch_fwd_kvouter_bf16(p, tq, tk, tv, O, LSE,
                                                      static_cast<float *>(workspace), di->status,
                                                      stream));
+}
+
+size_t fa_fwd_fp32_tc_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || d < 1) return 0;
+    return fa::tf32x3_workspace_bytes(1LL * B * Hq, 1LL * B * Hkv, N, d);
+}
+
+fa_status fa_fwd_fp32_tc(const float *Q, const float *K, const float *V, float *O, float *LSE,
+                         int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                         void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (d != 64) return FA_ERR_UNSUPPORTED;
+    if (1LL * B * Hq > 65535) return FA_ERR_UNSUPPORTED;
+    if (!fa::aligned16(Q) || !fa::aligned16(K) || !fa::aligned16(V) || !fa::aligned16(O) ||
+        !fa::aligned16(LSE))
+        return FA_ERR_MISALIGNED;
+    if (!fa::aligned16(workspace) ||
+        workspace_bytes < fa_fwd_fp32_tc_workspace_bytes(B, Hq, Hkv, N, d))
+        return FA_ERR_WORKSPACE;
+    fa::DeviceInfo *di = nullptr;
+    if ((st = fa::current_device(&di, true)) != FA_OK) return st;
+    const Problem p{B, Hq, Hkv, N, d, causal ? 1 : 0, scale};
+    const long long BH = 1LL * B * Hq, BHkv = 1LL * B * Hkv;
+    const long long Np = (N + 31) / 32 * 32;
+    float *ws = static_cast<float *>(workspace);
+    float *Qh = ws, *Ql = Qh + BH * N * d, *Kh = Ql + BH * N * d, *Kl = Kh + BHkv * N * d;
+    float *Vth = Kl + BHkv * N * d, *Vtl = Vth + BHkv * d * Np;
+    CUtensorMap maps[6];
+    if (!fa::encode_f32(&maps[0], Qh, d, N, BH, 128) || !fa::encode_f32(&maps[1], Ql, d, N, BH, 128) ||
+        !fa::encode_f32(&maps[2], Kh, d, N, BHkv, 32) || !fa::encode_f32(&maps[3], Kl, d, N, BHkv, 32) ||
+        !fa::encode_f32(&maps[4], Vth, Np, d, BHkv, 64) || !fa::encode_f32(&maps[5], Vtl, Np, d, BHkv, 64))
+        return FA_ERR_CUDA;
+    cudaError_t e = fa::launch_tf32x3_split(p, Q, K, V, ws, stream);
+    if (e == cudaSuccess) e = fa::launch_tf32x3_attn(p, maps, O, LSE, di->status, stream);
+    return fa::from_cuda(e);
 }
 
 fa_status fa_fwd_split(const void *Q, const void *K, const void *V, float *O_parts,

@@ -64,6 +64,15 @@ cudaError_t launch_fwd_kvouter_bf16(const Problem &p, const CUtensorMap &tmQ, co
                                     const CUtensorMap &tmV, void *O, float *LSE, float *workspace,
                                     unsigned *status, cudaStream_t stream);
 
+// K9: fp32 forward with three TF32 products per product (d = 64).  Workspace: Qh, Ql
+// [B*Hq, N, 64], Kh, Kl [B*Hkv, N, 64], V^T hi / lo [B*Hkv, 64, Np] fp32, Np = N rounded up to 32.
+// maps: Qh, Ql (box [32, 128, 1]), Kh, Kl (box [32, 32, 1]), Vth, Vtl (box [32, 64, 1]).
+size_t tf32x3_workspace_bytes(long long BH, long long BHkv, int N, int d);
+cudaError_t launch_tf32x3_split(const Problem &p, const float *Q, const float *K, const float *V,
+                                float *ws, cudaStream_t stream);
+cudaError_t launch_tf32x3_attn(const Problem &p, const CUtensorMap *maps, float *O, float *LSE,
+                               unsigned *status, cudaStream_t stream);
+
 // K2: D = rowsum(dO * O) in fp32 and zeroing of the fp32 dQ accumulator.
 cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const void *dO, float *D,
                                        float *dQacc, cudaStream_t stream);

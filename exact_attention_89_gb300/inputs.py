@@ -30,6 +30,7 @@ class Workload:
     mask: str = ""               # general-mask recipe (see workload_mask), "" for none
     dropout: float = 0.0         # dropout probability on P (keep decisions seeded by `seed`)
     kv_outer: bool = False       # forward in the key/value-outer loop order (IO ablation)
+    tensor_fp32: bool = False    # fp32 forward on the tensor cores (three TF32 products)
 
     @property
     def scale(self) -> float:
@@ -70,6 +71,9 @@ WORKLOADS = {
     # The bench workload's shape, forward only, in the key/value-outer loop order.
     "kvouter_n4096": Workload("kvouter_n4096", 2, 32, 32, 4096, 128, True, 2, torch.bfloat16, False,
                               kv_outer=True),
+    # fp32 at the tiny_fp32 head dim, at a size worth timing, forward on the tensor cores.
+    "fp32tc_n4096": Workload("fp32tc_n4096", 2, 16, 16, 4096, 64, True, 9, torch.float32, False,
+                             tensor_fp32=True),
 }
 
 MASK_BLOCK = 128        # side of the tiles a block mask covers

@@ -267,6 +267,21 @@ fa_status fa_bwd_fp32(const float *Q, const float *K, const float *V, const floa
                       void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * fp32 forward on the tensor cores: every product (Q K^T and P V) is formed from TF32 parts as
+ * hi(A) hi(B) + hi(A) lo(B) + lo(A) hi(B) with fp32 accumulation, hi(x) being x with its 13 low
+ * mantissa bits cleared and lo(x) = x - hi(x); the result agrees with the fp32 path to about
+ * 1e-6.  Same method, shapes and semantics as fa_fwd_fp32 (FlashAttention DAC'24 reading note,
+ * Methods); d must be 64 and B*Hq <= 65535.
+ *   workspace: caller-owned device scratch of at least fa_fwd_fp32_tc_workspace_bytes(...)
+ *   bytes, 16-byte aligned (the TF32 parts of Q, K and of V transposed); contents on entry do not
+ *   matter.  Errors as fa_fwd_fp32 plus FA_ERR_WORKSPACE.
+ */
+size_t fa_fwd_fp32_tc_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
+fa_status fa_fwd_fp32_tc(const float *Q, const float *K, const float *V, float *O, float *LSE,
+                         int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                         void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status word.
  * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_DEVICE_BOUNDS (first failure recorded since the
  * last read), or FA_ERR_CUDA if the synchronisation itself failed.
