@@ -74,6 +74,12 @@ struct Layout {
     // General mask: the CTA's list of steps (query head, query tile) its tile mask keeps.
     static constexpr int LIST_OFF = ABORT_OFF + 16;                  // [2] step count, then entries
     static constexpr int BYTES_MASK = LIST_OFF + 4 + MAX_MASK_STEPS * 2 + 1024;
+    // Dropout: keep words of the key rows for two steps [2][BKV] (bit c: query q0 + c), written
+    // by the dQ drain warps one step ahead, and their km_full[2] / km_empty[2] barriers.
+    static constexpr int KEEP_OFF = ABORT_OFF + 16;
+    static constexpr int KM_BAR_OFF = KEEP_OFF + 2 * BKV * 8;
+    static constexpr int XCH_OFF = KM_BAR_OFF + 4 * 8;            // [BKV] quad exchange words
+    static constexpr int BYTES_DROP = XCH_OFF + BKV * 8 + 1024;
 };
 
 constexpr uint32_t T_DK = 0, T_DV = 128, T_BUF = 256;
@@ -88,8 +94,10 @@ __device__ __forceinline__ int first_q_tile(int jb) {
 // split, the steps whose tile its mask keeps (rows past the valid length and key blocks past it
 // drop out); a key block with no step at all gets dK = dV = 0.
 // DROP = true: dropout on P (fa_philox.cuh has the keep rule): dV takes P Z / (1 - p) and
-// dS = P (Z / (1 - p) dP - D); the keep words of a quad of key rows come from one Philox call
-// per query, spread over the quad's four lanes and exchanged by shuffles.
+// dS = P (Z / (1 - p) dP - D).  The dQ drain warps, idle for most of a step, generate the keep
+// words one step ahead into shared memory: one Philox call gives the decisions of the four keys
+// of a quad at one query, so each lane of a quad calls it for a quarter of the queries and the
+// quad exchanges its four 64-bit results through shared memory (shuffles measured 4x slower).
 template <int D, int DR, bool CAUSAL, bool MASK, bool DROP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -123,6 +131,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::TMEM_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ABORT_OFF);
     float *stat = reinterpret_cast<float *>(smem + L::STAT_OFF);
+    uint64_t *keep_words = reinterpret_cast<uint64_t *>(smem + L::KEEP_OFF);
+    uint64_t *km_full = reinterpret_cast<uint64_t *>(smem + L::KM_BAR_OFF);
+    uint64_t *km_empty = km_full + 2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = Hq / Hkv;
@@ -185,6 +196,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(acc_full, 1);
         mbar_init(epi, 128);
         mbar_init(mma_done, 1);
+        if (DROP) {
+            uint64_t *kb = reinterpret_cast<uint64_t *>(smem + L::KM_BAR_OFF);
+            for (int k = 0; k < 4; ++k) mbar_init(&kb[k], 128);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -365,6 +380,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             sbuf[krow] = v;
             // executed by all four warps every step (even after a failed wait) so the counts match
             named_barrier_sync(1, 128);
+            uint64_t keep_s = ~0ull;
+            if constexpr (DROP) {
+                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&km_full[bsel], (s >> 1) & 1, abort_flag, status));
+                if (ok) {
+                    keep_s = keep_words[bsel * BKV + krow];
+                    mbar_arrive(&km_empty[bsel]);
+                }
+            }
             if (ok) {
                 tc_fence_after();
                 // P^T in place over the S^T registers, then dS^T with dP^T streamed in halves
@@ -396,25 +419,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 uint32_t pp[32], dd[32];
                 uint64_t keep = ~0ull;                  // bit c: query q0 + c keeps this key
-                if constexpr (DROP) {
-                    // one Philox call per query of the quad's 4t + (lane & 3), then a 4 x 4
-                    // transpose: round k takes from lane (lane ^ k) the word of this lane's key
-                    const int qd = lane & 3;
-                    const uint32_t mkey = static_cast<uint32_t>(key) >> 2;
-                    keep = 0ull;
-#pragma unroll 4
-                    for (int t = 0; t < BQ / 4; ++t) {
-                        const uint4 w = dropout_words(drop, mkey, static_cast<uint32_t>(q0 + 4 * t + qd),
-                                                      static_cast<uint32_t>(bhq));
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int sel = qd ^ k;
-                            const uint32_t mine = sel == 0 ? w.x : sel == 1 ? w.y : sel == 2 ? w.z : w.w;
-                            const uint32_t got = k == 0 ? mine : __shfl_xor_sync(0xffffffffu, mine, k);
-                            keep |= static_cast<uint64_t>(got < drop.thresh) << (4 * t + (qd ^ k));
-                        }
-                    }
-                }
+                if constexpr (DROP) keep = keep_s;
                 auto kept = [&](int c) -> bool { return !DROP || ((keep >> c) & 1ull); };
 #pragma unroll
                 for (int c = 0; c < BQ; c += 2) {
@@ -512,7 +517,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int wq = warp - 4;
         const int dcol = wq * 32 + lane;            // column of dQ = TMEM lane of dQ^T
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        // Dropout: keep words of step s for key row dcol of this block (the same lane <-> key
+        // row layout as the gradient warps, so a quad of lanes is a quad of keys).
+        auto make_keep = [&](int s) {
+            int g, i;
+            step_tile(s, g, i);
+            const int bhq = b * Hq + hk * G + g;
+            const int q0 = i * BQ;
+            const int qd = lane & 3;                // this lane's key within its quad
+            const uint32_t mkey = static_cast<uint32_t>(jb * BKV + dcol) >> 2;
+            // bit 4t + k of `mine`: query q0 + 4t + qd keeps key 4 mkey + k
+            uint64_t mine = 0ull;
+#pragma unroll
+            for (int t = 0; t < BQ / 4; ++t) {
+                const uint4 w = dropout_words(drop, mkey, static_cast<uint32_t>(q0 + 4 * t + qd),
+                                              static_cast<uint32_t>(bhq));
+                mine |= (static_cast<uint64_t>(w.x < drop.thresh) << (4 * t)) |
+                        (static_cast<uint64_t>(w.y < drop.thresh) << (4 * t + 1)) |
+                        (static_cast<uint64_t>(w.z < drop.thresh) << (4 * t + 2)) |
+                        (static_cast<uint64_t>(w.w < drop.thresh) << (4 * t + 3));
+            }
+            uint64_t *xch = reinterpret_cast<uint64_t *>(smem + L::XCH_OFF);
+            xch[dcol] = mine;
+            __syncwarp();
+            // from quad lane src, the bits of this lane's key (positions 4t + qd) are queries 4t + src
+            uint64_t keep = 0ull;
+#pragma unroll
+            for (int src = 0; src < 4; ++src)
+                keep |= ((xch[(dcol & ~3) + src] >> qd) & 0x1111111111111111ull) << src;
+            __syncwarp();                           // the exchange words are rewritten next call
+            keep_words[(s & 1) * BKV + dcol] = keep;
+            mbar_arrive(&km_full[s & 1]);
+        };
+        if (DROP && T > 0) make_keep(0);
         for (int s = 0; s < T; ++s) {
+            if constexpr (DROP) {
+                // the keep words of the next step, into the buffer step s-1 has released
+                if (s + 1 < T) {
+                    const int sn = s + 1;
+                    if (sn >= 2 &&
+                        !__all_sync(0xffffffffu, mbar_wait(&km_empty[sn & 1], ((sn - 2) >> 1) & 1, abort_flag, status)))
+                        break;
+                    make_keep(sn);
+                }
+            }
             int g, i;
             step_tile(s, g, i);
             const int bhq = b * Hq + hk * G + g;
@@ -632,7 +680,7 @@ cudaError_t launch_main(const Problem &p, const CUtensorMap &tmQ, const CUtensor
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (MASK && static_cast<long long>(p.Hq / p.Hkv) * ((p.N + BQ - 1) / BQ) > MAX_MASK_STEPS)
         return cudaErrorInvalidConfiguration;
-    const int smem = MASK ? Layout<128>::BYTES_MASK : Layout<128>::BYTES;
+    const int smem = MASK ? Layout<128>::BYTES_MASK : DROP ? Layout<128>::BYTES_DROP : Layout<128>::BYTES;
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                           const float *, const float *, float *, int, int, int, int, int, float, float,
