@@ -38,14 +38,19 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # matches the sources (the kernel changed since the capture) reports null.
 NCU_TRAFFIC = {
     # fa_bwd on causal_n4096: bwd_main 1.917 GB read + 0.986 GB write, bwd_preprocess 0.206 GB,
-    # bwd_dq_convert 0.160 GB (profiles/launches_causal_n4096.md)
-    "fa_bwd_sm103a.cu:10b725014a9bd498:causal_n4096": 3.27e9,
-    # split forward on splitkv_n32768: 25.4 MB read + 0.5 MB write
-    # (profiles/fwd_kernel_split_splitkv_n32768.md)
-    "fa_fwd_sm103a.cu:fbaf7783d9be90e0:splitkv_n32768": 2.59e7,
-    # fa_bwd_masked, three kernels (profiles/masked_local_n16384_varlen_n8192.md)
-    "fa_bwd_sm103a.cu:10b725014a9bd498:local_n16384": 0.994e9,
-    "fa_bwd_sm103a.cu:10b725014a9bd498:varlen_n8192": 25.0e9,
+    # bwd_dq_convert 0.160 GB
+    "fa_bwd_sm103a.cu:3ef17436d4cd1a3f:causal_n4096": 3.27e9,
+    # split forward on splitkv_n32768: 25.4 MB read + 0.2-0.5 MB write (partials stay in L2)
+    "fa_fwd_sm103a.cu:13f6438b56253de0:splitkv_n32768": 2.59e7,
+    # fa_bwd_masked, three kernels
+    "fa_bwd_sm103a.cu:3ef17436d4cd1a3f:local_n16384": 0.994e9,
+    "fa_bwd_sm103a.cu:3ef17436d4cd1a3f:varlen_n8192": 25.0e9,
+    # fa_bwd_dropout, three kernels
+    "fa_bwd_sm103a.cu:3ef17436d4cd1a3f:dropout_n4096": 3.72e9,
+    # key/value-outer forward
+    "fa_fwd_kvouter_sm103a.cu:cf980aee93773e67:kvouter_n4096": 4.14e9,
+    # fp32 tensor-core forward, split + attention kernels
+    "fa_fwd_tf32x3_sm103a.cu:b945be0e3f2d66ea:fp32tc_n4096": 0.491e9,
 }
 
 
