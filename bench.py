@@ -21,6 +21,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -93,7 +94,10 @@ def kernel_sources_hash(kernel_file: str) -> str:
     """Key prefix for NCU_TRAFFIC: the kernel's source file and the device headers it uses."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_89_gb300", "csrc")
-    for fn in (kernel_file, "fa_ptx.cuh", "fa_philox.cuh"):
+    with open(os.path.join(csrc, kernel_file)) as f:
+        own = re.findall(r'^#include "(\w+\.cuh)"', f.read(), re.M)
+    extra = [fn for fn in own if fn not in ("fa_ptx.cuh", "fa_philox.cuh")]
+    for fn in [kernel_file, "fa_ptx.cuh", "fa_philox.cuh"] + extra:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return "%s:%s" % (kernel_file, h.hexdigest()[:16])
