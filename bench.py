@@ -421,7 +421,9 @@ def main():
     LSE = torch.empty(B, Hq, N, dtype=torch.float32, device=dev)
     if w.backward:
         dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        wsp = torch.empty(fa.fa_bwd_workspace_bytes(B, Hq, N, d), dtype=torch.uint8, device=dev)
+        wbytes = (fa.fa_bwd_fp32_tc_workspace_bytes(B, Hq, Hkv, N, d) if w.tensor_fp32 else
+                  fa.fa_bwd_workspace_bytes(B, Hq, N, d))
+        wsp = torch.empty(wbytes, dtype=torch.uint8, device=dev)
     if split:
         Op = torch.empty(S, B, Hq, N, d, dtype=torch.float32, device=dev)
         Lp = torch.empty(S, B, Hq, N, dtype=torch.float32, device=dev)
@@ -457,6 +459,8 @@ def main():
         elif w.dropout:
             fa.fa_bwd_dropout(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, w.dropout,
                               w.seed, 0, wsp)
+        elif w.tensor_fp32 and w.backward:
+            fa.fa_bwd_fp32_tc(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsp)
         elif w.backward:
             fa.fa_bwd(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsp)
 
@@ -544,6 +548,18 @@ def main():
         o_e.record(stream)
         torch.cuda.synchronize()
         one_pass_ms = o_s.elapsed_time(o_e) / args.steps
+    simt_bwd_ms = None
+    if w.tensor_fp32 and w.backward and not args.no_extras:
+        # the fp32 backward on the CUDA cores, same inputs (it uses the D part of a workspace)
+        wsimt = torch.empty(fa.fa_bwd_workspace_bytes(B, Hq, N, d), dtype=torch.uint8, device=dev)
+        fa.fa_bwd_fp32(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsimt)
+        b_s = torch.cuda.Event(enable_timing=True)
+        b_e = torch.cuda.Event(enable_timing=True)
+        b_s.record(stream)
+        fa.fa_bwd_fp32(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsimt)
+        b_e.record(stream)
+        torch.cuda.synchronize()
+        simt_bwd_ms = b_s.elapsed_time(b_e)
 
     # ---------------------------------------------------------------- end to end (host buffers)
     pin = [t.pin_memory() for t in (Qh, Kh, Vh, dOh) if t is not None]
@@ -575,6 +591,9 @@ def main():
             res = res + fa.attention_backward_dropout(qd, kd, vd, res[0], dev_in[3], res[1],
                                                       w.causal, w.scale, w.dropout, w.seed,
                                                       workspace=wsp)
+        elif w.tensor_fp32 and w.backward:
+            res = res + fa.attention_backward_fp32_tc(qd, kd, vd, res[0], dev_in[3], res[1],
+                                                      w.causal, w.scale, workspace=wsp)
         elif w.backward:
             res = res + fa.attention_backward(qd, kd, vd, res[0], dev_in[3], res[1], w.causal,
                                               w.scale, workspace=wsp)
@@ -623,6 +642,25 @@ def main():
                               "bytes_per_launch": merge_bytes, "ms": second_ms,
                               "achieved": merge_gbs, "peak": hbm, "frac": merge_gbs / hbm},
                     "one_pass_fwd_ms": one_pass_ms, "sources": fwd_key}
+    elif w.backward and w.tensor_fp32:
+        # three TF32 products per product: the TF32 dense peak (bf16 / 2 nominal) x 1/3; the
+        # dq pass's recomputed S and dP (7 products instead of 5) count against the kernel
+        bwd_achieved = flops_bwd / (second_ms * 1e-3) / 1e12
+        tc_key = kernel_sources_hash("fa_bwd_tf32x3_sm103a.cu") + ":" + w.name
+        roofline = {"bound": "tensor",
+                    "kernel": "fa_bwd_fp32_tc (split + dq pass + dkv pass)",
+                    "achieved": bwd_achieved, "peak": peak / 2, "unit": "TFLOP/s",
+                    "frac": bwd_achieved * 3 / (peak / 2),
+                    "traffic": NCU_TRAFFIC.get(tc_key),
+                    "peak_source": peak_source + " x 1/2 (TF32 rate)",
+                    "note": "achieved counts the method's FLOPs once; frac counts the three TF32 "
+                            "products against the TF32 peak",
+                    "flops_per_launch": flops_bwd, "bwd_ms": second_ms,
+                    "simt_fp32_fwd_ms": one_pass_ms, "simt_fp32_bwd_ms": simt_bwd_ms,
+                    "fwd": {"kernel": "fa_fwd_fp32_tc (split + attn)", "achieved": fwd_achieved,
+                            "frac": fwd_achieved * 3 / (peak / 2), "ms": first_ms,
+                            "flops_per_launch": flops_fwd},
+                    "sources": tc_key}
     elif w.backward:
         bwd_achieved = flops_bwd / (second_ms * 1e-3) / 1e12
         bname, fname = (("fa_bwd_masked", "fa_fwd_masked") if masked else
@@ -667,15 +705,16 @@ def main():
     if rank == 0:
         if w.backward:
             what = "fwd+bwd" + (" under a general mask (%s)" % w.mask if masked else
-                                " with dropout p=%g" % w.dropout if w.dropout else "")
+                                " with dropout p=%g" % w.dropout if w.dropout else
+                                " on tensor cores (3xTF32)" if w.tensor_fp32 else "")
             l2 = ("inputs larger than L2 (Q,K,V,dO,O = 5 x %.0f MB), no flush"
-                  % (q.numel() * 2 / 1e6))
+                  % (q.numel() * q.element_size() / 1e6))
         else:
             what = ("fwd (split-KV x%d + merge)" % S if split else
                     "fwd, key/value-outer order" if w.kv_outer else
                     "fwd fp32 on tensor cores (3xTF32)" if w.tensor_fp32 else "fwd")
             l2 = ("Q,K,V,O = 4 x %.0f MB%s; no flush" % (
-                q.numel() * 2 / 1e6,
+                q.numel() * q.element_size() / 1e6,
                 " + fp32 partials %.0f MB" % (Op.numel() * 4 / 1e6) if split else ""))
         line = {"metric": "attention TFLOP/s %s, %s d=%d %s"
                           % (what, "fp32" if w.tensor_fp32 else "bf16", d,
@@ -697,7 +736,9 @@ def main():
                 "fwd_bwd_frac_of_peak": value / ws / peak if w.backward else None,
                 "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
-                "gpu_launches": args.steps * (2 if split else (1 + (3 if w.backward else 0))),
+                "gpu_launches": args.steps * (
+                    (2 if split or w.tensor_fp32 else 1) +
+                    ((4 if w.tensor_fp32 else 3) if w.backward else 0)),
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks}
         print(json.dumps(line))
     if ws > 1:

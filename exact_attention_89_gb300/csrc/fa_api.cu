@@ -418,6 +418,46 @@ fa_status fa_fwd_fp32_tc(const float *Q, const float *K, const float *V, float *
     return fa::from_cuda(e);
 }
 
+size_t fa_bwd_fp32_tc_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || d < 1) return 0;
+    return fa::tf32x3_bwd_layout(1LL * B * Hq, 1LL * B * Hkv, N, d, nullptr).bytes;
+}
+
+fa_status fa_bwd_fp32_tc(const float *Q, const float *K, const float *V, const float *O,
+                         const float *dO, const float *LSE, float *dQ, float *dK, float *dV,
+                         int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                         void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (d != 64) return FA_ERR_UNSUPPORTED;
+    if (1LL * B * Hq > 65535) return FA_ERR_UNSUPPORTED;
+    const void *ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
+    for (const void *q : ptrs)
+        if (!fa::aligned16(q)) return FA_ERR_MISALIGNED;
+    if (!fa::aligned16(workspace) ||
+        workspace_bytes < fa_bwd_fp32_tc_workspace_bytes(B, Hq, Hkv, N, d))
+        return FA_ERR_WORKSPACE;
+    fa::DeviceInfo *di = nullptr;
+    if ((st = fa::current_device(&di, true)) != FA_OK) return st;
+    const Problem p{B, Hq, Hkv, N, d, causal ? 1 : 0, scale};
+    const long long BH = 1LL * B * Hq, BHkv = 1LL * B * Hkv;
+    const fa::Tf32BwdWorkspace w = fa::tf32x3_bwd_layout(BH, BHkv, N, d, workspace);
+    CUtensorMap maps[14];
+    const bool enc =
+        fa::encode_f32(&maps[0], w.Kh, d, N, BHkv, 32) && fa::encode_f32(&maps[1], w.Kl, d, N, BHkv, 32) &&
+        fa::encode_f32(&maps[2], w.Vh, d, N, BHkv, 32) && fa::encode_f32(&maps[3], w.Vl, d, N, BHkv, 32) &&
+        fa::encode_f32(&maps[4], w.Kth, w.Np, d, BHkv, 64) && fa::encode_f32(&maps[5], w.Ktl, w.Np, d, BHkv, 64) &&
+        fa::encode_f32(&maps[6], w.Qh, d, N, BH, 32) && fa::encode_f32(&maps[7], w.Ql, d, N, BH, 32) &&
+        fa::encode_f32(&maps[8], w.dOh, d, N, BH, 32) && fa::encode_f32(&maps[9], w.dOl, d, N, BH, 32) &&
+        fa::encode_f32(&maps[10], w.dOth, w.Np, d, BH, 64) && fa::encode_f32(&maps[11], w.dOtl, w.Np, d, BH, 64) &&
+        fa::encode_f32(&maps[12], w.Qth, w.Np, d, BH, 64) && fa::encode_f32(&maps[13], w.Qtl, w.Np, d, BH, 64);
+    if (!enc) return FA_ERR_CUDA;
+    cudaError_t e = fa::launch_tf32x3_bwd_split(p, Q, K, V, dO, w, stream);
+    if (e == cudaSuccess)
+        e = fa::launch_tf32x3_bwd(p, maps, Q, K, V, O, dO, LSE, dQ, dK, dV, w.D, di->status, stream);
+    return fa::from_cuda(e);
+}
+
 fa_status fa_fwd_split(const void *Q, const void *K, const void *V, float *O_parts,
                        float *LSE_parts, int B, int Hq, int Hkv, int N, int d, int causal,
                        float scale, int num_splits, cudaStream_t stream) {

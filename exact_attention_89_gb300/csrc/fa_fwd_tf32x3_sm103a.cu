@@ -23,6 +23,7 @@
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
+#include "fa_tf32.cuh"
 
 namespace fa {
 namespace tf32x3 {
@@ -31,7 +32,6 @@ constexpr int D = 64;
 constexpr int BM = 128, BN = 32;
 constexpr int NUM_THREADS = 192;
 constexpr int WARP_TMA = 4, WARP_MMA = 5;
-constexpr uint32_t HI_MASK = 0xFFFFE000u;      // keeps sign, exponent and 10 mantissa bits
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr float LN2 = 0.693147180559945309f;
 
@@ -54,23 +54,6 @@ constexpr int ABORT_OFF = TMEM_OFF + 8;
 constexpr int SMEM_BYTES = ABORT_OFF + 8 + 1024;
 constexpr uint32_t T_S = 0, T_O = 64;
 
-// Instruction descriptor, kind::tf32: TF32 A and B (format 2), fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
-    return (1u << 4) | (2u << 7) | (2u << 10) | ((static_cast<uint32_t>(N) >> 3) << 17) |
-           ((static_cast<uint32_t>(M) >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ float hi_part(float x) { return __uint_as_float(__float_as_uint(x) & HI_MASK); }
-
 // K9a: Qh, Ql [BH, N, 64]; Kh, Kl [BHkv, N, 64]; Vth, Vtl [BHkv, 64, Np] (keys Np >= N zero).
 __global__ void __launch_bounds__(256) split_kernel(const float *__restrict__ Q, const float *__restrict__ K,
                                                     const float *__restrict__ V, float *__restrict__ ws,
@@ -80,12 +63,12 @@ __global__ void __launch_bounds__(256) split_kernel(const float *__restrict__ Q,
           *Vtl = Vth + nvt_el;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < nq_el; t += stride) {
-        const float x = Q[t], h = hi_part(x);
+        const float x = Q[t], h = tf32_hi(x);
         Qh[t] = h;
         Ql[t] = x - h;
     }
     for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < nk_el; t += stride) {
-        const float x = K[t], h = hi_part(x);
+        const float x = K[t], h = tf32_hi(x);
         Kh[t] = h;
         Kl[t] = x - h;
     }
@@ -95,7 +78,7 @@ __global__ void __launch_bounds__(256) split_kernel(const float *__restrict__ Q,
         const long long rest = t / Np;
         const int c = static_cast<int>(rest % D);
         const long long bkv = rest / D;
-        const float x = n < N ? V[(bkv * N + n) * D + c] : 0.f, h = hi_part(x);
+        const float x = n < N ? V[(bkv * N + n) * D + c] : 0.f, h = tf32_hi(x);
         Vth[t] = h;
         Vtl[t] = x - h;
     }
@@ -285,7 +268,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     pv[k] = ex2_approx(fmaf(s[4 * u + k], scale_log2, -m_sub));
                     l += pv[k];
                 }
-                h = make_float4(hi_part(pv[0]), hi_part(pv[1]), hi_part(pv[2]), hi_part(pv[3]));
+                h = make_float4(tf32_hi(pv[0]), tf32_hi(pv[1]), tf32_hi(pv[2]), tf32_hi(pv[3]));
                 lo = make_float4(pv[0] - h.x, pv[1] - h.y, pv[2] - h.z, pv[3] - h.w);
                 const int sw = (u ^ (row & 7)) << 4;          // 128-byte swizzle of the row
                 *reinterpret_cast<float4 *>(ph + sw) = h;

@@ -73,6 +73,26 @@ cudaError_t launch_tf32x3_split(const Problem &p, const float *Q, const float *K
 cudaError_t launch_tf32x3_attn(const Problem &p, const CUtensorMap *maps, float *O, float *LSE,
                                unsigned *status, cudaStream_t stream);
 
+// K10: fp32 backward with three TF32 products per product (d = 64): the split kernels write the
+// workspace below, then a dq pass (writes D and dQ) and a dkv pass (dK, dV).  Workspace, fp32:
+// Qh, Ql, dOh, dOl [B*Hq, N, 64]; Kh, Kl, Vh, Vl [B*Hkv, N, 64]; transposed Qth, Qtl, dOth, dOtl
+// [B*Hq, 64, Np]; Kth, Ktl [B*Hkv, 64, Np]; D [B*Hq, N]; Np = N rounded up to 32.
+struct Tf32BwdWorkspace {
+    float *Qh, *Ql, *dOh, *dOl, *Kh, *Kl, *Vh, *Vl, *Qth, *Qtl, *dOth, *dOtl, *Kth, *Ktl, *D;
+    long long Np;
+    size_t bytes;
+};
+// Pointers into `workspace` (null pointers when it is null) and the byte size.
+Tf32BwdWorkspace tf32x3_bwd_layout(long long BH, long long BHkv, int N, int d, void *workspace);
+cudaError_t launch_tf32x3_bwd_split(const Problem &p, const float *Q, const float *K, const float *V,
+                                    const float *dO, const Tf32BwdWorkspace &w, cudaStream_t stream);
+// maps: [0..5] Kh, Kl, Vh, Vl (box [32, 32, 1]), Kth, Ktl (box [32, 64, 1]); [6..13] Qh, Ql,
+// dOh, dOl (box [32, 32, 1]), dOth, dOtl, Qth, Qtl (box [32, 64, 1]).
+cudaError_t launch_tf32x3_bwd(const Problem &p, const CUtensorMap *maps, const float *Q, const float *K,
+                              const float *V, const float *O, const float *dO, const float *LSE,
+                              float *dQ, float *dK, float *dV, float *Dvec, unsigned *status,
+                              cudaStream_t stream);
+
 // K2: D = rowsum(dO * O) in fp32 and zeroing of the fp32 dQ accumulator.
 cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const void *dO, float *D,
                                        float *dQacc, cudaStream_t stream);

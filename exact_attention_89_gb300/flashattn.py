@@ -8,7 +8,8 @@ Low-level functions (same names and argument order as ``include/flashattn.h``):
     fa_fwd, fa_bwd, fa_bwd_workspace_bytes, fa_fwd_fp32, fa_bwd_fp32,
     fa_get_device_status, fa_status_string, fa_bwd_noalloc, fa_fwd_split, fa_merge,
     fa_fwd_masked, fa_bwd_masked, fa_fwd_dropout, fa_bwd_dropout, fa_dropout_mask,
-    fa_fwd_kvouter, fa_fwd_kvouter_workspace_bytes, fa_fwd_fp32_tc, fa_fwd_fp32_tc_workspace_bytes
+    fa_fwd_kvouter, fa_fwd_kvouter_workspace_bytes, fa_fwd_fp32_tc, fa_fwd_fp32_tc_workspace_bytes,
+    fa_bwd_fp32_tc, fa_bwd_fp32_tc_workspace_bytes
 Convenience wrappers that allocate outputs with torch:
     attention_forward, attention_backward, attention_forward_split
 """
@@ -37,7 +38,8 @@ EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_fp32", "fa_bwd
             "fa_get_device_status", "fa_status_string", "fa_bwd_noalloc", "fa_fwd_split",
             "fa_merge", "fa_fwd_masked", "fa_bwd_masked", "fa_fwd_dropout", "fa_bwd_dropout",
             "fa_dropout_mask", "fa_fwd_kvouter", "fa_fwd_kvouter_workspace_bytes",
-            "fa_fwd_fp32_tc", "fa_fwd_fp32_tc_workspace_bytes")
+            "fa_fwd_fp32_tc", "fa_fwd_fp32_tc_workspace_bytes", "fa_bwd_fp32_tc",
+            "fa_bwd_fp32_tc_workspace_bytes")
 
 # Side of the square tiles of a block mask (FA_MASK_BLOCK).
 MASK_BLOCK = 128
@@ -108,6 +110,10 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_fp32_tc.restype = i
             L.fa_fwd_fp32_tc_workspace_bytes.argtypes = [i, i, i, i, i]
             L.fa_fwd_fp32_tc_workspace_bytes.restype = sz
+            L.fa_bwd_fp32_tc.argtypes = [vp] * 9 + dims + [vp, sz, vp]
+            L.fa_bwd_fp32_tc.restype = i
+            L.fa_bwd_fp32_tc_workspace_bytes.argtypes = [i, i, i, i, i]
+            L.fa_bwd_fp32_tc_workspace_bytes.restype = sz
             _lib = L
     return _lib
 
@@ -283,6 +289,21 @@ def fa_fwd_fp32_tc(Q, K, V, O, LSE, causal: bool, scale: float, workspace, strea
     return _check(st, "fa_fwd_fp32_tc", check)
 
 
+def fa_bwd_fp32_tc_workspace_bytes(B: int, Hq: int, Hkv: int, N: int, d: int) -> int:
+    return int(lib().fa_bwd_fp32_tc_workspace_bytes(B, Hq, Hkv, N, d))
+
+
+def fa_bwd_fp32_tc(Q, K, V, O, dO, LSE, dQ, dK, dV, causal: bool, scale: float, workspace,
+                   stream=None, check: bool = True) -> int:
+    """fp32 backward on the tensor cores (three TF32 products per product); fp32 tensors."""
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().fa_bwd_fp32_tc(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ),
+                              _ptr(dK), _ptr(dV), B, Hq, Hkv, N, d, int(bool(causal)),
+                              float(scale), _ptr(workspace), wbytes, _stream(stream))
+    return _check(st, "fa_bwd_fp32_tc", check)
+
+
 def fa_fwd_fp32(Q, K, V, O, LSE, causal: bool, scale: float, stream=None, check: bool = True):
     B, Hq, Hkv, N, d = _dims(Q, K)
     st = lib().fa_fwd_fp32(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d,
@@ -419,6 +440,20 @@ def attention_forward_fp32_tc(Q, K, V, causal: bool, scale: float | None = None,
     LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=Q.device)
     fa_fwd_fp32_tc(Q, K, V, O, LSE, causal, scale, workspace, stream)
     return O, LSE
+
+
+def attention_backward_fp32_tc(Q, K, V, O, dO, LSE, causal: bool, scale: float | None = None,
+                               workspace=None, stream=None):
+    """Allocates dQ, dK, dV (and the workspace unless given) and runs fa_bwd_fp32_tc."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(Q.shape[-1])
+    B, Hq, N, d = Q.shape
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_fp32_tc_workspace_bytes(B, Hq, K.shape[1], N, d),
+                                dtype=torch.uint8, device=Q.device)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    fa_bwd_fp32_tc(Q, K, V, O, dO, LSE, dQ, dK, dV, causal, scale, workspace, stream)
+    return dQ, dK, dV
 
 
 def attention_backward(Q, K, V, O, dO, LSE, causal: bool, scale: float | None = None,

@@ -71,8 +71,9 @@ WORKLOADS = {
     # The bench workload's shape, forward only, in the key/value-outer loop order.
     "kvouter_n4096": Workload("kvouter_n4096", 2, 32, 32, 4096, 128, True, 2, torch.bfloat16, False,
                               kv_outer=True),
-    # fp32 at the tiny_fp32 head dim, at a size worth timing, forward on the tensor cores.
-    "fp32tc_n4096": Workload("fp32tc_n4096", 2, 16, 16, 4096, 64, True, 9, torch.float32, False,
+    # fp32 at the tiny_fp32 head dim, at a size worth timing, forward and backward on the tensor
+    # cores.
+    "fp32tc_n4096": Workload("fp32tc_n4096", 2, 16, 16, 4096, 64, True, 9, torch.float32, True,
                              tensor_fp32=True),
 }
 

@@ -282,6 +282,24 @@ fa_status fa_fwd_fp32_tc(const float *Q, const float *K, const float *V, float *
                          void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * fp32 backward on the tensor cores, the counterpart of fa_fwd_fp32_tc: same shapes and
+ * semantics as fa_bwd_fp32 (P recomputed from LSE, D = rowsum(dO O), dS = P (dP - D),
+ * dV = P^T dO, dK = scale dS^T Q, dQ = scale dS K; "Attention's hidden recurrence" blog,
+ * "Flash Attention backward"), every product formed from TF32 parts as in fa_fwd_fp32_tc.
+ * Two passes: one over query tiles (forms D and dQ) and one over key blocks (dK and dV, summed
+ * over the G query heads of each KV head); each gradient is written once, no atomics.
+ * d must be 64, B*Hq <= 65535; every pointer 16-byte aligned.
+ *   workspace: caller-owned device scratch of at least fa_bwd_fp32_tc_workspace_bytes(...) bytes,
+ *   16-byte aligned (TF32 parts of Q, dO, K, V, transposed copies of Q, dO, K, and D); contents
+ *   on entry do not matter.  Errors as fa_bwd_fp32 plus FA_ERR_UNSUPPORTED for d != 64.
+ */
+size_t fa_bwd_fp32_tc_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
+fa_status fa_bwd_fp32_tc(const float *Q, const float *K, const float *V, const float *O,
+                         const float *dO, const float *LSE, float *dQ, float *dK, float *dV,
+                         int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                         void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status word.
  * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_DEVICE_BOUNDS (first failure recorded since the
  * last read), or FA_ERR_CUDA if the synchronisation itself failed.

@@ -220,6 +220,27 @@ def test_fp32_tensor_core_forward_rejects_invalid_arguments(built_lib):
     assert tc(wbytes=need - 1) == E.FA_ERR_WORKSPACE
 
 
+def test_fp32_tensor_core_backward_rejects_invalid_arguments(built_lib):
+    L = built_lib.lib()
+    E = built_lib
+    need = L.fa_bwd_fp32_tc_workspace_bytes(1, 2, 1, 100, 64)
+    # hi / lo of Q, dO (2 heads) and K, V (1 head), transposed hi / lo of Q, dO and K over
+    # 128 padded columns, and D
+    assert need == 4 * (4 * 2 * 100 * 64 + 4 * 1 * 100 * 64 + 4 * 2 * 64 * 128
+                        + 2 * 1 * 64 * 128 + 2 * 100)
+    assert L.fa_bwd_fp32_tc_workspace_bytes(1, 2, 1, 0, 64) == 0
+
+    def tc(Q=A, dQ=A, d=64, ws=A, wbytes=need, Hq=2, Hkv=1):
+        return L.fa_bwd_fp32_tc(Q, A, A, A, A, A, dQ, A, A, 1, Hq, Hkv, 100, d, 1, 0.1, ws, wbytes,
+                                None)
+    assert tc(Hq=3, Hkv=2) == E.FA_ERR_INVALID_ARG
+    assert tc(d=128) == E.FA_ERR_UNSUPPORTED
+    assert tc(Q=MIS) == E.FA_ERR_MISALIGNED
+    assert tc(dQ=MIS) == E.FA_ERR_MISALIGNED
+    assert tc(wbytes=need - 1) == E.FA_ERR_WORKSPACE
+    assert tc(ws=MIS) == E.FA_ERR_WORKSPACE
+
+
 def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     """The binding never falls back: a missing library is an error, not a CPU path."""
     from exact_attention_89_gb300 import flashattn
