@@ -32,9 +32,9 @@
 // Roles (320 threads): warps 0-3 gradient warps (thread = owned row = TMEM lane), warps 4-7
 // accumulation warps (same rows: they own the register sums and write the gradients), warp 8
 // TMA producer (two-stage ring of streamed tiles), warp 9 TMEM allocator and MMA issuer.
-// TMEM (512 columns): X1 [0,32) (S or S^T), X2 [32,64) (dP or dP^T), Y1 [64,128) (dQ or dV of
-// the step), Y2 [128,192) (dK of the step), first resident operand hi [256,320) lo [320,384),
-// second hi [384,448) lo [448,512).
+// TMEM (512 columns): X1 / X2 (S or S^T, dP or dP^T) double-buffered at [0,64) and [192,256),
+// Y1 [64,128) (dQ or dV of the step), Y2 [128,192) (dK of the step), first resident operand hi
+// [256,320) lo [320,384), second hi [384,448) lo [448,512).
 #include <algorithm>
 #include <cmath>
 
@@ -56,19 +56,23 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr int XT_CHUNK = BC * 128;        // 32 rows x 32 fp32
 constexpr int XT_BYTES = 2 * XT_CHUNK;    // 32 rows x 64 fp32 (two chunks along d)
 constexpr int YT_BYTES = D * 128;         // 64 rows (d) x 32 fp32
-// stage: XA hi, XA lo, XB hi, XB lo, then YA hi, YA lo, YB hi, YB lo
-constexpr int Y_OFF = 4 * XT_BYTES;
-constexpr int STAGE_BYTES = 4 * XT_BYTES + 4 * YT_BYTES;
-constexpr int NSTAGE = 2;
+// Operands of the first products (XA hi, XA lo, XB hi, XB lo) in a 3-slot ring; those of the last
+// products (YA hi, YA lo, YB hi, YB lo) in a 2-slot ring: the first products of step s + 1 are
+// issued before the last ones of step s.
+constexpr int NXS = 3, NYS = 2;
+constexpr int XS_BYTES = 4 * XT_BYTES, YS_BYTES = 4 * YT_BYTES;
+constexpr int XS_OFF = 0, YS_OFF = NXS * XS_BYTES;
 constexpr int STG_BYTES = BR * 128;       // one staged 128 x 32 fp32 operand
-constexpr int STG_OFF = NSTAGE * STAGE_BYTES;   // P hi, P lo, dS hi, dS lo
+constexpr int STG_OFF = YS_OFF + NYS * YS_BYTES;   // P hi, P lo, dS hi, dS lo
 constexpr int BAR_OFF = STG_OFF + 4 * STG_BYTES;
-// x_full[2], x_empty[2], r_full, x_done, p_full, y_full, y_empty, mma_done
-constexpr int NBARS = 10;
+// xf[3], xe[3], yf[2], ye[2], r_full, x_done[2], p_full, y_full, y_empty, mma_done
+constexpr int NBARS = 17;
 constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
 constexpr int ABORT_OFF = TMEM_OFF + 8;
 constexpr int SMEM_BYTES = ABORT_OFF + 8 + 1024;
-constexpr uint32_t T_X1 = 0, T_X2 = 32, T_Y1 = 64, T_Y2 = 128, T_RA = 256, T_RB = 384;
+// X1 / X2 of buffer b at T_X + 192 b (+0 / +32)
+constexpr uint32_t T_X = 0, T_Y1 = 64, T_Y2 = 128, T_RA = 256, T_RB = 384;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 // Streamed operands of one pass (all 3-D [inner, rows, planes] fp32, 128-byte swizzle):
 //   dq pass : xa = K, xb = V (box 32 x 32), ya = K^T (box 32 x 64); yb unused
@@ -181,8 +185,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + BAR_OFF);
-    uint64_t *x_full = bars, *x_empty = bars + 2, *r_full = bars + 4, *x_done = bars + 5;
-    uint64_t *p_full = bars + 6, *y_full = bars + 7, *y_empty = bars + 8, *mma_done = bars + 9;
+    uint64_t *xf = bars, *xe = bars + 3, *yf = bars + 6, *ye = bars + 8, *r_full = bars + 10;
+    uint64_t *x_done = bars + 11, *p_full = bars + 13, *y_full = bars + 14, *y_empty = bars + 15;
+    uint64_t *mma_done = bars + 16;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + TMEM_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + ABORT_OFF);
 
@@ -218,12 +223,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&x_full[s], 1);
-            mbar_init(&x_empty[s], 1);
+        for (int i = 0; i < NXS; ++i) {
+            mbar_init(&xf[i], 1);
+            mbar_init(&xe[i], 1);
+        }
+        for (int i = 0; i < NYS; ++i) {
+            mbar_init(&yf[i], 1);
+            mbar_init(&ye[i], 1);
         }
         mbar_init(r_full, BR);
-        mbar_init(x_done, 1);
+        mbar_init(&x_done[0], 1);
+        mbar_init(&x_done[1], 1);
         mbar_init(p_full, BR);
         mbar_init(y_full, 1);
         mbar_init(y_empty, BR);
@@ -243,31 +253,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_TMA) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint32_t bytes = 4 * XT_BYTES + (DKV ? 4 : 2) * YT_BYTES;
-            int issued = 0;
+            const uint32_t ybytes = (DKV ? 4 : 2) * YT_BYTES;
+            int xissued = 0, yissued = 0;
             for (int s = 0; s < T; ++s) {
-                const int st = s & 1;
-                if (s >= NSTAGE && !mbar_wait(&x_empty[st], ((s - NSTAGE) >> 1) & 1, abort_flag, status)) break;
+                const int xs = s % NXS, ys = s % NYS;
+                if (s >= NXS && !mbar_wait(&xe[xs], (s / NXS - 1) & 1, abort_flag, status)) break;
                 int plane, blk;
                 step(s, plane, blk);
-                mbar_arrive_expect_tx(&x_full[st], bytes);
-                uint8_t *base = smem + st * STAGE_BYTES;
+                mbar_arrive_expect_tx(&xf[xs], XS_BYTES);
+                uint8_t *xb = smem + XS_OFF + xs * XS_BYTES;
                 for (int ch = 0; ch < D / 32; ++ch) {
-                    tma_load_3d(base + 0 * XT_BYTES + ch * XT_CHUNK, &maps.xa_h, ch * 32, blk * BC, plane, &x_full[st]);
-                    tma_load_3d(base + 1 * XT_BYTES + ch * XT_CHUNK, &maps.xa_l, ch * 32, blk * BC, plane, &x_full[st]);
-                    tma_load_3d(base + 2 * XT_BYTES + ch * XT_CHUNK, &maps.xb_h, ch * 32, blk * BC, plane, &x_full[st]);
-                    tma_load_3d(base + 3 * XT_BYTES + ch * XT_CHUNK, &maps.xb_l, ch * 32, blk * BC, plane, &x_full[st]);
+                    tma_load_3d(xb + 0 * XT_BYTES + ch * XT_CHUNK, &maps.xa_h, ch * 32, blk * BC, plane, &xf[xs]);
+                    tma_load_3d(xb + 1 * XT_BYTES + ch * XT_CHUNK, &maps.xa_l, ch * 32, blk * BC, plane, &xf[xs]);
+                    tma_load_3d(xb + 2 * XT_BYTES + ch * XT_CHUNK, &maps.xb_h, ch * 32, blk * BC, plane, &xf[xs]);
+                    tma_load_3d(xb + 3 * XT_BYTES + ch * XT_CHUNK, &maps.xb_l, ch * 32, blk * BC, plane, &xf[xs]);
                 }
-                tma_load_3d(base + Y_OFF, &maps.ya_h, blk * BC, 0, plane, &x_full[st]);
-                tma_load_3d(base + Y_OFF + YT_BYTES, &maps.ya_l, blk * BC, 0, plane, &x_full[st]);
+                xissued = s + 1;
+                if (s >= NYS && !mbar_wait(&ye[ys], (s / NYS - 1) & 1, abort_flag, status)) break;
+                mbar_arrive_expect_tx(&yf[ys], ybytes);
+                uint8_t *yb = smem + YS_OFF + ys * YS_BYTES;
+                tma_load_3d(yb, &maps.ya_h, blk * BC, 0, plane, &yf[ys]);
+                tma_load_3d(yb + YT_BYTES, &maps.ya_l, blk * BC, 0, plane, &yf[ys]);
                 if (DKV) {
-                    tma_load_3d(base + Y_OFF + 2 * YT_BYTES, &maps.yb_h, blk * BC, 0, plane, &x_full[st]);
-                    tma_load_3d(base + Y_OFF + 3 * YT_BYTES, &maps.yb_l, blk * BC, 0, plane, &x_full[st]);
+                    tma_load_3d(yb + 2 * YT_BYTES, &maps.yb_h, blk * BC, 0, plane, &yf[ys]);
+                    tma_load_3d(yb + 3 * YT_BYTES, &maps.yb_l, blk * BC, 0, plane, &yf[ys]);
                 }
-                issued = s + 1;
+                yissued = s + 1;
             }
-            if (*abort_flag)
-                for (int s = max(0, issued - NSTAGE); s < issued; ++s) mbar_drain(&x_full[s & 1], (s >> 1) & 1);
+            if (*abort_flag) {
+                // let copies still in flight land before the CTA's shared memory goes away
+                for (int s = max(0, xissued - NXS); s < xissued; ++s) mbar_drain(&xf[s % NXS], (s / NXS) & 1);
+                for (int s = max(0, yissued - NYS); s < yissued; ++s) mbar_drain(&yf[s % NYS], (s / NYS) & 1);
+            }
         }
         tc_fence_before();
         __syncthreads();
@@ -281,37 +298,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t dpl = sdesc_sw128(smem_u32(smem + STG_OFF + STG_BYTES), 16, 1024);
             const uint64_t dsh = sdesc_sw128(smem_u32(smem + STG_OFF + 2 * STG_BYTES), 16, 1024);
             const uint64_t dsl = sdesc_sw128(smem_u32(smem + STG_OFF + 3 * STG_BYTES), 16, 1024);
-            bool ok = mbar_wait(r_full, 0, abort_flag, status);
-            for (int s = 0; s < T && ok; ++s) {
-                const int st = s & 1;
-                if (!mbar_wait(&x_full[st], (s >> 1) & 1, abort_flag, status)) { ok = false; break; }
+            // X1 = RA xa^T and X2 = RB xb^T of step s into buffer s & 1, over d = 64 (8 k-steps)
+            auto issue_x = [&](int s) -> bool {
+                const int xs = s % NXS;
+                if (!mbar_wait(&xf[xs], (s / NXS) & 1, abort_flag, status)) return false;
                 tc_fence_after();
-                const uint32_t base = smem_u32(smem + st * STAGE_BYTES);
+                const uint32_t base = smem_u32(smem + XS_OFF + xs * XS_BYTES);
                 const uint64_t dxah = sdesc_sw128(base, 16, 1024);
                 const uint64_t dxal = sdesc_sw128(base + XT_BYTES, 16, 1024);
                 const uint64_t dxbh = sdesc_sw128(base + 2 * XT_BYTES, 16, 1024);
                 const uint64_t dxbl = sdesc_sw128(base + 3 * XT_BYTES, 16, 1024);
-                // X1 = RA xa^T and X2 = RB xb^T over d = 64 (8 k-steps of 8)
+                const uint32_t t1 = tmem + T_X + 192 * (s & 1), t2 = t1 + 32;
 #pragma unroll
                 for (int kk = 0; kk < D / 8; ++kk) {
                     const uint32_t off = (kk >> 2) * XT_CHUNK + (kk & 3) * 32;
                     const uint32_t ca = tmem + T_RA + kk * 8, cb = tmem + T_RB + kk * 8;
-                    mma_tf32_ts(tmem + T_X1, ca, sdesc_add(dxah, off), IDESC_X, kk > 0);
-                    mma_tf32_ts(tmem + T_X1, ca, sdesc_add(dxal, off), IDESC_X, 1u);
-                    mma_tf32_ts(tmem + T_X1, ca + 64, sdesc_add(dxah, off), IDESC_X, 1u);
-                    mma_tf32_ts(tmem + T_X2, cb, sdesc_add(dxbh, off), IDESC_X, kk > 0);
-                    mma_tf32_ts(tmem + T_X2, cb, sdesc_add(dxbl, off), IDESC_X, 1u);
-                    mma_tf32_ts(tmem + T_X2, cb + 64, sdesc_add(dxbh, off), IDESC_X, 1u);
+                    mma_tf32_ts(t1, ca, sdesc_add(dxah, off), IDESC_X, kk > 0);
+                    mma_tf32_ts(t1, ca, sdesc_add(dxal, off), IDESC_X, 1u);
+                    mma_tf32_ts(t1, ca + 64, sdesc_add(dxah, off), IDESC_X, 1u);
+                    mma_tf32_ts(t2, cb, sdesc_add(dxbh, off), IDESC_X, kk > 0);
+                    mma_tf32_ts(t2, cb, sdesc_add(dxbl, off), IDESC_X, 1u);
+                    mma_tf32_ts(t2, cb + 64, sdesc_add(dxbh, off), IDESC_X, 1u);
                 }
-                mma_commit(x_done);
+                mma_commit(&x_done[s & 1]);
+                mma_commit(&xe[xs]);
+                return true;
+            };
+            bool ok = mbar_wait(r_full, 0, abort_flag, status);
+            if (ok && T > 0) ok = issue_x(0);
+            for (int s = 0; s < T && ok; ++s) {
+                // buffer (s + 1) & 1 was read by the gradient warps before they signalled p_full
+                // of step s - 1
+                if (s + 1 < T && !issue_x(s + 1)) { ok = false; break; }
                 if (!mbar_wait(p_full, s & 1, abort_flag, status)) { ok = false; break; }
                 // the accumulation warps have read the previous step's Y
                 if (s > 0 && !mbar_wait(y_empty, (s - 1) & 1, abort_flag, status)) { ok = false; break; }
+                const int ys = s % NYS;
+                if (!mbar_wait(&yf[ys], (s / NYS) & 1, abort_flag, status)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t dyah = sdesc_sw128(base + Y_OFF, 16, 1024);
-                const uint64_t dyal = sdesc_sw128(base + Y_OFF + YT_BYTES, 16, 1024);
-                const uint64_t dybh = sdesc_sw128(base + Y_OFF + 2 * YT_BYTES, 16, 1024);
-                const uint64_t dybl = sdesc_sw128(base + Y_OFF + 3 * YT_BYTES, 16, 1024);
+                const uint32_t base = smem_u32(smem + YS_OFF + ys * YS_BYTES);
+                const uint64_t dyah = sdesc_sw128(base, 16, 1024);
+                const uint64_t dyal = sdesc_sw128(base + YT_BYTES, 16, 1024);
+                const uint64_t dybh = sdesc_sw128(base + 2 * YT_BYTES, 16, 1024);
+                const uint64_t dybl = sdesc_sw128(base + 3 * YT_BYTES, 16, 1024);
                 // Y1 = (P or dS) ya, Y2 = dS yb over the block's 32 rows (4 k-steps of 8), in a
                 // fresh accumulator
 #pragma unroll
@@ -329,7 +358,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 mma_commit(y_full);
-                mma_commit(&x_empty[st]);
+                mma_commit(&ye[ys]);
             }
             // Nothing issued may still be running when TMEM is released.
             mma_commit(mma_done);
@@ -380,12 +409,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         uint8_t *ph = smem + STG_OFF, *pl = ph + STG_BYTES, *sh = pl + STG_BYTES, *sl = sh + STG_BYTES;
         for (int s = 0; s < T; ++s) {
-            ok = __all_sync(0xffffffffu, mbar_wait(x_done, s & 1, abort_flag, status));
+            ok = __all_sync(0xffffffffu, mbar_wait(&x_done[s & 1], (s >> 1) & 1, abort_flag, status));
             if (!ok) break;
             tc_fence_after();
             uint32_t x1[32], x2[32];
-            tmem_ld_x32(tmem + lane_off + T_X1, x1);
-            tmem_ld_x32(tmem + lane_off + T_X2, x2);
+            tmem_ld_x32(tmem + lane_off + T_X + 192 * (s & 1), x1);
+            tmem_ld_x32(tmem + lane_off + T_X + 192 * (s & 1) + 32, x2);
             int plane, blk;
             step(s, plane, blk);
             const int c0 = blk * BC;
@@ -404,7 +433,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     p[c] = allowed ? ex2_approx(fmaf(__uint_as_float(x1[c]), scale_log2, -lq)) : 0.f;
                     ds[c] = p[c] * (__uint_as_float(x2[c]) - dq);
                 }
-                stage_row(ph, pl, row, p);
             } else {
                 // thread = query grow; column c = key c0 + c
 #pragma unroll
@@ -415,6 +443,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ds[c] = p[c] * (__uint_as_float(x2[c]) - Dr);
                 }
             }
+            // the last products of step s - 1 have finished reading the staged operands
+            if (s > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(y_full, (s - 1) & 1, abort_flag, status));
+                if (!ok) break;
+            }
+            if (DKV) stage_row(ph, pl, row, p);
             stage_row(sh, sl, row, ds);
             fence_proxy_async_smem();
             tc_fence_before();
