@@ -13,11 +13,15 @@
 // (transposed so that both operands of P V are K-major: TF32 operands are used K-major only).
 // K9b: one CTA per 128-row query tile, d = 64, 32-key blocks; 192 threads:
 //   warps 0-3 : softmax warps (thread = query row = TMEM lane)
-//   warp 4    : TMA producer (Q hi / lo once, K and V^T hi / lo per block, 2 stages)
+//   warp 4    : TMA producer (Q hi / lo once, K and V^T hi / lo per block, 3 stages)
 //   warp 5    : TMEM allocator and single-thread MMA issuer
-// TMEM: S at columns [0, 32), O at [64, 128).  P (split into hi / lo) is staged in shared memory
-// as the K-major A operand of P V.  The max is rescaled lazily (threshold 8, log2 units) as in
-// the bf16 forward.
+// TMEM: S double-buffered at columns [0, 32) and [32, 64), so S of block j + 1 is computed while
+// the softmax warps work on block j; P V of one block at [64, 128).  P (split into hi / lo) is
+// staged in shared memory as the K-major A operand of P V.  Each block's P V starts a fresh
+// accumulator and the softmax warps add it into fp32 register sums: the tensor core's
+// accumulation error grows with the number of MMAs chained into one accumulator, and this keeps
+// the chain at 12.  The max is rescaled lazily (threshold 8, log2 units) as in the bf16 forward,
+// on the register sums.
 #include <algorithm>
 #include <cmath>
 
@@ -43,15 +47,18 @@ constexpr int K_BYTES = 2 * K_CHUNK;
 constexpr int VT_BYTES = D * 128;               // V^T block: 64 rows (d) x 32 keys
 constexpr int P_BYTES = BM * 128;               // P block: 128 rows x 32 keys
 constexpr int QH_OFF = 0, QL_OFF = Q_BYTES;
-constexpr int STAGE_OFF = 2 * Q_BYTES;          // [2 stages][Kh | Kl | Vth | Vtl]
+constexpr int NST = 3;                          // K / V^T ring stages
+constexpr int STAGE_OFF = 2 * Q_BYTES;          // [NST stages][Kh | Kl | Vth | Vtl]
 constexpr int STAGE_BYTES = 2 * K_BYTES + 2 * VT_BYTES;
-constexpr int PH_OFF = STAGE_OFF + 2 * STAGE_BYTES, PL_OFF = PH_OFF + P_BYTES;
+constexpr int PH_OFF = STAGE_OFF + NST * STAGE_BYTES, PL_OFF = PH_OFF + P_BYTES;
 constexpr int BAR_OFF = PL_OFF + P_BYTES;
-// q_full, kv_full[2], kv_empty[2], s_full, p_full, o_done, mma_done
-constexpr int NBARS = 9;
+// q_full, kv_full[NST], kv_empty[NST], s_full[2], p_full, o_done, mma_done
+constexpr int NBARS = 1 + 2 * NST + 2 + 3;
 constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
 constexpr int ABORT_OFF = TMEM_OFF + 8;
 constexpr int SMEM_BYTES = ABORT_OFF + 8 + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+// S of block j in buffer j & 1 at T_S + 32 (j & 1); P V of one block (a fresh accumulator) at T_O
 constexpr uint32_t T_S = 0, T_O = 64;
 
 // K9a: Qh, Ql [BH, N, 64]; Kh, Kl [BHkv, N, 64]; Vth, Vtl [BHkv, 64, Np] (keys Np >= N zero).
@@ -95,8 +102,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + BAR_OFF);
-    uint64_t *q_full = bars, *kv_full = bars + 1, *kv_empty = bars + 3, *s_full = bars + 5;
-    uint64_t *p_full = bars + 6, *o_done = bars + 7, *mma_done = bars + 8;
+    uint64_t *q_full = bars, *kv_full = bars + 1, *kv_empty = bars + 1 + NST;
+    uint64_t *s_full = bars + 1 + 2 * NST, *p_full = s_full + 2, *o_done = p_full + 1;
+    uint64_t *mma_done = o_done + 1;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + TMEM_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + ABORT_OFF);
 
@@ -109,11 +117,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NST; ++s) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
-        mbar_init(s_full, 1);
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
         mbar_init(p_full, BM);
         mbar_init(o_done, 1);
         mbar_init(mma_done, 1);
@@ -139,8 +148,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             int issued = 0;
             for (int j = 0; j < nb; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !mbar_wait(&kv_empty[st], ((j - 2) >> 1) & 1, abort_flag, status)) break;
+                const int st = j % NST;
+                if (j >= NST && !mbar_wait(&kv_empty[st], (j / NST - 1) & 1, abort_flag, status)) break;
                 mbar_arrive_expect_tx(&kv_full[st], STAGE_BYTES);
                 uint8_t *base = smem + STAGE_OFF + st * STAGE_BYTES;
                 for (int ch = 0; ch < D / 32; ++ch) {
@@ -152,7 +161,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 issued = j + 1;
             }
             if (*abort_flag) {
-                for (int j = max(0, issued - 2); j < issued; ++j) mbar_drain(&kv_full[j & 1], (j >> 1) & 1);
+                for (int j = max(0, issued - NST); j < issued; ++j) mbar_drain(&kv_full[j % NST], (j / NST) & 1);
                 mbar_drain(q_full, 0);
             }
         }
@@ -167,33 +176,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t dql = sdesc_sw128(smem_u32(smem + QL_OFF), 16, 1024);
             const uint64_t dph = sdesc_sw128(smem_u32(smem + PH_OFF), 16, 1024);
             const uint64_t dpl = sdesc_sw128(smem_u32(smem + PL_OFF), 16, 1024);
-            bool ok = mbar_wait(q_full, 0, abort_flag, status);
-            for (int j = 0; j < nb && ok; ++j) {
-                const int st = j & 1;
-                if (!mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag, status)) { ok = false; break; }
+            // S = Qh Kh + Qh Kl + Ql Kh of block j into buffer j & 1, over d = 64 (8 k-steps of 8)
+            auto issue_s = [&](int j) -> bool {
+                const int st = j % NST;
+                if (!mbar_wait(&kv_full[st], (j / NST) & 1, abort_flag, status)) return false;
                 tc_fence_after();
                 const uint32_t base = smem_u32(smem + STAGE_OFF + st * STAGE_BYTES);
                 const uint64_t dkh = sdesc_sw128(base, 16, 1024);
                 const uint64_t dkl = sdesc_sw128(base + K_BYTES, 16, 1024);
-                const uint64_t dvh = sdesc_sw128(base + 2 * K_BYTES, 16, 1024);
-                const uint64_t dvl = sdesc_sw128(base + 2 * K_BYTES + VT_BYTES, 16, 1024);
-                // S = Qh Kh + Qh Kl + Ql Kh over d = 64 (8 k-steps of 8)
+                const uint32_t ts = tmem + T_S + 32 * (j & 1);
 #pragma unroll
                 for (int kk = 0; kk < D / 8; ++kk) {
                     const uint32_t oq = (kk >> 2) * Q_CHUNK + (kk & 3) * 32;
                     const uint32_t ok2 = (kk >> 2) * K_CHUNK + (kk & 3) * 32;
-                    mma_tf32(tmem + T_S, sdesc_add(dqh, oq), sdesc_add(dkh, ok2), IDESC_S, kk > 0);
-                    mma_tf32(tmem + T_S, sdesc_add(dqh, oq), sdesc_add(dkl, ok2), IDESC_S, 1u);
-                    mma_tf32(tmem + T_S, sdesc_add(dql, oq), sdesc_add(dkh, ok2), IDESC_S, 1u);
+                    mma_tf32(ts, sdesc_add(dqh, oq), sdesc_add(dkh, ok2), IDESC_S, kk > 0);
+                    mma_tf32(ts, sdesc_add(dqh, oq), sdesc_add(dkl, ok2), IDESC_S, 1u);
+                    mma_tf32(ts, sdesc_add(dql, oq), sdesc_add(dkh, ok2), IDESC_S, 1u);
                 }
-                mma_commit(s_full);
+                mma_commit(&s_full[j & 1]);
+                return true;
+            };
+            bool ok = mbar_wait(q_full, 0, abort_flag, status);
+            if (ok && nb > 0) ok = issue_s(0);
+            for (int j = 0; j < nb && ok; ++j) {
+                // S of block j + 1 overlaps the softmax of block j; its buffer held S of block
+                // j - 1, read before p_full of block j - 1
+                if (j + 1 < nb && !issue_s(j + 1)) { ok = false; break; }
                 if (!mbar_wait(p_full, j & 1, abort_flag, status)) { ok = false; break; }
                 tc_fence_after();
-                // O += Ph Vh + Ph Vl + Pl Vh over the block's 32 keys (4 k-steps of 8)
+                const int st = j % NST;
+                const uint32_t base = smem_u32(smem + STAGE_OFF + st * STAGE_BYTES);
+                const uint64_t dvh = sdesc_sw128(base + 2 * K_BYTES, 16, 1024);
+                const uint64_t dvl = sdesc_sw128(base + 2 * K_BYTES + VT_BYTES, 16, 1024);
+                // P V of the block = Ph Vh + Ph Vl + Pl Vh over its 32 keys (4 k-steps of 8), in
+                // a fresh accumulator that the softmax warps add into their fp32 sums
 #pragma unroll
                 for (int kk = 0; kk < BN / 8; ++kk) {
                     const uint32_t off = kk * 32;
-                    mma_tf32(tmem + T_O, sdesc_add(dph, off), sdesc_add(dvh, off), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_tf32(tmem + T_O, sdesc_add(dph, off), sdesc_add(dvh, off), IDESC_PV, kk > 0 ? 1u : 0u);
                     mma_tf32(tmem + T_O, sdesc_add(dph, off), sdesc_add(dvl, off), IDESC_PV, 1u);
                     mma_tf32(tmem + T_O, sdesc_add(dpl, off), sdesc_add(dvh, off), IDESC_PV, 1u);
                 }
@@ -216,13 +236,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int rq = q0 + row;
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
         float m = -INFINITY, l = 0.f;
+        float osum[D];                 // O (unnormalised) in fp32 registers, rounded to nearest
+#pragma unroll
+        for (int c = 0; c < D; ++c) osum[c] = 0.f;
+        // adds the finished P V of the previous block (every lane loads: .sync.aligned)
+        auto add_pv = [&]() {
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld_x32(tmem + lane_off + T_O + c0, o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) osum[c0 + i] += __uint_as_float(o[i]);
+            }
+        };
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag, status));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag, status));
             if (!ok) break;
             tc_fence_after();
             uint32_t sraw[32];
-            tmem_ld_x32(tmem + lane_off + T_S, sraw);
+            tmem_ld_x32(tmem + lane_off + T_S + 32 * (j & 1), sraw);
             float s[32];
             float mx = -INFINITY;
 #pragma unroll
@@ -231,31 +264,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 s[c] = ((CAUSAL && key > rq) || key >= N) ? -INFINITY : __uint_as_float(sraw[c]);
                 mx = fmaxf(mx, s[c]);
             }
-            // P V of the previous block must be done before P is restaged or O rescaled
+            // P V of the previous block must be done before P is restaged; its result joins the
+            // sums at the scale it was computed with, before any rescale
             if (j > 0) {
                 ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag, status));
                 if (!ok) break;
                 tc_fence_after();
+                add_pv();
             }
             const float m_blk = mx * scale_log2;
-            const bool need = m_blk > m + RESCALE_THRESHOLD;
-            if (__any_sync(0xffffffffu, need)) {
-                const float alpha = need ? ex2_approx(m - m_blk) : 1.f;
-                if (need) {
-                    l *= alpha;
-                    m = m_blk;
-                }
-                if (j > 0) {
+            if (m_blk > m + RESCALE_THRESHOLD) {
+                const float alpha = ex2_approx(m - m_blk);
+                l *= alpha;
+                m = m_blk;
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld_x32(tmem + lane_off + T_O + c0, o);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st_x32(tmem + lane_off + T_O + c0, o);
-                    }
-                    tmem_wait_st();
-                }
+                for (int c = 0; c < D; ++c) osum[c] *= alpha;
             }
             const float m_sub = (m == -INFINITY) ? 0.f : m;
             uint8_t *ph = smem + PH_OFF + row * 128, *pl = smem + PL_OFF + row * 128;
@@ -282,19 +305,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(o_done, (nb - 1) & 1, abort_flag, status));
             if (ok) {
                 tc_fence_after();
+                add_pv();
                 const float inv = 1.f / l;
                 float *orow = O + (static_cast<size_t>(bh) * N + rq) * D;
+                if (rq < N) {
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t o[32];
-                    tmem_ld_x32(tmem + lane_off + T_O + c0, o);     // every lane: .sync.aligned
-                    if (rq < N) {
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            reinterpret_cast<float4 *>(orow + c0)[u] =
-                                make_float4(__uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
-                                            __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
-                    }
+                    for (int u = 0; u < D / 4; ++u)
+                        reinterpret_cast<float4 *>(orow)[u] =
+                            make_float4(osum[4 * u] * inv, osum[4 * u + 1] * inv, osum[4 * u + 2] * inv,
+                                        osum[4 * u + 3] * inv);
                 }
                 if (rq < N) LSE[static_cast<size_t>(bh) * N + rq] = (m + log2f(l)) * LN2;
             }
