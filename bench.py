@@ -35,8 +35,8 @@ WORKLOAD = "causal_n4096"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic per launch of the reported kernel from one ncu capture, keyed by
-# "<kernel file>:<sha256 prefix of that file and fa_ptx.cuh>:<workload>"; a key that no longer
-# matches the sources (the kernel changed since the capture) reports null.
+# "<kernel file>:<sha256 prefix of that file and the device headers it includes>:<workload>";
+# a key that no longer matches the sources (the kernel changed since the capture) reports null.
 NCU_TRAFFIC = {
     # fa_bwd on causal_n4096: bwd_main 1.917 GB read + 0.986 GB write, bwd_preprocess 0.206 GB,
     # bwd_dq_convert 0.160 GB
@@ -50,8 +50,9 @@ NCU_TRAFFIC = {
     "fa_bwd_sm103a.cu:3ef17436d4cd1a3f:dropout_n4096": 3.72e9,
     # key/value-outer forward
     "fa_fwd_kvouter_sm103a.cu:cf980aee93773e67:kvouter_n4096": 4.14e9,
-    # fp32 tensor-core forward, split + attention kernels
-    "fa_fwd_tf32x3_sm103a.cu:b945be0e3f2d66ea:fp32tc_n4096": 0.491e9,
+    # fp32 tensor-core backward: split rows 0.343 GB, split transposes 0.239 GB, dq pass
+    # 0.328 GB, dkv pass 0.403 GB
+    "fa_bwd_tf32x3_sm103a.cu:920f747c9ad578a2:fp32tc_n4096": 1.314e9,
 }
 
 
