@@ -108,9 +108,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     float scale, float scale_log2, const MaskArgs mk, const DropoutArgs drop,
                     unsigned *status) {
     static_assert(!(MASK && DROP), "one variant at a time");
-    // Laid out for d = 128.  With a real head dim DR = 64 the tensor maps are 64 wide, so the
-    // second 64-column chunk of every load is TMA zero fill: all products see zero-padded
-    // operands and are unchanged; only the dQ reductions and the dK / dV stores use DR.
+    // Laid out for d = 128.  With a real head dim DR = 64 only the first 64-column chunk of Q,
+    // dO and V is loaded and S^T, dP^T (K dim), dV and dK (N) run over DR; dQ^T keeps M = 128
+    // (the MMA's row count), its upper rows coming from K's second chunk, which the 64-wide
+    // tensor map fills with zeros, so only the dQ reductions see DR there.
     static_assert(D == 128, "the bf16 backward main loop is laid out for d = 128");
     static_assert(DR == 64 || DR == 128, "real head dim 64 or 128");
     using L = Layout<D>;
@@ -243,9 +244,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 int g, i;
                 step_tile(s, g, i);
                 const int bhq = b * Hq + hk * G + g;
-                mbar_arrive_expect_tx(&q_full[st], 2 * L::Q_BYTES);
+                mbar_arrive_expect_tx(&q_full[st], 2 * (DR / 64) * L::Q_CHUNK);
                 uint8_t *qdst = smem + L::QR_OFF + st * 2 * L::Q_BYTES;
-                for (int ch = 0; ch < D / 64; ++ch) {
+                for (int ch = 0; ch < DR / 64; ++ch) {
                     tma_load_3d(qdst + ch * L::Q_CHUNK, &tmQ, ch * 64, i * BQ, bhq, &q_full[st]);
                     tma_load_3d(qdst + L::Q_BYTES + ch * L::Q_CHUNK, &tmdO, ch * 64, i * BQ, bhq,
                                 &q_full[st]);
@@ -262,7 +263,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t IDESC_SP = idesc_bf16(BKV, BQ, false, false);   // S^T, dP^T
-            constexpr uint32_t IDESC_KV = idesc_bf16(BKV, D, false, true);     // dV, dK
+            constexpr uint32_t IDESC_KV = idesc_bf16(BKV, DR, false, true);    // dV, dK
             constexpr uint32_t IDESC_DQ = idesc_bf16(D, BQ, true, true);       // dQ^T
             // Descriptors are built once; each k-step only moves the start address.
             const uint64_t dk_k = sdesc_sw128(smem_u32(smem + L::K_OFF), 16, 1024);        // K, K-major
@@ -278,13 +279,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint64_t ddo = sdesc_add(dq, L::Q_BYTES);
                 const uint32_t buf = tmem + T_BUF + (s & 1) * 128;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < DR / 16; ++kk) {
                     const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
                     mma_ss(buf + B_ST, sdesc_add(dk_k, oa), sdesc_add(dq, ob), IDESC_SP, kk > 0);
                 }
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < DR / 16; ++kk) {
                     const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
                     mma_ss(buf + B_DPT, sdesc_add(dv_k, oa), sdesc_add(ddo, ob), IDESC_SP, kk > 0);
@@ -479,7 +480,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float mul = which ? 1.f : scale;
                 uint8_t *dst = smem + (which ? L::V_OFF : L::K_OFF);
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = 0; c0 < DR; c0 += 32) {
                     uint32_t a[32];
                     tmem_ld_x32(tmem + lane_off + tcol + c0, a);
                     if (MASK && T == 0) {               // no step: TMEM was never written
