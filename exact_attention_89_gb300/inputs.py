@@ -65,6 +65,9 @@ WORKLOADS = {
     # Block-sparse causal pattern (general mask: tile mask): a local window plus a first tile.
     "local_n16384": Workload("local_n16384", 1, 16, 16, 16384, 128, True, 7, torch.bfloat16, True,
                              mask="local_sink"),
+    # The bench workload's shape at head dim 64.
+    "causal_d64_n4096": Workload("causal_d64_n4096", 2, 32, 32, 4096, 64, True, 10, torch.bfloat16,
+                                 True),
     # The bench workload's shape with dropout p = 0.1 on P.
     "dropout_n4096": Workload("dropout_n4096", 2, 32, 32, 4096, 128, True, 8, torch.bfloat16, True,
                               dropout=0.1),

@@ -59,7 +59,8 @@ def test_backward_invariants_on_gpu(flash):
     assert float(dK.double().sum(2).abs().max()) <= 0.05 * float(dK.double().abs().sum(2).max())
 
 
-@pytest.mark.parametrize("name", ["causal_n4096", "gqa_n8192", "long_n32768"])
+@pytest.mark.parametrize("name", ["causal_n4096", "gqa_n8192", "long_n32768",
+                                  "causal_d64_n4096"])
 def test_backward_full_size_workloads(flash, oracle_mod, name):
     w = WORKLOADS[name]
     Q, K, V, dO = workload_inputs(w)

@@ -77,7 +77,8 @@ def test_forward_fwd_d64_workload(flash, oracle_mod):
     assert_fwd_close(O, LSE, Oo, Lo, w.name)
 
 
-@pytest.mark.parametrize("name", ["causal_n4096", "gqa_n8192", "long_n32768"])
+@pytest.mark.parametrize("name", ["causal_n4096", "gqa_n8192", "long_n32768",
+                                  "causal_d64_n4096"])
 def test_forward_full_size_workloads(flash, oracle_mod, name):
     """Full-size causal workloads in the launch configuration the benchmark times: one whole
     (batch, KV-group) slice (N <= 8192) plus rows sampled over all heads."""
