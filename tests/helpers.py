@@ -40,7 +40,7 @@ def mean_abs(a, b):
 def rel_fro(a, ref):
     """||a - ref||_F / ||ref||_F, with the denominator floored at 1e-3 RMS: where the exact
     gradient is identically zero (one key per query: its weight is exactly 1, so dS = 0) a
-    relative error is undefined and the rounding noise is judged against that floor."""
+    relative error is undefined and the rounding noise is measured against that floor."""
     a = _np(a)
     ref = _np(ref)
     floor = 1e-3 * np.sqrt(ref.size)
