@@ -8,7 +8,8 @@ Printed JSON line (rank 0):
   value     attention TFLOP/s of fwd+bwd, whole job (all ranks), device-timed with CUDA events,
             inputs resident in HBM; FLOPs = 4 B Hq N^2 d (x2.5 for the backward, /2 for causal).
   e2e       the same metric through the public API with pinned host buffers: every step copies
-            Q, K, V, dO host->device and O, LSE, dQ, dK, dV device->host inside the timed region.
+            Q, K, V, dO host->device and O, LSE, dQ, dK, dV device->host inside the timed region;
+            the copies of neighbouring steps overlap the compute (copy streams, two buffer sets).
   roofline  the dominant launch sequence (fa_bwd) against the measured dense bf16 peak.
   cpu_baseline  the fp64 oracle on a bounded sample (whole heads) of the same workload.
 --impl reference times the oracle itself (the reference arm) on the same metric.
@@ -438,34 +439,44 @@ def main():
                           device=dev)
     stream = torch.cuda.current_stream()
 
-    def fwd_first():
+    # the tensors a step reads and writes (the end-to-end run swaps in other sets)
+    main_set = {"q": q, "k": k, "v": v, "do": do, "O": O, "LSE": LSE}
+    if w.backward:
+        main_set.update(dQ=dQ, dK=dK, dV=dV)
+
+    def fwd_first(t=main_set):
         # the forward's tensor-core launch
         if split:
-            fa.fa_fwd_split(q, k, v, Op, Lp, w.causal, w.scale, S)
+            fa.fa_fwd_split(t["q"], t["k"], t["v"], Op, Lp, w.causal, w.scale, S)
         elif masked:
-            fa.fa_fwd_masked(q, k, v, O, LSE, w.causal, w.scale, mq, mkk, mbm)
+            fa.fa_fwd_masked(t["q"], t["k"], t["v"], t["O"], t["LSE"], w.causal, w.scale, mq, mkk, mbm)
         elif w.dropout:
-            fa.fa_fwd_dropout(q, k, v, O, LSE, w.causal, w.scale, w.dropout, w.seed, 0)
+            fa.fa_fwd_dropout(t["q"], t["k"], t["v"], t["O"], t["LSE"], w.causal, w.scale, w.dropout,
+                              w.seed, 0)
         elif w.kv_outer:
-            fa.fa_fwd_kvouter(q, k, v, O, LSE, w.causal, w.scale, kws)
+            fa.fa_fwd_kvouter(t["q"], t["k"], t["v"], t["O"], t["LSE"], w.causal, w.scale, kws)
         elif w.tensor_fp32:
-            fa.fa_fwd_fp32_tc(q, k, v, O, LSE, w.causal, w.scale, kws)
+            fa.fa_fwd_fp32_tc(t["q"], t["k"], t["v"], t["O"], t["LSE"], w.causal, w.scale, kws)
         else:
-            fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
+            fa.fa_fwd(t["q"], t["k"], t["v"], t["O"], t["LSE"], w.causal, w.scale)
 
-    def second():
+    def second(t=main_set):
         # what follows it in a step: the merge of the partials, or the backward
         if split:
-            fa.fa_merge(Op, Lp, O, LSE)
-        elif masked:
-            fa.fa_bwd_masked(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsp, mq, mkk, mbm)
+            fa.fa_merge(Op, Lp, t["O"], t["LSE"])
+            return
+        if not w.backward:
+            return
+        args_b = (t["q"], t["k"], t["v"], t["O"], t["do"], t["LSE"], t["dQ"], t["dK"], t["dV"],
+                  w.causal, w.scale)
+        if masked:
+            fa.fa_bwd_masked(*args_b, wsp, mq, mkk, mbm)
         elif w.dropout:
-            fa.fa_bwd_dropout(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, w.dropout,
-                              w.seed, 0, wsp)
-        elif w.tensor_fp32 and w.backward:
-            fa.fa_bwd_fp32_tc(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsp)
-        elif w.backward:
-            fa.fa_bwd(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsp)
+            fa.fa_bwd_dropout(*args_b, w.dropout, w.seed, 0, wsp)
+        elif w.tensor_fp32:
+            fa.fa_bwd_fp32_tc(*args_b, wsp)
+        else:
+            fa.fa_bwd(*args_b, wsp)
 
     def step():
         fwd_first()
@@ -565,58 +576,64 @@ def main():
         simt_bwd_ms = b_s.elapsed_time(b_e)
 
     # ---------------------------------------------------------------- end to end (host buffers)
+    # Every step copies its inputs from pinned host memory, runs the path through the public
+    # entry points and copies its outputs back to pinned host memory.  The copies run on their
+    # own streams with two sets of device buffers, so the inputs of step k + 1 and the outputs of
+    # step k - 1 move while step k computes, as a training loop fed from host memory would run.
     pin = [t.pin_memory() for t in (Qh, Kh, Vh, dOh) if t is not None]
-    outs = (O, LSE, dQ, dK, dV) if w.backward else (O, LSE)
-    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    out_names = ["O", "LSE", "dQ", "dK", "dV"] if w.backward else ["O", "LSE"]
+    outs_h = [torch.empty(main_set[n].shape, dtype=main_set[n].dtype, pin_memory=True)
+              for n in out_names]
     h2d = sum(t.numel() * t.element_size() for t in pin)
     d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    in_names = ["q", "k", "v", "do"][:len(pin)]
+    e2e_sets = [main_set]
+    if not args.no_extras:
+        e2e_sets.append({n: torch.empty_like(main_set[n]) for n in in_names + out_names})
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
 
-    def e2e_step():
-        dev_in = [t.to(dev, non_blocking=True) for t in pin]
-        qd, kd, vd = dev_in[:3]
-        if split:
-            res = fa.attention_forward_split(qd, kd, vd, w.causal, w.scale, num_splits=S)
-        elif masked:
-            res = fa.attention_forward_masked(qd, kd, vd, w.causal, w.scale, mq, mkk, mbm)
-        elif w.dropout:
-            res = fa.attention_forward_dropout(qd, kd, vd, w.causal, w.scale, w.dropout, w.seed)
-        elif w.kv_outer:
-            res = fa.attention_forward_kvouter(qd, kd, vd, w.causal, w.scale, workspace=kws)
-        elif w.tensor_fp32:
-            res = fa.attention_forward_fp32_tc(qd, kd, vd, w.causal, w.scale, workspace=kws)
-        else:
-            res = fa.attention_forward(qd, kd, vd, w.causal, w.scale)
-        if masked:
-            res = res + fa.attention_backward_masked(qd, kd, vd, res[0], dev_in[3], res[1],
-                                                     w.causal, w.scale, mq, mkk, mbm,
-                                                     workspace=wsp)
-        elif w.dropout:
-            res = res + fa.attention_backward_dropout(qd, kd, vd, res[0], dev_in[3], res[1],
-                                                      w.causal, w.scale, w.dropout, w.seed,
-                                                      workspace=wsp)
-        elif w.tensor_fp32 and w.backward:
-            res = res + fa.attention_backward_fp32_tc(qd, kd, vd, res[0], dev_in[3], res[1],
-                                                      w.causal, w.scale, workspace=wsp)
-        elif w.backward:
-            res = res + fa.attention_backward(qd, kd, vd, res[0], dev_in[3], res[1], w.causal,
-                                              w.scale, workspace=wsp)
-        for hbuf, dbuf in zip(outs_h, res):
-            hbuf.copy_(dbuf, non_blocking=True)
+    def e2e_run(nsteps):
+        """nsteps pipelined steps; returns their time in ms (events on the compute stream)."""
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        ready = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        out_done = [torch.cuda.Event() for _ in range(2)]
+        t0.record(stream)
+        s_in.wait_event(t0)
+        s_out.wait_event(t0)
+        for kk in range(nsteps):
+            b = kk % 2
+            t = e2e_sets[b]
+            with torch.cuda.stream(s_in):
+                if kk >= 2:
+                    s_in.wait_event(done[b])          # step k - 2 has read this input set
+                for n, src in zip(in_names, pin):
+                    t[n].copy_(src, non_blocking=True)
+                ready[b].record(s_in)
+            stream.wait_event(ready[b])
+            if kk >= 2:
+                stream.wait_event(out_done[b])        # step k - 2's outputs have left this set
+            fwd_first(t)
+            second(t)
+            done[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done[b])
+                for hbuf, n in zip(outs_h, out_names):
+                    hbuf.copy_(t[n], non_blocking=True)
+                out_done[b].record(s_out)
+        for e in out_done[:min(nsteps, 2)]:
+            stream.wait_event(e)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
 
     e2e_ms = float("nan")
     if not args.no_extras:
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
+        e2e_run(2)
         barrier()
-        e_s = torch.cuda.Event(enable_timing=True)
-        e_e = torch.cuda.Event(enable_timing=True)
-        e_s.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e_e.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = e_s.elapsed_time(e_e)
+        e2e_ms = e2e_run(args.steps)
     e2e_ms = max_over_ranks(e2e_ms, ws, dev)
     e2e_value = whole_job_tflops(ws, flops_step, args.steps, e2e_ms)
 
@@ -738,7 +755,10 @@ def main():
                 "fwd_frac_of_peak": fwd_achieved / peak,
                 "fwd_bwd_frac_of_peak": value / ws / peak if w.backward else None,
                 "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps,
+                        "pipeline": "host-to-device copy of step k+1 and device-to-host copy "
+                                    "of step k-1 overlap step k (two device buffer sets, copy "
+                                    "streams); first and last copies inside the timed region"},
                 "gpu_launches": args.steps * (
                     (2 if split or w.tensor_fp32 else 1) +
                     ((4 if w.tensor_fp32 else 3) if w.backward else 0)),
