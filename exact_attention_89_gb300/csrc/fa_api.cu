@@ -98,6 +98,18 @@ bool encode_bf16(CUtensorMap *m, const void *base, int d, int N, long long BH, i
 
 fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
+// The backward's fp32 dQ accumulator [B*Hq, N, 64] as a target of TMA reductions: box
+// [64, 64, 1] (one 64-query step of one head), no swizzle.  Used at head dim 64 only.
+bool encode_dq64(CUtensorMap *m, float *dQacc, int N, long long BH) {
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {64 * 4, static_cast<cuuint64_t>(N) * 64 * 4};
+    cuuint32_t box[3] = {64, 64, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dQacc, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D fp32 view [inner, rows, planes] of a contiguous tensor, box [32, box_rows, 1], 128B swizzle.
 bool encode_f32(CUtensorMap *m, const void *base, long long inner, long long rows, long long planes,
                 int box_rows) {
@@ -258,7 +270,7 @@ fa_status fa_bwd_dropout(const void *Q, const void *K, const void *V, const void
     float *Dvec = static_cast<float *>(workspace);
     float *dQacc = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                              fa::align256(rows * sizeof(float)));
-    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
     if (!fa::encode_bf16(&tq, Q, d, N, 1LL * B * Hq, 64) ||
         !fa::encode_bf16(&tk, K, d, N, 1LL * B * Hkv, 128) ||
         !fa::encode_bf16(&tv, V, d, N, 1LL * B * Hkv, 128) ||
@@ -266,9 +278,11 @@ fa_status fa_bwd_dropout(const void *Q, const void *K, const void *V, const void
         !fa::encode_bf16(&tdk, dK, d, N, 1LL * B * Hkv, 128) ||
         !fa::encode_bf16(&tdv, dV, d, N, 1LL * B * Hkv, 128))
         return FA_ERR_CUDA;
+    if (d == 64 && !fa::encode_dq64(&tdq, dQacc, N, 1LL * B * Hq)) return FA_ERR_CUDA;
+    if (d != 64) tdq = tdk;                 // unused at head dim 128
     cudaError_t e = fa::launch_bwd_preprocess_bf16(p, O, dO, Dvec, dQacc, stream);
     if (e == cudaSuccess)
-        e = fa::launch_bwd_main_dropout_bf16(p, tq, tk, tv, tdo, tdk, tdv, LSE, Dvec, dQacc, dr,
+        e = fa::launch_bwd_main_dropout_bf16(p, tq, tk, tv, tdo, tdk, tdv, tdq, LSE, Dvec, dQacc, dr,
                                              di->status, stream);
     if (e == cudaSuccess) e = fa::launch_bwd_dq_convert_bf16(p, dQacc, dQ, stream);
     return fa::from_cuda(e);
@@ -337,7 +351,7 @@ fa_status fa_bwd_masked(const void *Q, const void *K, const void *V, const void 
     float *Dvec = static_cast<float *>(workspace);
     float *dQacc = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                              fa::align256(rows * sizeof(float)));
-    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
     if (!fa::encode_bf16(&tq, Q, d, N, 1LL * B * Hq, 64) ||
         !fa::encode_bf16(&tk, K, d, N, 1LL * B * Hkv, 128) ||
         !fa::encode_bf16(&tv, V, d, N, 1LL * B * Hkv, 128) ||
@@ -345,9 +359,11 @@ fa_status fa_bwd_masked(const void *Q, const void *K, const void *V, const void 
         !fa::encode_bf16(&tdk, dK, d, N, 1LL * B * Hkv, 128) ||
         !fa::encode_bf16(&tdv, dV, d, N, 1LL * B * Hkv, 128))
         return FA_ERR_CUDA;
+    if (d == 64 && !fa::encode_dq64(&tdq, dQacc, N, 1LL * B * Hq)) return FA_ERR_CUDA;
+    if (d != 64) tdq = tdk;                 // unused at head dim 128
     cudaError_t e = fa::launch_bwd_preprocess_bf16(p, O, dO, Dvec, dQacc, stream);
     if (e == cudaSuccess)
-        e = fa::launch_bwd_main_masked_bf16(p, tq, tk, tv, tdo, tdk, tdv, LSE, Dvec, dQacc, mk,
+        e = fa::launch_bwd_main_masked_bf16(p, tq, tk, tv, tdo, tdk, tdv, tdq, LSE, Dvec, dQacc, mk,
                                             di->status, stream);
     if (e == cudaSuccess) e = fa::launch_bwd_dq_convert_bf16(p, dQacc, dQ, stream);
     return fa::from_cuda(e);
@@ -514,7 +530,7 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
     float *Dvec = static_cast<float *>(workspace);
     float *dQacc = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                              fa::align256(rows * sizeof(float)));
-    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
     if (!fa::encode_bf16(&tq, Q, d, N, 1LL * B * Hq, 64) ||
         !fa::encode_bf16(&tk, K, d, N, 1LL * B * Hkv, 128) ||
         !fa::encode_bf16(&tv, V, d, N, 1LL * B * Hkv, 128) ||
@@ -522,9 +538,12 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
         !fa::encode_bf16(&tdk, dK, d, N, 1LL * B * Hkv, 128) ||
         !fa::encode_bf16(&tdv, dV, d, N, 1LL * B * Hkv, 128))
         return FA_ERR_CUDA;
+    if (d == 64 && !fa::encode_dq64(&tdq, dQacc, N, 1LL * B * Hq)) return FA_ERR_CUDA;
+    if (d != 64) tdq = tdk;                 // unused at head dim 128
     cudaError_t e = fa::launch_bwd_preprocess_bf16(p, O, dO, Dvec, dQacc, stream);
     if (e == cudaSuccess)
-        e = fa::launch_bwd_main_bf16(p, tq, tk, tv, tdo, tdk, tdv, LSE, Dvec, dQacc, di->status, stream);
+        e = fa::launch_bwd_main_bf16(p, tq, tk, tv, tdo, tdk, tdv, tdq, LSE, Dvec, dQacc, di->status,
+                                     stream);
     if (e == cudaSuccess) e = fa::launch_bwd_dq_convert_bf16(p, dQacc, dQ, stream);
     return fa::from_cuda(e);
 }

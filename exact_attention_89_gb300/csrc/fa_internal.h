@@ -98,11 +98,14 @@ cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const vo
                                        float *dQacc, cudaStream_t stream);
 
 // K3: bf16 backward main loop on tcgen05.  tmQ / tmdO use a [64, 64, 1] box; tmK, tmV, tmdK,
-// tmdV a [64, 128, 1] box.  Accumulates scale * dS K into dQacc with fp32 reductions.
+// tmdV a [64, 128, 1] box.  Accumulates scale * dS K into dQacc with fp32 reductions: per
+// element at head dim 128, per 64 x 64 tile through tmdQ (fp32 [64, N, B*Hq], box [64, 64, 1],
+// no swizzle) at head dim 64, where tmdQ is otherwise unused.
 cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                                  const CUtensorMap &tmV, const CUtensorMap &tmdO,
                                  const CUtensorMap &tmdK, const CUtensorMap &tmdV,
-                                 const float *LSE, const float *D, float *dQacc, unsigned *status,
+                                 const CUtensorMap &tmdQ, const float *LSE, const float *D,
+                                 float *dQacc, unsigned *status,
                                  cudaStream_t stream);
 
 // K3 under a general mask.  Needs (Hq / Hkv) * ceil(N / 64) <= MASK_BWD_MAX_STEPS (the CTA's
@@ -111,7 +114,8 @@ constexpr int MASK_BWD_MAX_STEPS = 16384;
 cudaError_t launch_bwd_main_masked_bf16(const Problem &p, const CUtensorMap &tmQ,
                                         const CUtensorMap &tmK, const CUtensorMap &tmV,
                                         const CUtensorMap &tmdO, const CUtensorMap &tmdK,
-                                        const CUtensorMap &tmdV, const float *LSE, const float *D,
+                                        const CUtensorMap &tmdV, const CUtensorMap &tmdQ,
+                                        const float *LSE, const float *D,
                                         float *dQacc, const MaskArgs &mk, unsigned *status,
                                         cudaStream_t stream);
 
@@ -119,7 +123,8 @@ cudaError_t launch_bwd_main_masked_bf16(const Problem &p, const CUtensorMap &tmQ
 cudaError_t launch_bwd_main_dropout_bf16(const Problem &p, const CUtensorMap &tmQ,
                                          const CUtensorMap &tmK, const CUtensorMap &tmV,
                                          const CUtensorMap &tmdO, const CUtensorMap &tmdK,
-                                         const CUtensorMap &tmdV, const float *LSE, const float *D,
+                                         const CUtensorMap &tmdV, const CUtensorMap &tmdQ,
+                                         const float *LSE, const float *D,
                                          float *dQacc, const DropoutArgs &dr, unsigned *status,
                                          cudaStream_t stream);
 
