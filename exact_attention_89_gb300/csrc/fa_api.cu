@@ -98,11 +98,11 @@ bool encode_bf16(CUtensorMap *m, const void *base, int d, int N, long long BH, i
 
 fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
-// The backward's fp32 dQ accumulator [B*Hq, N, 64] as a target of TMA reductions: box
-// [64, 64, 1] (one 64-query step of one head), no swizzle.  Used at head dim 64 only.
-bool encode_dq64(CUtensorMap *m, float *dQacc, int N, long long BH) {
-    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-    cuuint64_t strides[2] = {64 * 4, static_cast<cuuint64_t>(N) * 64 * 4};
+// The backward's fp32 dQ accumulator [B*Hq, N, d] as a target of TMA reductions: box
+// [64, 64, 1] (64 columns of one 64-query step of one head), no swizzle.
+bool encode_dq(CUtensorMap *m, float *dQacc, int d, int N, long long BH) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
     cuuint32_t box[3] = {64, 64, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dQacc, dims, strides, box, estr,
@@ -110,7 +110,6 @@ bool encode_dq64(CUtensorMap *m, float *dQacc, int N, long long BH) {
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D fp32 view [inner, rows, planes] of a contiguous tensor, box [32, box_rows, 1], 128B swizzle.
 bool encode_f32(CUtensorMap *m, const void *base, long long inner, long long rows, long long planes,
                 int box_rows) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
@@ -278,8 +277,7 @@ fa_status fa_bwd_dropout(const void *Q, const void *K, const void *V, const void
         !fa::encode_bf16(&tdk, dK, d, N, 1LL * B * Hkv, 128) ||
         !fa::encode_bf16(&tdv, dV, d, N, 1LL * B * Hkv, 128))
         return FA_ERR_CUDA;
-    if (d == 64 && !fa::encode_dq64(&tdq, dQacc, N, 1LL * B * Hq)) return FA_ERR_CUDA;
-    if (d != 64) tdq = tdk;                 // unused at head dim 128
+    if (!fa::encode_dq(&tdq, dQacc, d, N, 1LL * B * Hq)) return FA_ERR_CUDA;
     cudaError_t e = fa::launch_bwd_preprocess_bf16(p, O, dO, Dvec, dQacc, stream);
     if (e == cudaSuccess)
         e = fa::launch_bwd_main_dropout_bf16(p, tq, tk, tv, tdo, tdk, tdv, tdq, LSE, Dvec, dQacc, dr,
@@ -359,8 +357,7 @@ fa_status fa_bwd_masked(const void *Q, const void *K, const void *V, const void 
         !fa::encode_bf16(&tdk, dK, d, N, 1LL * B * Hkv, 128) ||
         !fa::encode_bf16(&tdv, dV, d, N, 1LL * B * Hkv, 128))
         return FA_ERR_CUDA;
-    if (d == 64 && !fa::encode_dq64(&tdq, dQacc, N, 1LL * B * Hq)) return FA_ERR_CUDA;
-    if (d != 64) tdq = tdk;                 // unused at head dim 128
+    if (!fa::encode_dq(&tdq, dQacc, d, N, 1LL * B * Hq)) return FA_ERR_CUDA;
     cudaError_t e = fa::launch_bwd_preprocess_bf16(p, O, dO, Dvec, dQacc, stream);
     if (e == cudaSuccess)
         e = fa::launch_bwd_main_masked_bf16(p, tq, tk, tv, tdo, tdk, tdv, tdq, LSE, Dvec, dQacc, mk,
@@ -538,8 +535,7 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
         !fa::encode_bf16(&tdk, dK, d, N, 1LL * B * Hkv, 128) ||
         !fa::encode_bf16(&tdv, dV, d, N, 1LL * B * Hkv, 128))
         return FA_ERR_CUDA;
-    if (d == 64 && !fa::encode_dq64(&tdq, dQacc, N, 1LL * B * Hq)) return FA_ERR_CUDA;
-    if (d != 64) tdq = tdk;                 // unused at head dim 128
+    if (!fa::encode_dq(&tdq, dQacc, d, N, 1LL * B * Hq)) return FA_ERR_CUDA;
     cudaError_t e = fa::launch_bwd_preprocess_bf16(p, O, dO, Dvec, dQacc, stream);
     if (e == cudaSuccess)
         e = fa::launch_bwd_main_bf16(p, tq, tk, tv, tdo, tdk, tdv, tdq, LSE, Dvec, dQacc, di->status,

@@ -133,6 +133,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // tensor map fills with zeros, so only the dQ reductions see DR there.
     static_assert(D == 128, "the bf16 backward main loop is laid out for d = 128");
     static_assert(DR == 64 || DR == 128, "real head dim 64 or 128");
+    // At head dim 64 dQ leaves through bulk tensor reductions (see the drain warps); at 128 the
+    // per-element reductions measured faster (a staged 64 x 128 tile: 0.944 ms against 0.917).
+    constexpr bool DQ_TMA = DR == 64;
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -594,18 +597,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_ld_x64(tmem + lane_off + T_BUF + bsel * 128 + B_DQT, a);
             tc_fence_before();
             mbar_arrive(&dq_empty[bsel]);
-            if constexpr (DR == 64) {
-                // The 64 x 64 tile (query rows, d columns) goes to the accumulator as one bulk
-                // reduction from shared memory (V's unused second chunk): per-element reductions
-                // measured 25% of this step's time at d = 64.  Rows past the sequence end are
-                // clipped by the tensor map; rows past a mask's valid length hold zeros.
+            if constexpr (DQ_TMA) {
+                // The 64 x 64 tile of dQ (query rows, d columns) goes to the accumulator as one
+                // bulk reduction from shared memory, V's unused second chunk (per-element
+                // reductions measured 25% of the step's time at d = 64).  Rows past the sequence
+                // end are clipped by the tensor map; rows past a mask's valid length hold zeros.
+                // Lanes 64-127 (K's zero-filled half of dQ^T) sit out.
                 if (wq < 2) {
                     float *tile = reinterpret_cast<float *>(smem + L::V_OFF + L::KV_CHUNK);
-                    // the previous tile's reduction has finished reading shared memory
+                    // the previous tile's reductions have finished reading shared memory
                     if (threadIdx.x == 128) bulk_wait_read();
                     named_barrier_sync(2, 64);
+                    float *trow = tile + dcol;
 #pragma unroll
-                    for (int c = 0; c < BQ; ++c) tile[c * 64 + dcol] = __uint_as_float(a[c]) * scale;
+                    for (int c = 0; c < BQ; ++c) trow[c * 64] = __uint_as_float(a[c]) * scale;
                     fence_proxy_async_smem();
                     named_barrier_sync(2, 64);
                     if (threadIdx.x == 128) tma_reduce_add_3d(&tmdQ, tile, 0, q0, bhq);
@@ -619,7 +624,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
         // the last bulk reductions have finished reading shared memory (and writing)
-        if (DR == 64 && threadIdx.x == 128) bulk_wait_all();
+        if (DQ_TMA && threadIdx.x == 128) bulk_wait_all();
         tc_fence_before();
         __syncthreads();
     }

@@ -99,8 +99,8 @@ cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const vo
 
 // K3: bf16 backward main loop on tcgen05.  tmQ / tmdO use a [64, 64, 1] box; tmK, tmV, tmdK,
 // tmdV a [64, 128, 1] box.  Accumulates scale * dS K into dQacc with fp32 reductions: per
-// element at head dim 128, per 64 x 64 tile through tmdQ (fp32 [64, N, B*Hq], box [64, 64, 1],
-// no swizzle) at head dim 64, where tmdQ is otherwise unused.
+// element at head dim 128, per 64 x 64 tile through tmdQ (fp32 [d, N, B*Hq], box [64, 64, 1],
+// no swizzle) at head dim 64; tmdQ is unused at 128.
 cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                                  const CUtensorMap &tmV, const CUtensorMap &tmdO,
                                  const CUtensorMap &tmdK, const CUtensorMap &tmdV,
