@@ -44,9 +44,10 @@ constexpr int BQ = 64;            // query rows per step
 constexpr int NSQ = 3;            // Q / dO ring stages
 constexpr int NUM_THREADS = 384;   // three warpgroups
 constexpr int WARP_TMA = 8;
-constexpr int WARP_MMA = 9;
+constexpr int WARP_MMA = 9;       // TMEM allocator; issues S^T and dP^T
+constexpr int WARP_MMA2 = 10;     // issues dQ^T, dV and dK
 // Register split: softmax-gradient warpgroup grows; dQ drain and TMA/MMA warpgroups shrink.
-constexpr uint32_t REGS_GRAD = 256, REGS_DRAIN = 104, REGS_OTHER = 64;
+constexpr uint32_t REGS_GRAD = 256, REGS_DRAIN = 96, REGS_OTHER = 72;
 constexpr int REGS_NEEDED = 128 * (REGS_GRAD + REGS_DRAIN + REGS_OTHER);
 constexpr float LOG2E = 1.4426950408889634f;
 // Steps (query head of the group x query tile) a masked CTA can list in shared memory.
@@ -66,8 +67,8 @@ struct Layout {
     static constexpr int STAT_OFF = DS_OFF + 2 * DS_BYTES;     // [2][lse2 64 | D 64] fp32
     static constexpr int BAR_OFF = STAT_OFF + 2 * 2 * BQ * 4;
     // kv_full, q_full[NSQ], q_empty[NSQ], s_full[2], p_full[2], dq_full[2], dq_empty[2],
-    // acc_full, epi, mma_done
-    static constexpr int NBARS = 1 + 2 * NSQ + 8 + 3;
+    // acc_full, epi, mma_done, kvd[2]
+    static constexpr int NBARS = 1 + 2 * NSQ + 8 + 3 + 2;
     static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
     static constexpr int ABORT_OFF = TMEM_OFF + 8;
     static constexpr int BYTES = ABORT_OFF + 8 + 1024;
@@ -151,6 +152,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t *acc_full = dq_empty + 2;
     uint64_t *epi = acc_full + 1;
     uint64_t *mma_done = epi + 1;
+    uint64_t *kvd = mma_done + 1;          // [2] dV / dK of the buffer's last step done
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::TMEM_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ABORT_OFF);
     float *stat = reinterpret_cast<float *>(smem + L::STAT_OFF);
@@ -218,7 +220,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         mbar_init(acc_full, 1);
         mbar_init(epi, 128);
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, 2);            // one commit from each issuer
+        mbar_init(&kvd[0], 1);
+        mbar_init(&kvd[1], 1);
         if (DROP) {
             uint64_t *kb = reinterpret_cast<uint64_t *>(smem + L::KM_BAR_OFF);
             for (int k = 0; k < 4; ++k) mbar_init(&kb[k], 128);
@@ -283,8 +287,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (T > 0) mbar_drain(kv_full, 0);
             }
         }
-    } else if (warp == WARP_MMA) {
-        // ------------------------------------------------------------------ MMA issuer
+    } else if (warp == WARP_MMA || warp == WARP_MMA2) {
+        // ------------------------------------------------------------------ MMA issuers
+        // Two threads issue: one the S^T / dP^T products of step s + 1 as soon as their buffer
+        // is free, the other this step's dQ^T, dV and dK as soon as the gradient warps are done,
+        // so neither stream queues behind the other in one thread.  The reuse of a buffer that
+        // one in-order stream would order by itself is ordered by barriers: S^T(s+2) waits for
+        // dV / dK(s) (kvd, P^T and dS^T are their operands) and for the drain's read of dQ^T(s).
         if (lane == 0) {
             constexpr uint32_t IDESC_SP = idesc_bf16(BKV, BQ, false, false);   // S^T, dP^T
             constexpr uint32_t IDESC_KV = idesc_bf16(BKV, DR, false, true);    // dV, dK
@@ -297,63 +306,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t dq_mn = sdesc_sw128(smem_u32(smem + L::QR_OFF), L::Q_CHUNK, 1024);  // ring, MN-major
             const uint64_t dds = sdesc_sw128(smem_u32(smem + L::DS_OFF), L::DS_BYTES, 1024);   // dS^T
             auto ring_off = [&](int s) { return static_cast<uint32_t>((s % NSQ) * 2 * L::Q_BYTES); };
-            // S^T(s) and dP^T(s) into buffer s & 1
-            auto issue_sp = [&](int s) {
-                const uint64_t dq = sdesc_add(dq_k, ring_off(s));
-                const uint64_t ddo = sdesc_add(dq, L::Q_BYTES);
-                const uint32_t buf = tmem + T_BUF + (s & 1) * 128;
-#pragma unroll
-                for (int kk = 0; kk < DR / 16; ++kk) {
-                    const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
-                    const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
-                    mma_ss(buf + B_ST, sdesc_add(dk_k, oa), sdesc_add(dq, ob), IDESC_SP, kk > 0);
-                }
-#pragma unroll
-                for (int kk = 0; kk < DR / 16; ++kk) {
-                    const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
-                    const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
-                    mma_ss(buf + B_DPT, sdesc_add(dv_k, oa), sdesc_add(ddo, ob), IDESC_SP, kk > 0);
-                }
-                mma_commit(&s_full[s & 1]);
-            };
-            bool ok = T > 0 && mbar_wait(kv_full, 0, abort_flag, status) &&
-                      mbar_wait(&q_full[0], 0, abort_flag, status);
-            tc_fence_after();
-            if (ok) issue_sp(0);
-            for (int s = 0; s < T && ok; ++s) {
-                const int bsel = s & 1;
-                const uint32_t buf = tmem + T_BUF + bsel * 128;
-                if (s + 1 < T) {
-                    if (!mbar_wait(&q_full[(s + 1) % NSQ], ((s + 1) / NSQ) & 1, abort_flag, status)) break;
-                    // buffer (s+1)&1 last held dQ^T(s-1): wait until the drain warps read it
-                    if (s >= 1 && !mbar_wait(&dq_empty[bsel ^ 1], ((s - 1) >> 1) & 1, abort_flag, status)) break;
+            bool ok = T > 0;
+            if (warp == WARP_MMA) {
+                // S^T(s) and dP^T(s) into buffer s & 1
+                ok = ok && mbar_wait(kv_full, 0, abort_flag, status);
+                for (int s = 0; s < T && ok; ++s) {
+                    const int bsel = s & 1;
+                    if (!mbar_wait(&q_full[s % NSQ], (s / NSQ) & 1, abort_flag, status)) break;
+                    if (s >= 2 && (!mbar_wait(&kvd[bsel], ((s - 2) >> 1) & 1, abort_flag, status) ||
+                                   !mbar_wait(&dq_empty[bsel], ((s - 2) >> 1) & 1, abort_flag, status)))
+                        break;
                     tc_fence_after();
-                    issue_sp(s + 1);
+                    const uint64_t dq = sdesc_add(dq_k, ring_off(s));
+                    const uint64_t ddo = sdesc_add(dq, L::Q_BYTES);
+                    const uint32_t buf = tmem + T_BUF + bsel * 128;
+#pragma unroll
+                    for (int kk = 0; kk < DR / 16; ++kk) {
+                        const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
+                        const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
+                        mma_ss(buf + B_ST, sdesc_add(dk_k, oa), sdesc_add(dq, ob), IDESC_SP, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < DR / 16; ++kk) {
+                        const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
+                        const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
+                        mma_ss(buf + B_DPT, sdesc_add(dv_k, oa), sdesc_add(ddo, ob), IDESC_SP, kk > 0);
+                    }
+                    mma_commit(&s_full[bsel]);
                 }
-                if (!mbar_wait(&p_full[bsel], (s >> 1) & 1, abort_flag, status)) break;
-                tc_fence_after();
-                // dQ^T = K^T dS^T first (A = K MN-major, B = dS^T MN-major, K dim = 128 keys), so
-                // the drain warps read it out while dV / dK run and buffer s&1 frees up early.
-                const uint64_t dsb = sdesc_add(dds, bsel * L::DS_BYTES);
+            } else {
+                for (int s = 0; s < T && ok; ++s) {
+                    const int bsel = s & 1;
+                    const uint32_t buf = tmem + T_BUF + bsel * 128;
+                    // the gradient warps have staged P^T / dS^T (and so S^T(s), dP^T(s) are done)
+                    if (!mbar_wait(&p_full[bsel], (s >> 1) & 1, abort_flag, status)) break;
+                    tc_fence_after();
+                    // dQ^T = K^T dS^T first (A = K MN-major, B = dS^T MN-major, K dim = 128 keys),
+                    // so the drain warps read it out while dV / dK run.
+                    const uint64_t dsb = sdesc_add(dds, bsel * L::DS_BYTES);
 #pragma unroll
-                for (int kk = 0; kk < BKV / 16; ++kk)
-                    mma_ss(buf + B_DQT, sdesc_add(dk_mn, kk * 2048), sdesc_add(dsb, kk * 2048),
-                           IDESC_DQ, kk > 0);
-                mma_commit(&dq_full[bsel]);
-                const uint64_t dqm = sdesc_add(dq_mn, ring_off(s));
-                const uint64_t dom = sdesc_add(dqm, L::Q_BYTES);
-                // dV += P^T dO ; dK += dS^T Q   (B operands MN-major: d contiguous)
+                    for (int kk = 0; kk < BKV / 16; ++kk)
+                        mma_ss(buf + B_DQT, sdesc_add(dk_mn, kk * 2048), sdesc_add(dsb, kk * 2048),
+                               IDESC_DQ, kk > 0);
+                    mma_commit(&dq_full[bsel]);
+                    const uint64_t dqm = sdesc_add(dq_mn, ring_off(s));
+                    const uint64_t dom = sdesc_add(dqm, L::Q_BYTES);
+                    // dV += P^T dO ; dK += dS^T Q   (B operands MN-major: d contiguous)
 #pragma unroll
-                for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + T_DV, buf + B_PT + kk * 8, sdesc_add(dom, kk * 2048), IDESC_KV,
-                           (s > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BQ / 16; ++kk)
+                        mma_ts(tmem + T_DV, buf + B_PT + kk * 8, sdesc_add(dom, kk * 2048), IDESC_KV,
+                               (s > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + T_DK, buf + B_DST + kk * 8, sdesc_add(dqm, kk * 2048), IDESC_KV,
-                           (s > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&q_empty[s % NSQ]);
+                    for (int kk = 0; kk < BQ / 16; ++kk)
+                        mma_ts(tmem + T_DK, buf + B_DST + kk * 8, sdesc_add(dqm, kk * 2048), IDESC_KV,
+                               (s > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&kvd[bsel]);
+                    mma_commit(&q_empty[s % NSQ]);
+                }
+                mma_commit(acc_full);
             }
-            mma_commit(acc_full);
+            // Nothing either issued may still be running when TMEM is released.
             mma_commit(mma_done);
             mbar_drain(mma_done, 0);
         }
