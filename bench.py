@@ -41,16 +41,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # fa_bwd on causal_n4096: bwd_main 1.917 GB read + 0.986 GB write, bwd_preprocess 0.206 GB,
     # bwd_dq_convert 0.160 GB
-    "fa_bwd_sm103a.cu:e220a8fee16b9454:causal_n4096": 3.27e9,
-    # fa_bwd at head dim 64: bwd_main 1.024 GB, bwd_preprocess 0.073 GB, bwd_dq_convert 0.069 GB
-    "fa_bwd_sm103a.cu:e220a8fee16b9454:causal_d64_n4096": 1.166e9,
+    "fa_bwd_sm103a.cu:2cc428e9de32c439:causal_n4096": 3.27e9,
+    # fa_bwd at head dim 64: bwd_main 0.997 GB, bwd_preprocess 0.073 GB, bwd_dq_convert 0.069 GB
+    "fa_bwd_sm103a.cu:2cc428e9de32c439:causal_d64_n4096": 1.139e9,
     # split forward on splitkv_n32768: 25.4 MB read + 0.2-0.5 MB write (partials stay in L2)
     "fa_fwd_sm103a.cu:13f6438b56253de0:splitkv_n32768": 2.59e7,
     # fa_bwd_masked, three kernels
-    "fa_bwd_sm103a.cu:e220a8fee16b9454:local_n16384": 0.994e9,
-    "fa_bwd_sm103a.cu:e220a8fee16b9454:varlen_n8192": 25.0e9,
+    "fa_bwd_sm103a.cu:2cc428e9de32c439:local_n16384": 0.996e9,
+    "fa_bwd_sm103a.cu:2cc428e9de32c439:varlen_n8192": 25.1e9,
     # fa_bwd_dropout, three kernels
-    "fa_bwd_sm103a.cu:e220a8fee16b9454:dropout_n4096": 3.45e9,
+    "fa_bwd_sm103a.cu:2cc428e9de32c439:dropout_n4096": 3.79e9,
     # key/value-outer forward
     "fa_fwd_kvouter_sm103a.cu:cf980aee93773e67:kvouter_n4096": 4.14e9,
     # fp32 tensor-core backward: split rows 0.343 GB, split transposes 0.239 GB, dq pass

@@ -25,8 +25,10 @@
 // the tensor core's work on the other.  Inside a buffer, P^T and dS^T (bf16) are both written over
 // the S^T half, which frees the dP^T half for the dQ^T product of the same step.
 //
-// Roles (384 threads): warps 0-3 softmax-gradient, warps 4-7 dQ drain, warp 8 TMA, warp 9 MMA,
-// warps 10-11 idle (they complete the third warpgroup for the register split).
+// Roles (384 threads): warps 0-3 softmax-gradient (and the dK / dV epilogue), warps 4-7 dQ drain
+// (at head dim 64 also the dV half of the epilogue), warp 8 TMA, warp 9 the S^T / dP^T MMAs and
+// warp 10 the dQ^T / dV / dK MMAs (one elected lane each), warp 11 idle (it completes the third
+// warpgroup for the register split).
 // TMEM (512 columns): dK [0,128), dV [128,256), buffer b at 256 + 128 b:
 //   [+0,+64) S^T -> P^T [+0,+32) and dS^T [+32,+64);  [+64,+128) dP^T -> dQ^T.
 #include <algorithm>
@@ -47,7 +49,7 @@ constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;       // TMEM allocator; issues S^T and dP^T
 constexpr int WARP_MMA2 = 10;     // issues dQ^T, dV and dK
 // Register split: softmax-gradient warpgroup grows; dQ drain and TMA/MMA warpgroups shrink.
-constexpr uint32_t REGS_GRAD = 256, REGS_DRAIN = 96, REGS_OTHER = 72;
+constexpr uint32_t REGS_GRAD = 256, REGS_DRAIN = 88, REGS_OTHER = 80;
 constexpr int REGS_NEEDED = 128 * (REGS_GRAD + REGS_DRAIN + REGS_OTHER);
 constexpr float LOG2E = 1.4426950408889634f;
 // Steps (query head of the group x query tile) a masked CTA can list in shared memory.
@@ -67,8 +69,8 @@ struct Layout {
     static constexpr int STAT_OFF = DS_OFF + 2 * DS_BYTES;     // [2][lse2 64 | D 64] fp32
     static constexpr int BAR_OFF = STAT_OFF + 2 * 2 * BQ * 4;
     // kv_full, q_full[NSQ], q_empty[NSQ], s_full[2], p_full[2], dq_full[2], dq_empty[2],
-    // acc_full, epi, mma_done, kvd[2]
-    static constexpr int NBARS = 1 + 2 * NSQ + 8 + 3 + 2;
+    // acc_full, mma_done, kvd[2]
+    static constexpr int NBARS = 1 + 2 * NSQ + 8 + 2 + 2;
     static constexpr int TMEM_OFF = BAR_OFF + NBARS * 8;
     static constexpr int ABORT_OFF = TMEM_OFF + 8;
     static constexpr int BYTES = ABORT_OFF + 8 + 1024;
@@ -104,6 +106,41 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+template <int W>
+__device__ __forceinline__ void tmem_ld_w(uint32_t taddr, uint32_t (&r)[W]) {
+    if constexpr (W == 32) tmem_ld_x32(taddr, r);
+    else if constexpr (W == 64) tmem_ld_x64(taddr, r);
+    else tmem_ld_x128(taddr, r);
+}
+
+// Epilogue of one fp32 accumulator (dK or dV) held in TMEM, thread = key row = TMEM lane:
+// row `row` times mul -> bf16 -> the 128B-swizzled [DR / 64][128 rows][64] tile at dst (the
+// layout of the K / V operand tiles, which the TMA store reads back).  W columns per TMEM load.
+template <int W, int DR>
+__device__ __forceinline__ void stage_acc_rows(uint32_t tsrc, float mul, uint8_t *dst, int row,
+                                               bool zero) {
+#pragma unroll
+    for (int c0 = 0; c0 < DR; c0 += W) {
+        uint32_t a[W];
+        tmem_ld_w<W>(tsrc + c0, a);
+        if (zero) {                                  // (a masked key block with no step)
+#pragma unroll
+            for (int k = 0; k < W; ++k) a[k] = 0u;
+        }
+#pragma unroll
+        for (int c = 0; c < W; c += 8) {
+            const int col = c0 + c;
+            uint4 w4;
+            w4.x = pack_bf16x2(__uint_as_float(a[c + 0]) * mul, __uint_as_float(a[c + 1]) * mul);
+            w4.y = pack_bf16x2(__uint_as_float(a[c + 2]) * mul, __uint_as_float(a[c + 3]) * mul);
+            w4.z = pack_bf16x2(__uint_as_float(a[c + 4]) * mul, __uint_as_float(a[c + 5]) * mul);
+            w4.w = pack_bf16x2(__uint_as_float(a[c + 6]) * mul, __uint_as_float(a[c + 7]) * mul);
+            uint8_t *rowp = dst + (col / 64) * (BKV * 128) + row * 128;
+            *reinterpret_cast<uint4 *>(rowp + ((((col % 64) / 8) ^ (row & 7)) << 4)) = w4;
+        }
+    }
+}
+
 template <bool CAUSAL>
 __device__ __forceinline__ int first_q_tile(int jb) {
     return CAUSAL ? (jb * BKV) / BQ : 0;
@@ -137,6 +174,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // At head dim 64 dQ leaves through bulk tensor reductions (see the drain warps); at 128 the
     // per-element reductions measured faster (a staged 64 x 128 tile: 0.944 ms against 0.917).
     constexpr bool DQ_TMA = DR == 64;
+    // The dK / dV epilogue: split between the gradient warps (dK) and the drain warps (dV) where
+    // the drain warps' per-step work is the short staged reduction (DR = 64); at DR = 128 the
+    // drain warps are still busy with the last step's per-element reductions then.
+    constexpr bool SPLIT_EPI = DQ_TMA;
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -150,8 +191,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t *dq_full = p_full + 2;        // [2]
     uint64_t *dq_empty = dq_full + 2;      // [2]
     uint64_t *acc_full = dq_empty + 2;
-    uint64_t *epi = acc_full + 1;
-    uint64_t *mma_done = epi + 1;
+    uint64_t *mma_done = acc_full + 1;
     uint64_t *kvd = mma_done + 1;          // [2] dV / dK of the buffer's last step done
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::TMEM_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ABORT_OFF);
@@ -206,7 +246,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) *reinterpret_cast<int *>(smem + L::LIST_OFF) = min(count, MAX_MASK_STEPS);
     }
 
-    if (threadIdx.x == 0) {
+    // The loads that depend on nothing: K / V of the block and, without a general mask (the step
+    // list then follows from the shape), Q / dO of the first ring stages, issued by the TMA
+    // thread right after it sets up the barriers, before TMEM allocation and the block barrier.
+    auto issue_kv = [&]() {
+        // K: both chunks (at DR = 64 the second is zero fill, the upper rows of dQ^T's A
+        // operand); V: only the real columns (its second chunk stages dQ at DR = 64)
+        mbar_arrive_expect_tx(kv_full, L::KV_BYTES + (DR / 64) * L::KV_CHUNK);
+        for (int ch = 0; ch < D / 64; ++ch)
+            tma_load_3d(smem + L::K_OFF + ch * L::KV_CHUNK, &tmK, ch * 64, jb * BKV, bkv, kv_full);
+        for (int ch = 0; ch < DR / 64; ++ch)
+            tma_load_3d(smem + L::V_OFF + ch * L::KV_CHUNK, &tmV, ch * 64, jb * BKV, bkv, kv_full);
+    };
+    auto issue_q = [&](int s, int g, int i) {
+        const int st = s % NSQ;
+        const int bhq = b * Hq + hk * G + g;
+        mbar_arrive_expect_tx(&q_full[st], 2 * (DR / 64) * L::Q_CHUNK);
+        uint8_t *qdst = smem + L::QR_OFF + st * 2 * L::Q_BYTES;
+        for (int ch = 0; ch < DR / 64; ++ch) {
+            tma_load_3d(qdst + ch * L::Q_CHUNK, &tmQ, ch * 64, i * BQ, bhq, &q_full[st]);
+            tma_load_3d(qdst + L::Q_BYTES + ch * L::Q_CHUNK, &tmdO, ch * 64, i * BQ, bhq, &q_full[st]);
+        }
+    };
+    const int early_q = MASK ? 0 : min(G * tiles_per_head, NSQ);
+    if (threadIdx.x == WARP_TMA * 32) {
         mbar_init(kv_full, 1);
         for (int s = 0; s < NSQ; ++s) {
             mbar_init(&q_full[s], 1);
@@ -219,7 +282,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&dq_empty[k], 128);
         }
         mbar_init(acc_full, 1);
-        mbar_init(epi, 128);
         mbar_init(mma_done, 2);            // one commit from each issuer
         mbar_init(&kvd[0], 1);
         mbar_init(&kvd[1], 1);
@@ -229,6 +291,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         *abort_flag = 0;
         fence_mbar_init();
+        if (!MASK) {
+            issue_kv();
+            for (int s = 0; s < early_q; ++s) issue_q(s, s / tiles_per_head, i0 + s % tiles_per_head);
+        }
     }
     if (warp == WARP_MMA) {
         tmem_alloc(tmem_holder, 512);
@@ -254,31 +320,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (warp == WARP_TMA) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmdO);
-            if (T > 0) {                            // (a masked key block may have no step)
-                // K: both chunks (at DR = 64 the second is zero fill, the upper rows of dQ^T's
-                // A operand); V: only the real columns (its second chunk stages dQ at DR = 64)
-                mbar_arrive_expect_tx(kv_full, L::KV_BYTES + (DR / 64) * L::KV_CHUNK);
-                for (int ch = 0; ch < D / 64; ++ch)
-                    tma_load_3d(smem + L::K_OFF + ch * L::KV_CHUNK, &tmK, ch * 64, jb * BKV, bkv, kv_full);
-                for (int ch = 0; ch < DR / 64; ++ch)
-                    tma_load_3d(smem + L::V_OFF + ch * L::KV_CHUNK, &tmV, ch * 64, jb * BKV, bkv, kv_full);
-            }
-            int issued = 0;
-            for (int s = 0; s < T; ++s) {
+            // (a masked key block may have no step; without a mask K / V and the first stages
+            // are already on their way)
+            if (MASK && T > 0) issue_kv();
+            int issued = early_q;
+            for (int s = early_q; s < T; ++s) {
                 const int st = s % NSQ, rnd = s / NSQ;
                 if (!mbar_wait(&q_empty[st], (rnd & 1) ^ 1, abort_flag, status)) break;
                 int g, i;
                 step_tile(s, g, i);
-                const int bhq = b * Hq + hk * G + g;
-                mbar_arrive_expect_tx(&q_full[st], 2 * (DR / 64) * L::Q_CHUNK);
-                uint8_t *qdst = smem + L::QR_OFF + st * 2 * L::Q_BYTES;
-                for (int ch = 0; ch < DR / 64; ++ch) {
-                    tma_load_3d(qdst + ch * L::Q_CHUNK, &tmQ, ch * 64, i * BQ, bhq, &q_full[st]);
-                    tma_load_3d(qdst + L::Q_BYTES + ch * L::Q_CHUNK, &tmdO, ch * 64, i * BQ, bhq,
-                                &q_full[st]);
-                }
+                issue_q(s, g, i);
                 ++issued;
             }
             if (*abort_flag) {
@@ -406,7 +457,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int s = 0; s < T; ++s) {
             int g, i;
             step_tile(s, g, i);
-            const int bhq = b * Hq + hk * G + g;
             const int q0 = i * BQ;
             const int bsel = s & 1;
             const uint32_t buf = tmem + lane_off + T_BUF + bsel * 128;
@@ -506,45 +556,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_arrive(&p_full[bsel]);
             }
         }
-        // epilogue: dK (scaled) and dV rows -> bf16 -> smem (over K / V) -> TMA store
+        // epilogue: scale * dK rows (and dV rows unless the drain warps take them) -> bf16 ->
+        // smem over K (V) -> TMA store.  The barrier is passed by all four warps whatever their
+        // wait returned, so its count always matches.
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, status));
         if (ok) {
             tc_fence_after();
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t tcol = which ? T_DV : T_DK;
-                const float mul = which ? 1.f : scale;
-                uint8_t *dst = smem + (which ? L::V_OFF : L::K_OFF);
-#pragma unroll
-                for (int c0 = 0; c0 < DR; c0 += 32) {
-                    uint32_t a[32];
-                    tmem_ld_x32(tmem + lane_off + tcol + c0, a);
-                    if (MASK && T == 0) {               // no step: TMEM was never written
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) a[k] = 0u;
-                    }
-                    uint8_t *rowp = dst + (c0 / 64) * L::KV_CHUNK + krow * 128;
-                    const int u0 = (c0 % 64) / 8;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        uint4 w4;
-                        w4.x = pack_bf16x2(__uint_as_float(a[8 * u + 0]) * mul, __uint_as_float(a[8 * u + 1]) * mul);
-                        w4.y = pack_bf16x2(__uint_as_float(a[8 * u + 2]) * mul, __uint_as_float(a[8 * u + 3]) * mul);
-                        w4.z = pack_bf16x2(__uint_as_float(a[8 * u + 4]) * mul, __uint_as_float(a[8 * u + 5]) * mul);
-                        w4.w = pack_bf16x2(__uint_as_float(a[8 * u + 6]) * mul, __uint_as_float(a[8 * u + 7]) * mul);
-                        *reinterpret_cast<uint4 *>(rowp + (((u0 + u) ^ (krow & 7)) << 4)) = w4;
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(epi);
-            if (krow == 0 && mbar_wait(epi, 0, abort_flag, status)) {
-                for (int ch = 0; ch < DR / 64; ++ch) {
-                    tma_store_3d(&tmdK, smem + L::K_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
+            stage_acc_rows<DR, DR>(tmem + lane_off + T_DK, scale, smem + L::K_OFF, krow, MASK && T == 0);
+            if constexpr (!SPLIT_EPI)
+                stage_acc_rows<DR, DR>(tmem + lane_off + T_DV, 1.f, smem + L::V_OFF, krow, MASK && T == 0);
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (ok && krow == 0 && !*abort_flag) {
+            for (int ch = 0; ch < DR / 64; ++ch) {
+                tma_store_3d(&tmdK, smem + L::K_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
+                if constexpr (!SPLIT_EPI)
                     tma_store_3d(&tmdV, smem + L::V_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
-                }
-                tma_store_commit_and_wait_read();
             }
+            tma_store_commit_and_wait_read();
         }
         tc_fence_before();
         __syncthreads();
@@ -587,29 +617,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_arrive(&km_full[s & 1]);
         };
         if (DROP && T > 0) make_keep(0);
-        for (int s = 0; s < T; ++s) {
-            if constexpr (DROP) {
-                // the keep words of the next step, into the buffer step s-1 has released
-                if (s + 1 < T) {
-                    const int sn = s + 1;
-                    if (sn >= 2 &&
-                        !__all_sync(0xffffffffu, mbar_wait(&km_empty[sn & 1], ((sn - 2) >> 1) & 1, abort_flag, status)))
-                        break;
-                    make_keep(sn);
+        if constexpr (DQ_TMA) {
+            // After a failed wait a warp keeps stepping without work, so the named barriers of the
+            // staged reductions always see both of their warps.
+            bool dok = true;
+            for (int s = 0; s < T; ++s) {
+                if constexpr (DROP) {
+                    // the keep words of the next step, into the buffer step s-1 has released
+                    if (s + 1 < T && dok) {
+                        const int sn = s + 1;
+                        if (sn >= 2)
+                            dok = __all_sync(0xffffffffu, mbar_wait(&km_empty[sn & 1], ((sn - 2) >> 1) & 1, abort_flag, status));
+                        if (dok) make_keep(sn);
+                    }
                 }
-            }
-            int g, i;
-            step_tile(s, g, i);
-            const int bhq = b * Hq + hk * G + g;
-            const int q0 = i * BQ;
-            const int bsel = s & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&dq_full[bsel], (s >> 1) & 1, abort_flag, status))) break;
-            tc_fence_after();
-            uint32_t a[64];
-            tmem_ld_x64(tmem + lane_off + T_BUF + bsel * 128 + B_DQT, a);
-            tc_fence_before();
-            mbar_arrive(&dq_empty[bsel]);
-            if constexpr (DQ_TMA) {
+                int g, i;
+                step_tile(s, g, i);
+                const int bhq = b * Hq + hk * G + g;
+                const int q0 = i * BQ;
+                const int bsel = s & 1;
+                if (dok) dok = __all_sync(0xffffffffu, mbar_wait(&dq_full[bsel], (s >> 1) & 1, abort_flag, status));
+                uint32_t a[64];
+                if (dok) {
+                    tc_fence_after();
+                    tmem_ld_x64(tmem + lane_off + T_BUF + bsel * 128 + B_DQT, a);
+                    tc_fence_before();
+                    mbar_arrive(&dq_empty[bsel]);
+                }
                 // The 64 x 64 tile of dQ (query rows, d columns) goes to the accumulator as one
                 // bulk reduction from shared memory, V's unused second chunk (per-element
                 // reductions measured 25% of the step's time at d = 64).  Rows past the sequence
@@ -621,18 +655,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (threadIdx.x == 128) bulk_wait_read();
                     named_barrier_sync(2, 64);
                     float *trow = tile + dcol;
+                    if (dok) {
 #pragma unroll
-                    for (int c = 0; c < BQ; ++c) trow[c * 64] = __uint_as_float(a[c]) * scale;
+                        for (int c = 0; c < BQ; ++c) trow[c * 64] = __uint_as_float(a[c]) * scale;
+                    }
                     fence_proxy_async_smem();
                     named_barrier_sync(2, 64);
-                    if (threadIdx.x == 128) tma_reduce_add_3d(&tmdQ, tile, 0, q0, bhq);
+                    if (threadIdx.x == 128 && dok && !*abort_flag) tma_reduce_add_3d(&tmdQ, tile, 0, q0, bhq);
                 }
-            } else {
+            }
+        } else {
+            // (no named barrier inside: a warp whose wait failed just leaves)
+            for (int s = 0; s < T; ++s) {
+                if constexpr (DROP) {
+                    // the keep words of the next step, into the buffer step s-1 has released
+                    if (s + 1 < T) {
+                        const int sn = s + 1;
+                        if (sn >= 2 &&
+                            !__all_sync(0xffffffffu, mbar_wait(&km_empty[sn & 1], ((sn - 2) >> 1) & 1, abort_flag, status)))
+                            break;
+                        make_keep(sn);
+                    }
+                }
+                int g, i;
+                step_tile(s, g, i);
+                const int bhq = b * Hq + hk * G + g;
+                const int q0 = i * BQ;
+                const int bsel = s & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&dq_full[bsel], (s >> 1) & 1, abort_flag, status))) break;
+                tc_fence_after();
+                uint32_t a[64];
+                tmem_ld_x64(tmem + lane_off + T_BUF + bsel * 128 + B_DQT, a);
+                tc_fence_before();
+                mbar_arrive(&dq_empty[bsel]);
                 float *dst = dQacc + (static_cast<size_t>(bhq) * N + q0) * DR + dcol;
                 const int nvalid = min(BQ, qend - q0);   // rows of this tile inside the sequence
 #pragma unroll
                 for (int c = 0; c < BQ; ++c)
                     if (c < nvalid) atomicAdd(dst + static_cast<size_t>(c) * DR, __uint_as_float(a[c]) * scale);
+            }
+        }
+        if constexpr (SPLIT_EPI) {
+            // epilogue, dV half: dV rows -> bf16 -> smem over V (its first DR / 64 chunks; at
+            // DR = 64 the second one is the dQ staging tile) -> TMA store.  Same barrier rule as
+            // the gradient warps' half.
+            const bool acc_ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, status));
+            if (acc_ok) {
+                tc_fence_after();
+                stage_acc_rows<32, DR>(tmem + lane_off + T_DV, 1.f, smem + L::V_OFF, dcol, MASK && T == 0);
+            }
+            fence_proxy_async_smem();
+            named_barrier_sync(3, 128);
+            if (acc_ok && threadIdx.x == 128 && !*abort_flag) {
+                for (int ch = 0; ch < DR / 64; ++ch)
+                    tma_store_3d(&tmdV, smem + L::V_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
+                tma_store_commit_and_wait_read();
             }
         }
         // the last bulk reductions have finished reading shared memory (and writing)
