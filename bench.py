@@ -51,6 +51,13 @@ NCU_TRAFFIC = {
     "fa_bwd_sm103a.cu:2cc428e9de32c439:varlen_n8192": 25.1e9,
     # fa_bwd_dropout, three kernels
     "fa_bwd_sm103a.cu:2cc428e9de32c439:dropout_n4096": 3.79e9,
+    # fa_bwd on gqa_n8192: bwd_main 0.645 + 0.279 GB, bwd_preprocess 0.206 GB, bwd_dq_convert
+    # 0.160 GB; on long_n32768: bwd_main 7.658 + 3.892 GB, bwd_preprocess 0.475 GB,
+    # bwd_dq_convert 0.354 GB
+    "fa_bwd_sm103a.cu:2cc428e9de32c439:gqa_n8192": 1.290e9,
+    "fa_bwd_sm103a.cu:2cc428e9de32c439:long_n32768": 12.38e9,
+    # forward at head dim 64 on fwd_d64: 25.2 MB read (Q, K, V), O written back from L2 later
+    "fa_fwd_sm103a.cu:13f6438b56253de0:fwd_d64": 2.52e7,
     # key/value-outer forward
     "fa_fwd_kvouter_sm103a.cu:cf980aee93773e67:kvouter_n4096": 4.14e9,
     # fp32 tensor-core backward: split rows 0.343 GB, split transposes 0.239 GB, dq pass
@@ -754,8 +761,10 @@ def main():
                 "fwd_tflops": fwd_achieved,
                 "fwd_frac_of_peak": fwd_achieved / peak,
                 "fwd_bwd_frac_of_peak": value / ws / peak if w.backward else None,
-                "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps,
+                # (not measured under --no-extras: null rather than NaN, which is not JSON)
+                "e2e": {"value": None if math.isnan(e2e_ms) else e2e_value, "unit": "TFLOP/s",
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                        "ms_per_step": None if math.isnan(e2e_ms) else e2e_ms / args.steps,
                         "pipeline": "host-to-device copy of step k+1 and device-to-host copy "
                                     "of step k-1 overlap step k (two device buffer sets, copy "
                                     "streams); first and last copies inside the timed region"},
