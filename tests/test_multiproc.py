@@ -64,3 +64,24 @@ def test_single_rank_helpers():
     assert bench.max_over_ranks(3.5, 1, None) == 3.5
     assert bench.replica_seed_offset(3) == 3
     assert abs(bench.whole_job_tflops(1, 2e12, 4, 8.0) - 1000.0) < 1e-9
+
+
+def test_split_key_ranges_partition_the_keys():
+    """The merge-traffic accounting assumes the split forward's ranges: ceil(nb / S) 128-key
+    blocks per range, the last ones possibly short or empty, together exactly [0, N)."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    for N in (1, 127, 128, 129, 1000, 4096, 32768):
+        for S in (1, 2, 3, 4, 7, 64):
+            r = bench.split_key_ranges(N, S)
+            assert len(r) == S
+            nb = -(-N // 128)
+            per = -(-nb // S)
+            pos = 0
+            for s, (k0, k1) in enumerate(r):
+                assert k0 == min(N, s * per * 128) and k1 == min(N, (s + 1) * per * 128)
+                assert k0 == pos or k1 == k0
+                assert k0 % 128 == 0 or k0 == N
+                pos = max(pos, k1)
+            assert pos == N
