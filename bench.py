@@ -33,7 +33,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOAD = "causal_n4096"
+# The other full-size causal d = 128 workloads, timed the same way in the same run (extra keys).
+OTHER_WORKLOADS = ("gqa_n8192", "long_n32768")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GB300's nominal dense bf16 tensor rate (datasheet), reported beside the measured peak.
+NOMINAL_BF16_TFLOPS = 2250.0
+# ex2.approx results per clock per SM (MUFU), measured with a single-SM probe on this GPU; the
+# forward and backward each evaluate one exponential per allowed (query, key) pair.
+MUFU_EX2_PER_CLK_PER_SM = 32.0
 
 # DRAM traffic per launch of the reported kernel from one ncu capture, keyed by
 # "<kernel file>:<sha256 prefix of that file and the device headers it includes>:<workload>";
@@ -185,6 +192,95 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(under) if under else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
                 "samples": len(mine)}
+
+
+def cpu_info() -> dict:
+    """Host CPU model, logical cores and OMP_NUM_THREADS, for the oracle's timings."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith(("model name", "cpu part")):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return {"cpu_model": model, "machine": platform.machine(), "logical_cores": os.cpu_count(),
+            "omp_num_threads": os.environ.get("OMP_NUM_THREADS")}
+
+
+def ex2_ceiling(exps: float, flops: float, ms: float, sm_mhz, num_sms: int) -> dict:
+    """The MUFU exponential ceiling of a pass: its exponentials at MUFU_EX2_PER_CLK_PER_SM on
+    every SM at the sampled SM clock, as a time floor and as the TFLOP/s that floor allows."""
+    mhz = float(sm_mhz) if sm_mhz else 2070.0
+    rate = MUFU_EX2_PER_CLK_PER_SM * num_sms * mhz * 1e6
+    floor_ms = exps / rate * 1e3
+    return {"exps_per_launch": exps, "rate_per_clk_per_sm": MUFU_EX2_PER_CLK_PER_SM,
+            "sm_mhz": mhz, "sms": num_sms, "time_floor_ms": floor_ms,
+            "ceiling_tflops": flops / (floor_ms * 1e-3) / 1e12,
+            "share_of_launch": floor_ms / ms if ms else None}
+
+
+def time_plain_workload(name: str, steps: int, warmup: int, dev, peak: float) -> dict:
+    """fa_fwd then fa_bwd on one of the plain causal workloads, CUDA events around every pass of
+    `steps` timed steps after `warmup` untimed ones (the same timing as the main line)."""
+    import torch
+
+    from exact_attention_89_gb300 import flashattn as fa
+    from exact_attention_89_gb300.inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS[name]
+    Qh, Kh, Vh, dOh = workload_inputs(w)
+    q, k, v, do = (t.to(dev) for t in (Qh, Kh, Vh, dOh))
+    O, LSE = torch.empty_like(q), torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsp = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.Hq, w.N, w.d), dtype=torch.uint8,
+                      device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        fa.fa_fwd(q, k, v, O, LSE, w.causal, w.scale)
+
+    def bwd():
+        fa.fa_bwd(q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wsp)
+
+    for _ in range(max(3, warmup)):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        fwd()
+        e1.record(stream)
+        bwd()
+        e2.record(stream)
+    torch.cuda.synchronize()
+    st = fa.fa_get_device_status()
+    if st != fa.FA_OK:
+        raise RuntimeError("device status after %s: %s" % (name, fa.fa_status_string(st)))
+    fwd_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / steps
+    bwd_ms = sum(b.elapsed_time(c) for _, b, c in ev) / steps
+    ff, fb = w.flops_fwd(), w.flops_bwd()
+    fwd_t = ff / (fwd_ms * 1e-3) / 1e12
+    tot_t = (ff + fb) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12
+    return {"config": {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+                       "causal": w.causal, "seed": w.seed, "q_mult": w.q_mult},
+            "steps": steps, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "fwd_tflops": fwd_t, "bwd_tflops": fb / (bwd_ms * 1e-3) / 1e12,
+            "fwd_bwd_tflops": tot_t,
+            "fwd_frac_of_peak": fwd_t / peak, "fwd_bwd_frac_of_peak": tot_t / peak,
+            "fwd_frac_of_nominal_peak": fwd_t / NOMINAL_BF16_TFLOPS,
+            "fwd_bwd_frac_of_nominal_peak": tot_t / NOMINAL_BF16_TFLOPS}
 
 
 def dist_env():
@@ -342,6 +438,97 @@ def cpu_oracle_sample(w, budget_s: float, max_heads: int, inputs=None, first_gro
             "seconds": t_total, "heads": heads_done}
 
 
+TABLE_CONFIGS = ("tiny_fp32", "fwd_d64", "causal_n4096", "gqa_n8192", "long_n32768")
+
+
+def oracle_table_rows(names, c5_groups: int = 1):
+    """The fp64 oracle timed on the host cores, forward and backward separately, per workload:
+    every head / KV group, except the N = 32768 workload, which is timed on whole KV groups and
+    extrapolated linearly (groups are independent and equal work).  Its forward runs row by row
+    (a whole N x N probability matrix per head would take 8.6 GB); its backward is the row pass
+    for dQ plus the key-column pass for dK / dV.  The backward of the full-size functions
+    recomputes P, O and D itself, as the oracle's backward does."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from exact_attention_89_gb300.inputs import WORKLOADS, workload_inputs
+    rows_out = []
+    for name in names:
+        w = WORKLOADS[name]
+        Q, K, V, dO = workload_inputs(w)
+        f = lambda t: t.to(torch.float64).numpy()
+        G = w.Hq // w.Hkv
+        n_groups = w.B * w.Hkv
+        def mean_time(fn):
+            # repeated up to half a second, so the small workloads are not timer noise
+            n, t = 0, 0.0
+            while t < 0.5 or n == 0:
+                t0 = time.perf_counter()
+                fn()
+                t += time.perf_counter() - t0
+                n += 1
+            return t / n
+
+        if w.N <= 8192:
+            q, k, v = f(Q), f(K), f(V)
+            t_fwd = mean_time(lambda: oracle.forward(q, k, v, w.causal, w.scale))
+            t_bwd = None
+            if w.backward:
+                do = f(dO)
+                t_bwd = mean_time(lambda: oracle.backward(q, k, v, do, w.causal, w.scale))
+            timed, extrap = n_groups, 1.0
+        else:
+            t_fwd, t_bwd = 0.0, 0.0
+            timed = min(c5_groups, n_groups)
+            for bk in range(timed):
+                b, hk = divmod(bk, w.Hkv)
+                sl = slice(hk * G, (hk + 1) * G)
+                q, k, v = f(Q[b:b + 1, sl]), f(K[b:b + 1, hk:hk + 1]), f(V[b:b + 1, hk:hk + 1])
+                do = f(dO[b:b + 1, sl])
+                rows = np.arange(G * w.N, dtype=np.int64)
+                cols = np.arange(w.N, dtype=np.int64)
+                t0 = time.perf_counter()
+                oracle.forward_rows(q, k, v, w.causal, w.scale, rows)
+                t_fwd += time.perf_counter() - t0
+                t0 = time.perf_counter()
+                oracle.backward_dq_rows(q, k, v, do, w.causal, w.scale, rows)
+                oracle.backward_dkv_cols(q, k, v, do, w.causal, w.scale, cols)
+                t_bwd += time.perf_counter() - t0
+            extrap = n_groups / timed
+            t_fwd *= extrap
+            t_bwd *= extrap
+        ff, fb = w.flops_fwd(), (w.flops_bwd() if w.backward else None)
+        rows_out.append({
+            "workload": name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+            "causal": w.causal, "dtype": "fp32 inputs" if w.dtype == torch.float32 else "bf16 inputs",
+            "threads": oracle.num_threads(),
+            "fwd_s": t_fwd, "fwd_gflops": ff / t_fwd / 1e9,
+            "bwd_s": t_bwd, "bwd_gflops": (fb / t_bwd / 1e9) if t_bwd else None,
+            "groups_timed": "%d of %d" % (timed, n_groups),
+            "extrapolated": extrap != 1.0})
+    return rows_out
+
+
+def run_oracle_table(args):
+    """Prints one JSON object: the oracle's forward and backward times per workload on all host
+    cores, and on one core for the two small workloads (a child process with
+    OMP_NUM_THREADS=1)."""
+    names = [n for n in args.oracle_table.split(",") if n] if args.oracle_table != "all" else \
+        list(TABLE_CONFIGS)
+    out = {"cpu": cpu_info(), "rows": oracle_table_rows(names)}
+    if args.oracle_table == "all":
+        env = dict(os.environ, OMP_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--impl", "reference",
+                            "--oracle-table", "tiny_fp32,fwd_d64"], env=env,
+                           capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("single-thread oracle timing failed:\n" + r.stderr[-2000:])
+        out["single_thread"] = json.loads(r.stdout.strip().splitlines()[-1])
+    print(json.dumps(out))
+    return 0
+
+
 def run_reference(args):
     """The reference arm: the fp64 oracle as it stands, on the host cores, same metric."""
     ws, rank, _ = dist_env()
@@ -390,7 +577,12 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="only warm-up and timed steps (no clock load, e2e or cpu baseline); "
                          "for profiler runs")
+    ap.add_argument("--oracle-table", default=None,
+                    help="with --impl reference: time the oracle's forward and backward per "
+                         "workload ('all' or a comma-separated list) instead of the bench line")
     args = ap.parse_args()
+    if args.impl == "reference" and args.oracle_table:
+        return run_oracle_table(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.warmup < 3:
@@ -647,6 +839,21 @@ def main():
     # ---------------------------------------------------------------- roofline + cpu baseline
     peaks, peaks_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    # the other full-size causal d = 128 workloads, when the main one is the default
+    others = None
+    if w.name == WORKLOAD and not args.no_extras:
+        others = {}
+        for name in OTHER_WORKLOADS:
+            others[name] = time_plain_workload(name, args.steps, args.warmup, dev, peak)
+            torch.cuda.empty_cache()
+        if ws > 1:
+            for r in others.values():
+                for key in ("fwd_ms", "bwd_ms"):
+                    r[key] = max_over_ranks(r[key], ws, dev)
+    # one exponential per allowed (query, key) pair in each pass
+    exps = (allowed_pairs(w, ql_h, kl_h, bm_h) if masked else
+            w.B * w.Hq * w.N * w.N / (2.0 if w.causal else 1.0))
     fwd_key = kernel_sources_hash("fa_fwd_sm103a.cu") + ":" + w.name
     bwd_key = kernel_sources_hash("fa_bwd_sm103a.cu") + ":" + w.name
     peak_source = ("%s burst bf16 (MEASURED_PEAKS.json)" % peaks_src if peaks_src == "measured"
@@ -700,7 +907,11 @@ def main():
                     "flops_per_launch": flops_bwd,
                     "fwd": {"kernel": fname, "achieved": fwd_achieved,
                             "frac": fwd_achieved / peak, "ms": first_ms,
-                            "flops_per_launch": flops_fwd},
+                            "flops_per_launch": flops_fwd,
+                            "mufu_ex2": ex2_ceiling(exps, flops_fwd, first_ms,
+                                                    (clocks or {}).get("sm_mhz"), num_sms)},
+                    "mufu_ex2": ex2_ceiling(exps, flops_bwd, second_ms,
+                                            (clocks or {}).get("sm_mhz"), num_sms),
                     "bwd_ms": second_ms, "sources": bwd_key}
     else:
         roofline = {"bound": "tensor",
@@ -728,6 +939,8 @@ def main():
     if rank == 0 and ws == 1 and args.cpu_budget > 0 and not args.no_extras:
         r = cpu_oracle_sample(w, args.cpu_budget, w.B * w.Hq)
         cpu = {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        ci = cpu_info()
+        cpu.update(cpu_model=ci["cpu_model"], omp_num_threads=ci["omp_num_threads"])
 
     if rank == 0:
         if w.backward:
@@ -761,6 +974,12 @@ def main():
                 "fwd_tflops": fwd_achieved,
                 "fwd_frac_of_peak": fwd_achieved / peak,
                 "fwd_bwd_frac_of_peak": value / ws / peak if w.backward else None,
+                # the same fractions against the nominal dense bf16 rate of the datasheet
+                "nominal_peak_tflops": NOMINAL_BF16_TFLOPS,
+                "fwd_frac_of_nominal_peak": fwd_achieved / NOMINAL_BF16_TFLOPS,
+                "fwd_bwd_frac_of_nominal_peak": (value / ws / NOMINAL_BF16_TFLOPS
+                                                 if w.backward else None),
+                "other_workloads": others,
                 # (not measured under --no-extras: null rather than NaN, which is not JSON)
                 "e2e": {"value": None if math.isnan(e2e_ms) else e2e_value, "unit": "TFLOP/s",
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -771,6 +990,7 @@ def main():
                 "gpu_launches": args.steps * (
                     (2 if split or w.tensor_fp32 else 1) +
                     ((4 if w.tensor_fp32 else 3) if w.backward else 0)),
+                "gpu_launches_other_workloads": (4 * args.steps * len(others)) if others else 0,
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks}
         print(json.dumps(line))
     if ws > 1:

@@ -25,6 +25,7 @@ struct DeviceInfo {
     bool probed = false;
     bool sm103 = false;
     unsigned *status = nullptr;
+    unsigned long long ctx_id = 0;   // context the status address belongs to
 };
 
 std::mutex g_mutex;
@@ -36,12 +37,54 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
-// Current device's entry, probed once.  Returns FA_OK or the reason it cannot run.
+// Driver entry points behind current_context_id (looked up once through the runtime, so the
+// library needs no link against libcuda).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+std::mutex g_ctx_mutex;
+
+void *driver_entry(const char *name) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return fn;
+}
+
+}  // namespace
+
+fa_status current_context_id(unsigned long long *id) {
+    {
+        std::lock_guard<std::mutex> lock(g_ctx_mutex);
+        if (!g_ctx_get_current || !g_ctx_get_id) {
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(driver_entry("cuCtxGetCurrent"));
+            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(driver_entry("cuCtxGetId"));
+            if (!g_ctx_get_current || !g_ctx_get_id) return FA_ERR_CUDA;
+        }
+    }
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return FA_ERR_CUDA;
+    *id = 0;
+    if (ctx != nullptr && g_ctx_get_id(ctx, id) != CUDA_SUCCESS) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+namespace {
+
+// Current device's entry, probed once per context.  Returns FA_OK or the reason it cannot run.
 fa_status current_device(DeviceInfo **out, bool need_sm103) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceInfo &di = g_dev[dev];
+    // A device reset (or the primary context being released and created again) invalidates the
+    // cached status address: look it up again in the new context.
+    unsigned long long ctx = 0;
+    if (current_context_id(&ctx) != FA_OK) return FA_ERR_CUDA;
+    if (di.probed && (ctx == 0 || ctx != di.ctx_id)) di.probed = false;
     if (!di.probed) {
         int major = 0, minor = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -51,6 +94,8 @@ fa_status current_device(DeviceInfo **out, bool need_sm103) {
         if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return FA_ERR_CUDA;
         di.status = static_cast<unsigned *>(p);
         di.sm103 = (major == 10 && minor == 3);
+        // the symbol lookup made the device's context current: remember which one it was
+        if (current_context_id(&di.ctx_id) != FA_OK || di.ctx_id == 0) return FA_ERR_CUDA;
         di.probed = true;
     }
     if (need_sm103 && !di.sm103) return FA_ERR_UNSUPPORTED;
@@ -160,8 +205,12 @@ const char *fa_status_string(fa_status s) {
 
 size_t fa_bwd_workspace_bytes(int B, int Hq, int N, int d) {
     if (B < 1 || Hq < 1 || N < 1 || d < 1) return 0;
-    const size_t rows = static_cast<size_t>(B) * Hq * N;
-    return fa::align256(rows * sizeof(float)) + rows * d * sizeof(float);
+    // rows * (d + 1) * 4 + 255 must fit in size_t, or no workspace check could be trusted
+    const size_t rows = static_cast<size_t>(B) * Hq;   // < 2^62: both factors are below 2^31
+    const size_t limit = (SIZE_MAX - 256) / 4 / (static_cast<size_t>(d) + 1);
+    if (rows > limit / static_cast<size_t>(N)) return SIZE_MAX;
+    const size_t r = rows * static_cast<size_t>(N);
+    return fa::align256(r * sizeof(float)) + r * static_cast<size_t>(d) * sizeof(float);
 }
 
 fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int Hq,

@@ -324,15 +324,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // are already on their way)
             if (MASK && T > 0) issue_kv();
             int issued = early_q;
+            bool injected = false;
             for (int s = early_q; s < T; ++s) {
                 const int st = s % NSQ, rnd = s / NSQ;
                 if (!mbar_wait(&q_empty[st], (rnd & 1) ^ 1, abort_flag, status)) break;
+#ifdef FA_FAULT_INJECT
+                // Test builds only: CTA 0 stops delivering Q / dO after the ring's first fill, so
+                // the S^T / dP^T issuer's bounded wait runs out, every role unwinds and
+                // FA_ERR_DEVICE_TIMEOUT is recorded.
+                if (blockIdx.x == 0 && s == NSQ) {
+                    injected = true;
+                    break;
+                }
+#endif
                 int g, i;
                 step_tile(s, g, i);
                 issue_q(s, g, i);
                 ++issued;
             }
-            if (*abort_flag) {
+            if (*abort_flag || injected) {
                 for (int s = max(0, issued - NSQ); s < issued; ++s)
                     mbar_drain(&q_full[s % NSQ], (s / NSQ) & 1);
                 if (T > 0) mbar_drain(kv_full, 0);

@@ -12,6 +12,10 @@ namespace fa {
 // Number of SMs of the current device (cached per device).
 int num_sms();
 
+// Unique id (cuCtxGetId) of the calling thread's current CUDA context, 0 when none is current.
+// Device addresses cached per device are tied to the context they were looked up in.
+fa_status current_context_id(unsigned long long *id);
+
 // Problem description after host validation.
 struct Problem {
     int B, Hq, Hkv, N, d, causal;

@@ -9,13 +9,15 @@
 // device memory on every GPU that loads the library, for as long as the library stays loaded.
 //
 // Host code must not use the array's name as a device address: on the host it names a
-// stand-in object.  The device address is looked up once per device with
-// cudaGetSymbolAddress (with that device current) and cached.
+// stand-in object.  The device address is looked up with cudaGetSymbolAddress (with the device
+// current) on the first call on each device and cached; it is looked up again when the device's
+// context has changed since (after cudaDeviceReset, the array lives in a new context).
 #include <cstdint>
 #include <mutex>
 
 #include <cuda_runtime.h>
 
+#include "fa_internal.h"
 #include "flashattn.h"
 
 namespace {
@@ -25,17 +27,24 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRA
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void *g_noalloc_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {0};   // context each cached address belongs to
 
-// Device address of the scratch array on the current device (looked up on first use).
+// Device address of the scratch array on the current device (looked up on first use, and again
+// in a new context).
 fa_status noalloc_scratch(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    unsigned long long ctx = 0;
+    if (fa::current_context_id(&ctx) != FA_OK) return FA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (g_noalloc_ptr[dev] == nullptr) {
+    if (g_noalloc_ptr[dev] == nullptr || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
             return FA_ERR_CUDA;
+        // the lookup made the device's context current: remember which one it was
+        if (fa::current_context_id(&ctx) != FA_OK || ctx == 0) return FA_ERR_CUDA;
         g_noalloc_ptr[dev] = p;
+        g_noalloc_ctx[dev] = ctx;
     }
     *out = g_noalloc_ptr[dev];
     return FA_OK;

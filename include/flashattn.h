@@ -201,7 +201,8 @@ fa_status fa_merge(const float *O_parts, const float *LSE_parts, int num_parts, 
 
 /*
  * Bytes of device workspace fa_bwd and fa_bwd_fp32 need: D [B,Hq,N] fp32 followed (at a
- * 256-byte boundary) by the fp32 dQ accumulator [B,Hq,N,d].  Returns 0 for invalid sizes.
+ * 256-byte boundary) by the fp32 dQ accumulator [B,Hq,N,d].  Returns 0 for invalid sizes and
+ * SIZE_MAX when the size does not fit in size_t (no workspace can then pass the size checks).
  */
 size_t fa_bwd_workspace_bytes(int B, int Hq, int N, int d);
 
@@ -239,7 +240,9 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
  *   exceeds FA_NOALLOC_SCRATCH_BYTES (with d = 128 that is B*Hq*N above about 130,000 rows).
  *   It calls no allocation routine.  The first call on a device looks up the array's device
  *   address (cudaGetSymbolAddress, on the current device); make that first call before any
- *   stream capture.
+ *   stream capture.  The lookup is repeated in the first call after the device's context has
+ *   changed (cudaDeviceReset, or the primary context released and created again), so the
+ *   address never outlives its context; the array's contents do not survive such a reset.
  *   All calls on one device share the array.  Each call rewrites what it needs at its start,
  *   so what an earlier call left there does not matter, but calls that overlap on the GPU
  *   (other streams, other host threads) race on the array and give wrong results: order them.

@@ -66,3 +66,40 @@ def sample_rows(B, H, N, n, seed):
                 rows.append(int(bh) * N + i)
     rows += rng.integers(0, B * H * N, size=n).tolist()
     return np.unique(np.asarray(rows, dtype=np.int64))
+
+
+def chosen_groups(n_groups, k, seed):
+    """k distinct (batch * KV head) group indices out of n_groups, drawn with a seeded generator
+    (for workloads whose every group is too slow for the oracle)."""
+    rng = np.random.default_rng(seed)
+    return sorted(int(g) for g in rng.choice(n_groups, size=min(k, n_groups), replace=False))
+
+
+class ErrorTally:
+    """Running max / mean absolute error and relative Frobenius error over chunks of a tensor,
+    so a full-size comparison can run the oracle a few heads at a time."""
+
+    def __init__(self):
+        self.max_abs = 0.0
+        self.abs_sum = 0.0
+        self.count = 0
+        self.diff_sq = 0.0
+        self.ref_sq = 0.0
+
+    def add(self, got, ref):
+        g, r = _np(got), _np(ref)
+        diff = g - r
+        self.max_abs = max(self.max_abs, float(np.max(np.abs(diff))) if diff.size else 0.0)
+        self.abs_sum += float(np.sum(np.abs(diff)))
+        self.count += diff.size
+        self.diff_sq += float(np.sum(diff * diff))
+        self.ref_sq += float(np.sum(r * r))
+
+    @property
+    def mean_abs(self):
+        return self.abs_sum / max(self.count, 1)
+
+    @property
+    def rel_fro(self):
+        floor = 1e-3 * np.sqrt(max(self.count, 1))
+        return float(np.sqrt(self.diff_sq) / max(np.sqrt(self.ref_sq), floor))

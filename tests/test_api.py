@@ -44,6 +44,16 @@ def test_workspace_bytes(built_lib):
     assert f(2, 32, 4096, 128) == ((rows * 4 + 255) // 256) * 256 + rows * 128 * 4
     assert f(1, 1, 1, 1) == 256 + 4
     assert f(0, 1, 1, 1) == 0 and f(1, 1, -1, 64) == 0
+    # sizes whose byte count does not fit in size_t give SIZE_MAX, never a wrapped small value
+    big = 2 ** 31 - 1
+    assert f(big, big, big, 128) == 2 ** 64 - 1
+    assert f(big, big, big, big) == 2 ** 64 - 1
+    assert f(big, big, 1, 1) == 2 ** 64 - 1          # 8 * (2^31 - 1)^2 bytes > 2^64
+    assert f(big, 4, 1, 1) == ((big * 4 * 4 + 255) // 256) * 256 + big * 4 * 4
+    L = built_lib.lib()
+    # ... so the backward's workspace check rejects every buffer for them
+    st = L.fa_bwd_noalloc(*([A] * 9), big, 2, 2, big, 128, 1, 0.088, None)
+    assert st == built_lib.FA_ERR_WORKSPACE
 
 
 def fwd(L, Q=A, K=A, V=A, O=A, LSE=A, B=1, Hq=2, Hkv=1, N=64, d=128, causal=1, scale=0.1, fp32=False):

@@ -2,15 +2,17 @@
 
 Tolerance: relative Frobenius error <= 2e-2 for each of dQ, dK, dV.  The GPU backward consumes
 the GPU forward's O and LSE (as a user would); the oracle recomputes everything in fp64 from the
-same bf16 inputs.  Full-size workloads are checked on one whole (batch, KV-group) slice (N <= 8192)
-and on sampled dQ rows and dK/dV rows computed by the oracle one by one."""
+same bf16 inputs.  Full-size workloads up to N = 8192 are checked over every element; the
+N = 32768 workload over every dQ, dK and dV element of four whole KV groups drawn by seed plus
+dQ rows sampled over all heads."""
 import numpy as np
 import pytest
 import torch
 
 import helpers
 from exact_attention_89_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
-from helpers import BF16_GRAD_REL_FRO, f64, group_slice, rel_fro, sample_rows
+from helpers import (BF16_GRAD_REL_FRO, ErrorTally, chosen_groups, f64, group_slice, rel_fro,
+                     sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -59,27 +61,59 @@ def test_backward_invariants_on_gpu(flash):
     assert float(dK.double().sum(2).abs().max()) <= 0.05 * float(dK.double().abs().sum(2).max())
 
 
-@pytest.mark.parametrize("name", ["causal_n4096", "gqa_n8192", "long_n32768",
-                                  "causal_d64_n4096"])
-def test_backward_full_size_workloads(flash, oracle_mod, name):
+# Workloads whose every element the oracle checks (a few KV groups per oracle call), and the
+# one too long for that: its check covers whole KV groups drawn by seed.
+EVERY_ELEMENT = ["causal_n4096", "gqa_n8192", "causal_d64_n4096"]
+WHOLE_GROUPS = {"long_n32768": 4}
+
+
+@pytest.mark.parametrize("name", EVERY_ELEMENT)
+def test_backward_full_size_every_element(flash, oracle_mod, name):
+    """Full-size workloads in the launch configuration the benchmark times: every element of dQ,
+    dK and dV against the oracle, which runs a few KV groups at a time."""
     w = WORKLOADS[name]
     Q, K, V, dO = workload_inputs(w)
     dQ, dK, dV = gpu_fwd_bwd(flash, Q, K, V, dO, w.causal, w.scale)
     G = w.Hq // w.Hkv
-    b, hk = 0, w.Hkv - 1
-    q, k, v, do = (f64(t) for t in group_slice(Q, K, V, dO, b, hk))
-    if w.N <= 8192:
-        ref = oracle_mod.backward(q, k, v, do, w.causal, w.scale)
-        got = (dQ[b:b + 1, hk * G:(hk + 1) * G].reshape(ref[0].shape),
-               dK[b:b + 1, hk:hk + 1].reshape(ref[1].shape),
-               dV[b:b + 1, hk:hk + 1].reshape(ref[2].shape))
-        assert_grads_close(got, ref, name + " group")
-    # sampled rows of the same group (sub-problem indices) and across all heads for dQ
-    rows = sample_rows(1, G, w.N, 48, seed=w.seed)
-    dq_ref = oracle_mod.backward_dq_rows(q, k, v, do, w.causal, w.scale, rows)
-    dq_got = dQ[b:b + 1, hk * G:(hk + 1) * G].reshape(-1, w.d)[rows]
-    cols = sample_rows(1, 1, w.N, 48, seed=w.seed + 1)
-    dk_ref, dv_ref = oracle_mod.backward_dkv_cols(q, k, v, do, w.causal, w.scale, cols)
-    dk_got = dK[b:b + 1, hk:hk + 1].reshape(-1, w.d)[cols]
-    dv_got = dV[b:b + 1, hk:hk + 1].reshape(-1, w.d)[cols]
-    assert_grads_close((dq_got, dk_got, dv_got), (dq_ref, dk_ref, dv_ref), name + " rows")
+    q64, k64, v64, do64 = f64(Q), f64(K), f64(V), f64(dO)
+    dQg = dQ.reshape(w.B * w.Hkv, G, w.N, w.d)
+    dKg, dVg = dK.reshape(w.B * w.Hkv, w.N, w.d), dV.reshape(w.B * w.Hkv, w.N, w.d)
+    tq, tk, tv = ErrorTally(), ErrorTally(), ErrorTally()
+    step = max(1, 8 // G)
+    for g0 in range(0, w.B * w.Hkv, step):
+        groups = list(range(g0, min(g0 + step, w.B * w.Hkv)))
+        rq, rk, rv = oracle_mod.backward(q64, k64, v64, do64, w.causal, w.scale, groups=groups)
+        tq.add(dQg[groups], rq)
+        tk.add(dKg[groups], rk)
+        tv.add(dVg[groups], rv)
+    errs = (tq.rel_fro, tk.rel_fro, tv.rel_fro)
+    print("[parity] %s backward, every element: rel fro dQ %.3e dK %.3e dV %.3e" % ((name,) + errs))
+    assert tq.count == w.B * w.Hq * w.N * w.d and tk.count == w.B * w.Hkv * w.N * w.d
+    assert all(e <= BF16_GRAD_REL_FRO for e in errs), (name, errs)
+
+
+@pytest.mark.parametrize("name", sorted(WHOLE_GROUPS))
+def test_backward_full_size_whole_groups(flash, oracle_mod, name):
+    """The longest workload: every dQ row and every dK / dV row of KV groups drawn by seed
+    (exact for those heads: groups are independent), plus dQ rows sampled over all heads."""
+    w = WORKLOADS[name]
+    Q, K, V, dO = workload_inputs(w)
+    dQ, dK, dV = gpu_fwd_bwd(flash, Q, K, V, dO, w.causal, w.scale)
+    G = w.Hq // w.Hkv
+    tq, tk, tv = ErrorTally(), ErrorTally(), ErrorTally()
+    groups = chosen_groups(w.B * w.Hkv, WHOLE_GROUPS[name], w.seed)
+    for bk in groups:
+        b, hk = divmod(bk, w.Hkv)
+        q, k, v, do = (f64(t) for t in group_slice(Q, K, V, dO, b, hk))
+        # the full backward of the group's sub-problem (it holds one N x N matrix, 8.6 GB here)
+        rq, rk, rv = oracle_mod.backward(q, k, v, do, w.causal, w.scale)
+        tq.add(dQ[b, hk * G:(hk + 1) * G], rq[0])
+        tk.add(dK[b, hk], rk[0, 0])
+        tv.add(dV[b, hk], rv[0, 0])
+    errs = (tq.rel_fro, tk.rel_fro, tv.rel_fro)
+    rows = sample_rows(w.B, w.Hq, w.N, 48, seed=w.seed)
+    dq_rows = oracle_mod.backward_dq_rows(f64(Q), f64(K), f64(V), f64(dO), w.causal, w.scale, rows)
+    err_rows = rel_fro(dQ.reshape(-1, w.d)[rows], dq_rows)
+    print("[parity] %s backward, groups %s: rel fro dQ %.3e dK %.3e dV %.3e; %d sampled dQ rows "
+          "%.3e" % ((name, groups) + errs + (len(rows), err_rows)))
+    assert all(e <= BF16_GRAD_REL_FRO for e in errs + (err_rows,)), (name, errs, err_rows)

@@ -1,16 +1,17 @@
 """bf16 forward on tcgen05 (fa_fwd) against the fp64 oracle on the same seeded inputs.
 
 Tolerances: O max abs <= 1e-2 and mean abs <= 1e-3; LSE max abs <= 1e-3.
-Small shapes are compared over every element; the full-size workloads are compared over whole
-(batch, KV-group) slices or sampled rows that the oracle computes one by one."""
+Small shapes and the full-size workloads up to N = 8192 are compared over every element; the
+N = 32768 workload over every row of four whole KV groups drawn by seed plus rows sampled over
+all heads (its oracle computes one row at a time)."""
 import numpy as np
 import pytest
 import torch
 
 import helpers
 from exact_attention_89_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
-from helpers import (BF16_LSE_MAX_ABS, BF16_O_MAX_ABS, BF16_O_MEAN_ABS, f64, group_slice,
-                     max_abs, mean_abs, sample_rows)
+from helpers import (BF16_LSE_MAX_ABS, BF16_O_MAX_ABS, BF16_O_MEAN_ABS, ErrorTally,
+                     chosen_groups, f64, group_slice, max_abs, mean_abs, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -77,21 +78,57 @@ def test_forward_fwd_d64_workload(flash, oracle_mod):
     assert_fwd_close(O, LSE, Oo, Lo, w.name)
 
 
-@pytest.mark.parametrize("name", ["causal_n4096", "gqa_n8192", "long_n32768",
-                                  "causal_d64_n4096"])
-def test_forward_full_size_workloads(flash, oracle_mod, name):
-    """Full-size causal workloads in the launch configuration the benchmark times: one whole
-    (batch, KV-group) slice (N <= 8192) plus rows sampled over all heads."""
+# Workloads whose every element the oracle checks (a few heads per oracle call), and the one
+# too long for that: its whole-group check covers KV groups drawn by seed.
+EVERY_ELEMENT = ["causal_n4096", "gqa_n8192", "causal_d64_n4096"]
+WHOLE_GROUPS = {"long_n32768": 4}
+
+
+@pytest.mark.parametrize("name", EVERY_ELEMENT)
+def test_forward_full_size_every_element(flash, oracle_mod, name):
+    """Full-size causal workloads in the launch configuration the benchmark times, compared with
+    the oracle over every element of O and LSE (the oracle runs a few heads at a time)."""
     w = WORKLOADS[name]
     Q, K, V, _ = workload_inputs(w)
     O, LSE = gpu_forward(flash, Q, K, V, w.causal, w.scale)
-    if w.N <= 8192:
-        b, hk = w.B - 1, w.Hkv - 1
+    q64, k64, v64 = f64(Q), f64(K), f64(V)
+    O2, L2 = O.reshape(w.B * w.Hq, w.N, w.d), LSE.reshape(w.B * w.Hq, w.N)
+    to, tl = ErrorTally(), ErrorTally()
+    step = 8
+    for h0 in range(0, w.B * w.Hq, step):
+        heads = list(range(h0, min(h0 + step, w.B * w.Hq)))
+        Oo, Lo = oracle_mod.forward(q64, k64, v64, w.causal, w.scale, heads=heads)
+        to.add(O2[heads], Oo)
+        tl.add(L2[heads], Lo)
+    print("[parity] %s forward, every element: O max abs %.3e mean abs %.3e, LSE max abs %.3e"
+          % (name, to.max_abs, to.mean_abs, tl.max_abs))
+    assert to.count == w.B * w.Hq * w.N * w.d
+    assert (to.max_abs <= BF16_O_MAX_ABS and to.mean_abs <= BF16_O_MEAN_ABS
+            and tl.max_abs <= BF16_LSE_MAX_ABS), (name, to.max_abs, to.mean_abs, tl.max_abs)
+
+
+@pytest.mark.parametrize("name", sorted(WHOLE_GROUPS))
+def test_forward_full_size_whole_groups(flash, oracle_mod, name):
+    """The longest workload: every row of KV groups drawn by seed (groups are independent, so
+    this is exact for those heads), plus rows sampled over all heads."""
+    w = WORKLOADS[name]
+    Q, K, V, _ = workload_inputs(w)
+    O, LSE = gpu_forward(flash, Q, K, V, w.causal, w.scale)
+    G = w.Hq // w.Hkv
+    to, tl = ErrorTally(), ErrorTally()
+    groups = chosen_groups(w.B * w.Hkv, WHOLE_GROUPS[name], w.seed)
+    for bk in groups:
+        b, hk = divmod(bk, w.Hkv)
         q, k, v, _ = group_slice(Q, K, V, None, b, hk)
-        Oo, Lo = oracle_mod.forward(f64(q), f64(k), f64(v), w.causal, w.scale)
-        G = w.Hq // w.Hkv
-        assert_fwd_close(O[b:b + 1, hk * G:(hk + 1) * G], LSE[b:b + 1, hk * G:(hk + 1) * G],
-                         Oo, Lo, name + " group")
+        rows = np.arange(G * w.N, dtype=np.int64)
+        Oo, Lo = oracle_mod.forward_rows(f64(q), f64(k), f64(v), w.causal, w.scale, rows)
+        to.add(O[b, hk * G:(hk + 1) * G].reshape(-1, w.d), Oo)
+        tl.add(LSE[b, hk * G:(hk + 1) * G].reshape(-1), Lo)
     rows = sample_rows(w.B, w.Hq, w.N, 96, seed=w.seed)
     Or, Lr = oracle_mod.forward_rows(f64(Q), f64(K), f64(V), w.causal, w.scale, rows)
-    assert_fwd_close(O.reshape(-1, w.d)[rows], LSE.reshape(-1)[rows], Or, Lr, name + " rows")
+    to.add(O.reshape(-1, w.d)[rows], Or)
+    tl.add(LSE.reshape(-1)[rows], Lr)
+    print("[parity] %s forward, groups %s + %d sampled rows: O max abs %.3e mean abs %.3e, "
+          "LSE max abs %.3e" % (name, groups, len(rows), to.max_abs, to.mean_abs, tl.max_abs))
+    assert (to.max_abs <= BF16_O_MAX_ABS and to.mean_abs <= BF16_O_MEAN_ABS
+            and tl.max_abs <= BF16_LSE_MAX_ABS), (name, to.max_abs, to.mean_abs, tl.max_abs)
