@@ -81,15 +81,20 @@ class ErrorTally:
 
     def __init__(self):
         self.max_abs = 0.0
+        self.worst = None          # (chunk label, index in the chunk, got, ref) of the max error
         self.abs_sum = 0.0
         self.count = 0
         self.diff_sq = 0.0
         self.ref_sq = 0.0
 
-    def add(self, got, ref):
+    def add(self, got, ref, label=None):
         g, r = _np(got), _np(ref)
         diff = g - r
-        self.max_abs = max(self.max_abs, float(np.max(np.abs(diff))) if diff.size else 0.0)
+        if diff.size:
+            k = int(np.argmax(np.abs(diff)))
+            if abs(diff.flat[k]) > self.max_abs:
+                self.max_abs = float(abs(diff.flat[k]))
+                self.worst = (label, np.unravel_index(k, diff.shape), float(g.flat[k]), float(r.flat[k]))
         self.abs_sum += float(np.sum(np.abs(diff)))
         self.count += diff.size
         self.diff_sq += float(np.sum(diff * diff))

@@ -98,10 +98,10 @@ def test_forward_full_size_every_element(flash, oracle_mod, name):
     for h0 in range(0, w.B * w.Hq, step):
         heads = list(range(h0, min(h0 + step, w.B * w.Hq)))
         Oo, Lo = oracle_mod.forward(q64, k64, v64, w.causal, w.scale, heads=heads)
-        to.add(O2[heads], Oo)
-        tl.add(L2[heads], Lo)
-    print("[parity] %s forward, every element: O max abs %.3e mean abs %.3e, LSE max abs %.3e"
-          % (name, to.max_abs, to.mean_abs, tl.max_abs))
+        to.add(O2[heads], Oo, label="heads %d.." % h0)
+        tl.add(L2[heads], Lo, label="heads %d.." % h0)
+    print("[parity] %s forward, every element: O max abs %.3e mean abs %.3e, LSE max abs %.3e; "
+          "worst O element %s" % (name, to.max_abs, to.mean_abs, tl.max_abs, to.worst))
     assert to.count == w.B * w.Hq * w.N * w.d
     assert (to.max_abs <= BF16_O_MAX_ABS and to.mean_abs <= BF16_O_MEAN_ABS
             and tl.max_abs <= BF16_LSE_MAX_ABS), (name, to.max_abs, to.mean_abs, tl.max_abs)
@@ -122,13 +122,14 @@ def test_forward_full_size_whole_groups(flash, oracle_mod, name):
         q, k, v, _ = group_slice(Q, K, V, None, b, hk)
         rows = np.arange(G * w.N, dtype=np.int64)
         Oo, Lo = oracle_mod.forward_rows(f64(q), f64(k), f64(v), w.causal, w.scale, rows)
-        to.add(O[b, hk * G:(hk + 1) * G].reshape(-1, w.d), Oo)
-        tl.add(LSE[b, hk * G:(hk + 1) * G].reshape(-1), Lo)
+        to.add(O[b, hk * G:(hk + 1) * G].reshape(-1, w.d), Oo, label="group %d" % bk)
+        tl.add(LSE[b, hk * G:(hk + 1) * G].reshape(-1), Lo, label="group %d" % bk)
     rows = sample_rows(w.B, w.Hq, w.N, 96, seed=w.seed)
     Or, Lr = oracle_mod.forward_rows(f64(Q), f64(K), f64(V), w.causal, w.scale, rows)
     to.add(O.reshape(-1, w.d)[rows], Or)
     tl.add(LSE.reshape(-1)[rows], Lr)
     print("[parity] %s forward, groups %s + %d sampled rows: O max abs %.3e mean abs %.3e, "
-          "LSE max abs %.3e" % (name, groups, len(rows), to.max_abs, to.mean_abs, tl.max_abs))
+          "LSE max abs %.3e; worst O element %s" % (name, groups, len(rows), to.max_abs, to.mean_abs,
+                                                    tl.max_abs, to.worst))
     assert (to.max_abs <= BF16_O_MAX_ABS and to.mean_abs <= BF16_O_MEAN_ABS
             and tl.max_abs <= BF16_LSE_MAX_ABS), (name, to.max_abs, to.mean_abs, tl.max_abs)
