@@ -46,6 +46,9 @@ MUFU_EX2_PER_CLK_PER_SM = 32.0
 # "<kernel file>:<sha256 prefix of that file and the device headers it includes>:<workload>";
 # a key that no longer matches the sources (the kernel changed since the capture) reports null.
 NCU_TRAFFIC = {
+    # fa_bwd on causal_n4096, KV heads in chunks of 16: bwd_main 0.415 GB read + 0.227 GB write,
+    # bwd_preprocess 0.206 GB, bwd_dq_convert 0.160 GB
+    "fa_bwd_sm103a.cu:85dc86856cd698dd:causal_n4096": 1.008e9,
     # fa_bwd on causal_n4096: bwd_main 1.917 GB read + 0.986 GB write, bwd_preprocess 0.206 GB,
     # bwd_dq_convert 0.160 GB
     "fa_bwd_sm103a.cu:2cc428e9de32c439:causal_n4096": 3.27e9,

@@ -21,11 +21,15 @@
 // S = Q K_j^T runs as SS MMAs (both operands K-major in 128B-swizzled smem); P is written back
 // over S as packed bf16 and O += P V_j runs as a TS MMA (P from TMEM, V MN-major in smem).
 // The MMA order S0(j+1) after PV0(j) lets softmax of one tile overlap the other tile's MMAs.
-// Rescaling of O is lazy: the stale max is kept until the block max exceeds it by 8 (log2
-// units), so p <= 2^8; the shift cancels in O = u / l, so the result is unchanged.
+// Rescaling of O is lazy: the stale max is kept until the block max exceeds it by 1 (log2
+// units), so p <= 2; the shift cancels in O = u / l.  Keeping the max that close to the row's
+// true max keeps its largest weight near 1, where bf16 rounds it finely; a looser threshold
+// measurably cost accuracy on rows whose weight is concentrated on a few keys.
 // O is divided by the sum of the fp32 weights plus the rounding residual of each block's largest
-// bf16 weight (when one weight dominates, the weights P V applies then sum to one); LSE uses the
-// sum of the fp32 weights alone.
+// bf16 weight when that weight dominates the row so far (at least half of its sum: the weights P V
+// applies then sum to one); LSE uses the sum of the fp32 weights alone.  Rows that see no key
+// past the first block (the first query tile of a causal head) apply that block's weights as two
+// bf16 parts, hi + lo, through a second P V product (two_part_p).
 #include <algorithm>
 #include <cmath>
 
@@ -45,7 +49,7 @@ constexpr int WARP_MMA = 9;
 // Register split: softmax warpgroups 0 and 1 grow, warpgroup 2 (TMA, MMA, two idle warps) shrinks.
 constexpr uint32_t REGS_SOFTMAX = 208, REGS_OTHER = 88;
 constexpr int REGS_NEEDED = 2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER;
-constexpr float RESCALE_THRESHOLD = 8.0f;
+constexpr float RESCALE_THRESHOLD = 1.0f;
 constexpr float LN2 = 0.693147180559945309f;
 
 template <int D>
@@ -134,6 +138,17 @@ __device__ __forceinline__ Item decode_item(int k, int Hq, int Hkv, int N, int B
     return it;
 }
 
+// Rows that see no key beyond the first block (query tile 0 under causal masking, or at most BN
+// valid keys) hold a few large weights, and rounding those to bf16 before P V can cost more
+// accuracy than the output's own bf16 rounding leaves room for.  On that block the weights are
+// applied as two bf16 parts, hi = bf16(p) and lo = bf16(p - hi), through a second P V product;
+// jb is the absolute key block; dropout keeps its own rounding rule.
+template <bool CAUSAL, bool MASK, bool DROP>
+__device__ __forceinline__ bool two_part_p(const Item &it, int t, int jb, int N) {
+    if (DROP || jb != 0) return false;
+    return (CAUSAL && it.q0[t] == 0) || (MASK ? it.lk : N) <= BN;
+}
+
 // Does tile t take key block jj (relative to the item's range)?  Without MASK every block of its
 // prefix; with MASK also only those its tile mask row keeps.
 template <bool MASK>
@@ -189,6 +204,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                float scale_log2, const MaskArgs mk, const DropoutArgs dr, unsigned *status) {
     static_assert(int(SPLIT) + int(MASK) + int(DROP) <= 1, "one variant at a time");
     constexpr bool SKIP_EMPTY = SPLIT || MASK;      // items may have no key block at all
+    // rows of O (or of the partials) and of LSE: the extent debug builds check writes against
+    const long long rows_total = static_cast<long long>(SPLIT ? S : 1) * BH * N;
+    (void)rows_total;
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -318,6 +336,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, sdesc_add(db, kk * 2048),
                            IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
             };
+            // The second product of a two-part block (two_part_p): the lo parts, stored 64
+            // columns after the hi parts, times the same V, added to O.
+            auto issue_pv_lo = [&](int t, int st) {
+#pragma unroll 1
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(tmem + 256 + t * 128, tmem + t * 128 + 64 + kk * 8,
+                           sdesc_add(dv0, st * L::TILE_BYTES + kk * 2048), IDESC_PV, 1u);
+            };
             int base = 0;                       // K/V ring index of the current item's K_0
             int pb[2] = {0, 0};                 // blocks consumed per tile (p_full phases)
             int of[2] = {0, 0};                 // items finished per tile (o_full / o_empty phases)
@@ -331,6 +357,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const Item it = decode_item<CAUSAL, SPLIT, MASK>(item_index(r), Hq, Hkv, N, BH, S, mk);
                 int u = next_of_pair<MASK>(it, 0);
                 if (u >= it.nmax) continue;
+                // the tiles' two-part P blocks (only relative block 0 can be one)
+                const bool two0 = two_part_p<CAUSAL, MASK, DROP>(it, 0, it.jb0, N);
+                const bool two1 = two_part_p<CAUSAL, MASK, DROP>(it, 1, it.jb0, N);
                 const int last0 = last_of_tile<MASK>(it, 0), last1 = last_of_tile<MASK>(it, 1);
                 const int ulast = max(last0, last1);
                 ok = mbar_wait(q_full, qn & 1, abort_flag, status) &&
@@ -356,6 +385,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ++pb[0];
                         tc_fence_after();
                         issue_pv(0, vst, started[0]);
+                        if (two0 && u == 0) issue_pv_lo(0, vst);
                         started[0] = true;
                         if (u == last0) mma_commit(&o_full[0]);
                     }
@@ -371,6 +401,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ++pb[1];
                         tc_fence_after();
                         issue_pv(1, vst, started[1]);
+                        if (two1 && u == 0) issue_pv_lo(1, vst);
                         started[1] = true;
                         if (u == last1) mma_commit(&o_full[1]);
                     }
@@ -401,6 +432,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mma_commit(&kv_empty[base % NS]);
                 if (it.nmax == 1) mma_commit(q_empty);     // every S product of the item issued
                 const int nb0 = it.nblk[0], nb1 = it.nblk[1], nmax = it.nmax;
+                // An item with a two-part block (only relative block 0 of a tile can be one: the
+                // first query tile of a causal head, or a sequence of at most BN keys) takes its
+                // own copy of the issue sequence with the lo products, so the sequence every
+                // other item runs is unchanged.
+                const bool two0 = two_part_p<CAUSAL, MASK, DROP>(it, 0, it.jb0, N);
+                const bool two1 = two_part_p<CAUSAL, MASK, DROP>(it, 1, it.jb0, N);
+                if (two0 || two1) {
+                    for (int j = 0; j < nmax; ++j) {
+                        const int vidx = base + 2 * j + 1, kidx = base + 2 * j + 2;
+                        const int vst = vidx % NS, kst = kidx % NS;
+                        const bool next = j + 1 < nmax;
+                        if (!mbar_wait(&kv_full[vst], (vidx / NS) & 1, abort_flag, status)) { ok = false; break; }
+                        if (j < nb0) {
+                            if (j == 0 && of[0] > 0 &&
+                                !mbar_wait(&o_empty[0], (of[0] - 1) & 1, abort_flag, status)) { ok = false; break; }
+                            if (!mbar_wait(&p_full[0], pb[0] & 1, abort_flag, status)) { ok = false; break; }
+                            ++pb[0];
+                            tc_fence_after();
+                            issue_pv(0, vst, j > 0);
+                            if (two0 && j == 0) issue_pv_lo(0, vst);
+                            if (j == nb0 - 1) mma_commit(&o_full[0]);
+                        }
+                        if (next) {
+                            if (!mbar_wait(&kv_full[kst], (kidx / NS) & 1, abort_flag, status)) { ok = false; break; }
+                            tc_fence_after();
+                            if (j + 1 < nb0) issue_s(0, kst);
+                        }
+                        if (j < nb1) {
+                            if (j == 0 && of[1] > 0 &&
+                                !mbar_wait(&o_empty[1], (of[1] - 1) & 1, abort_flag, status)) { ok = false; break; }
+                            if (!mbar_wait(&p_full[1], pb[1] & 1, abort_flag, status)) { ok = false; break; }
+                            ++pb[1];
+                            tc_fence_after();
+                            issue_pv(1, vst, j > 0);
+                            if (two1 && j == 0) issue_pv_lo(1, vst);
+                            if (j == nb1 - 1) mma_commit(&o_full[1]);
+                        }
+                        mma_commit(&kv_empty[vst]);
+                        if (next) {
+                            if (j + 1 < nb1) issue_s(1, kst);
+                            mma_commit(&kv_empty[kst]);
+                            if (j + 1 == nmax - 1) mma_commit(q_empty);
+                        }
+                    }
+                    if (!ok) break;
+                    for (int t = 0; t < 2; ++t)
+                        if (it.nblk[t] > 0) ++of[t];
+                    base += 2 * it.nmax;
+                    ++qn;
+                    continue;
+                }
                 for (int j = 0; j < nmax; ++j) {
                     const int vidx = base + 2 * j + 1, kidx = base + 2 * j + 2;
                     const int vst = vidx % NS, kst = kidx % NS;
@@ -476,10 +558,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int jfirst = next_of_tile<MASK>(it, t, 0);
             if (nb == 0 || (MASK && jfirst >= nb)) {
                 // Split-KV: these rows have no allowed key in the range; the merge skips them.
-                if (SPLIT && rq < N)
+                const long long drow = (static_cast<long long>(SPLIT ? it.split : 0) * BH + it.bh) * N + rq;
+                if (SPLIT && rq < N && in_bounds(drow, rows_total, status))
                     LSE[(static_cast<size_t>(it.split) * BH + it.bh) * N + rq] = -INFINITY;
                 // General mask: no allowed key at all, so O = 0 and LSE = -inf.
-                if (MASK && rq < N) {
+                if (MASK && rq < N && in_bounds(drow, rows_total, status)) {
                     uint4 *orow = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(Out) +
                                                             (static_cast<size_t>(it.bh) * N + rq) * D);
 #pragma unroll
@@ -537,8 +620,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if ((MASK ? jj : j) > 0) rescale_o_row<D>(tO, alpha);
                 }
                 const float m_sub = (m == -INFINITY) ? 0.f : m;
-                uint32_t p[64];
+                // P (bf16 pairs) goes over the first 64 columns of S in each branch below
                 if constexpr (DROP) {
+                    uint32_t p[64];
                     // p = 2^(s c - m) for four keys at a time, with the keep words of those four
                     // keys from one Philox call; l sums every weight, lc the rounding residuals
                     // of the kept ones (the weights P V applies)
@@ -562,7 +646,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     l += lsum;
                     lc += lres;
+                    tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+                    tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+                } else if (two_part_p<CAUSAL, MASK, DROP>(it, t, it.jb0 + j, N)) {
+                // the row sees only this block: p = hi + lo, both bf16, stored a quarter at a time
+                // (hi over the first 64 columns of S, lo over the next 64, which S no longer needs)
+                // for the two P V products; the applied weights then equal p to about 2^-17
+                const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+                const uint64_t nm2 = f2_pack(-m_sub, -m_sub);
+                uint64_t acc[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[k] = 0ull;
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t hi[16], lo[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const int e = 2 * (16 * h + c);
+                        const float2 x = f2_unpack(f2_fma(f2_pack(s[e], s[e + 1]), c2, nm2));
+                        const float p0 = ex2_approx(x.x);
+                        const float p1 = ex2_approx(x.y);
+                        acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
+                        hi[c] = pack_bf16x2(p0, p1);
+                        const float h0 = __uint_as_float(hi[c] << 16);
+                        const float h1 = __uint_as_float(hi[c] & 0xFFFF0000u);
+                        lo[c] = pack_bf16x2(p0 - h0, p1 - h1);
+                    }
+                    tmem_st_x16(tS + 16 * h, hi);
+                    tmem_st_x16(tS + 64 + 16 * h, lo);
+                }
+                const float2 a = f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])));
+                l += a.x + a.y;
                 } else {
+                uint32_t p[64];
                 // p = 2^(s c - m) on pairs: one packed FMA, two ex2, packed sums in 4 chains
                 const uint64_t c2 = f2_pack(scale_log2, scale_log2);
                 const uint64_t nm2 = f2_pack(-m_sub, -m_sub);
@@ -580,13 +696,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 {
                     const float2 a = f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])));
                     l += a.x + a.y;
-                    // the block's largest weight is computed exactly as its element was above
+                    // the block's largest weight, computed exactly as its element was above: its
+                    // rounding residual joins the normaliser only when it dominates the row so far
                     const float ptop = ex2_approx(fmaf(mx, scale_log2, -m_sub));
-                    lc += __bfloat162float(__float2bfloat16_rn(ptop)) - ptop;
-                }
+                    if (ptop >= 0.5f * l) lc += __bfloat162float(__float2bfloat16_rn(ptop)) - ptop;
                 }
                 tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
                 tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+                }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&p_full[t]);
@@ -602,11 +719,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float inv_l = dead ? 0.f : (DROP ? dr.rscale : 1.f) / (l + lc);
             const size_t orow_idx = ((SPLIT ? static_cast<size_t>(it.split) * BH : 0) + it.bh) *
                                         static_cast<size_t>(N) + rq;
+            // (debug builds: the row of O and LSE this thread writes lies inside them)
+            const bool row_ok = rq < N && in_bounds(static_cast<long long>(orow_idx), rows_total, status);
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
                 tmem_ld_x32(tO + c0, o);
-                if (rq < N) {
+                if (row_ok) {
                     if constexpr (SPLIT) {
                         float *orow = static_cast<float *>(Out) + orow_idx * D;
 #pragma unroll
@@ -636,7 +755,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            if (rq < N) LSE[orow_idx] = (MASK && dead) ? -INFINITY : (m + log2f(l)) * LN2;
+            if (row_ok) LSE[orow_idx] = (MASK && dead) ? -INFINITY : (m + log2f(l)) * LN2;
             tc_fence_before();
             mbar_arrive(&o_empty[t]);
         }

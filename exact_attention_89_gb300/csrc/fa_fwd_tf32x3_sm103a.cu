@@ -20,8 +20,8 @@
 // staged in shared memory as the K-major A operand of P V.  Each block's P V starts a fresh
 // accumulator and the softmax warps add it into fp32 register sums: the tensor core's
 // accumulation error grows with the number of MMAs chained into one accumulator, and this keeps
-// the chain at 12.  The max is rescaled lazily (threshold 8, log2 units) as in the bf16 forward,
-// on the register sums.
+// the chain at 12.  The max is rescaled lazily (threshold 8, log2 units) on the register sums;
+// P is kept in three TF32 parts here, so the size of the weights does not limit its precision.
 #include <algorithm>
 #include <cmath>
 

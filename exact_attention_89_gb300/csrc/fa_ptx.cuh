@@ -36,6 +36,26 @@ __device__ __forceinline__ void record_status(unsigned *status, unsigned code) {
     if (status) atomicCAS(status, 0u, code);
 }
 
+// Debug builds (FA_DEBUG_BOUNDS) check the index of every computed plain (non-TMA) global
+// access of the bf16 forward and backward kernels against the extent of its buffer: an index
+// out of range records FA_ERR_DEVICE_BOUNDS in the status word and the access is skipped, so a
+// wrong index is reported instead of faulting.  Regular builds compile the checks away.
+// FA_DEBUG_BOUNDS_SHRINK (test builds only) treats every extent as that many units smaller, so
+// the accesses at the end of each buffer are reported and skipped: the reporting path runs
+// without any access leaving its buffer.
+#ifdef FA_DEBUG_BOUNDS
+#ifndef FA_DEBUG_BOUNDS_SHRINK
+#define FA_DEBUG_BOUNDS_SHRINK 0
+#endif
+__device__ __forceinline__ bool in_bounds(long long idx, long long extent, unsigned *status) {
+    if (idx >= 0 && idx < extent - FA_DEBUG_BOUNDS_SHRINK) return true;
+    record_status(status, FA_ERR_DEVICE_BOUNDS);
+    return false;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(long long, long long, unsigned *) { return true; }
+#endif
+
 // ------------------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

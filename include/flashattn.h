@@ -31,7 +31,11 @@
  *    detected on the device (a bounded wait that ran out) are recorded in a per-device status
  *    word read by fa_get_device_status.  The library never prints, traps or exits.
  *  - Precision of the bf16 entry points: bf16 inputs and outputs, fp32 accumulation, fp32 LSE,
- *    probabilities rounded to bf16 (round-to-nearest-even) before the second product.
+ *    probabilities rounded to bf16 (round-to-nearest-even) before the second product; rows that
+ *    see only the first 128 keys (the first query tile of a causal head) apply them as two bf16
+ *    parts, so their few large weights are not rounded.  Failures detected on the device also
+ *    include FA_ERR_DEVICE_BOUNDS, reported only by debug builds (FA_DEBUG_BOUNDS), which check
+ *    the kernels' computed global indices.
  */
 #ifndef FLASHATTN_H
 #define FLASHATTN_H
@@ -51,7 +55,7 @@ typedef enum {
     FA_ERR_WORKSPACE = 4,      /* workspace null or smaller than fa_bwd_workspace_bytes */
     FA_ERR_CUDA = 5,           /* a CUDA runtime/driver call or a launch failed */
     FA_ERR_DEVICE_TIMEOUT = 6, /* a kernel's bounded wait ran out (reported by the status word) */
-    FA_ERR_DEVICE_BOUNDS = 7   /* a kernel's own bounds check failed (reported likewise) */
+    FA_ERR_DEVICE_BOUNDS = 7   /* a debug build's bounds check caught an index (reported likewise) */
 } fa_status;
 
 /*
