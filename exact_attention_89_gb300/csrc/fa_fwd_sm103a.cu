@@ -67,17 +67,27 @@ struct Layout {
     static constexpr int BYTES = ABORT_OFF + 8 + 1024;   // + slack for 1024-byte alignment
 };
 
+// O row *= alpha in TMEM; the caller waits for the stores.  At head dim 128 one load and one
+// store of the whole row (the caller has no other large register arrays live); at 64, in
+// 32-column pieces (measured: fewer spills there).
 template <int D>
 __device__ __forceinline__ void rescale_o_row(uint32_t tO, float alpha) {
+    if constexpr (D == 128) {
+        uint32_t o[128];
+        tmem_ld_x128(tO, o);
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld_x32(tO + c0, o);
+        for (int i = 0; i < 128; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st_x128(tO, o);
+    } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st_x32(tO + c0, o);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(tO + c0, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st_x32(tO + c0, o);
+        }
     }
-    tmem_wait_st();
 }
 
 // One work item = two 128-row query tiles (a "pair") of one (batch, head) against one range of key
@@ -610,6 +620,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                        fmaxf(m8[6], m8[7]));
                 const float m_blk = mx * scale_log2;
                 const bool need = m_blk > m + RESCALE_THRESHOLD;
+                // At head dim 128, O is rescaled after this block's P is stored (below): it stays
+                // untouched until p_full releases this block's P V, and by then the S and P
+                // registers are free for one full-row TMEM load and store.  (At 64 that measured
+                // more spills; O is rescaled here.)
+                bool rescale_o = false;
+                float alpha_o = 1.f;
                 if (__any_sync(0xffffffffu, need)) {
                     const float alpha = need ? ex2_approx(m - m_blk) : 1.f;
                     if (need) {
@@ -617,7 +633,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         lc *= alpha;
                         m = m_blk;
                     }
-                    if ((MASK ? jj : j) > 0) rescale_o_row<D>(tO, alpha);
+                    if constexpr (D == 128) {
+                        rescale_o = (MASK ? jj : j) > 0;
+                        alpha_o = alpha;
+                    } else {
+                        if ((MASK ? jj : j) > 0) {
+                            rescale_o_row<D>(tO, alpha);
+                            tmem_wait_st();
+                        }
+                    }
                 }
                 const float m_sub = (m == -INFINITY) ? 0.f : m;
                 // P (bf16 pairs) goes over the first 64 columns of S in each branch below
@@ -704,6 +728,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_st_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
                 tmem_st_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
                 }
+                if (D == 128 && rescale_o) rescale_o_row<D>(tO, alpha_o);   // (warp-uniform)
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&p_full[t]);
