@@ -46,33 +46,28 @@ MUFU_EX2_PER_CLK_PER_SM = 32.0
 # "<kernel file>:<sha256 prefix of that file and the device headers it includes>:<workload>";
 # a key that no longer matches the sources (the kernel changed since the capture) reports null.
 NCU_TRAFFIC = {
-    # fa_bwd on causal_n4096, KV heads in chunks of 16: bwd_main 0.415 GB read + 0.227 GB write,
-    # bwd_preprocess 0.206 GB, bwd_dq_convert 0.160 GB
-    "fa_bwd_sm103a.cu:85dc86856cd698dd:causal_n4096": 1.008e9,
-    # fa_bwd on causal_n4096: bwd_main 1.917 GB read + 0.986 GB write, bwd_preprocess 0.206 GB,
-    # bwd_dq_convert 0.160 GB
-    "fa_bwd_sm103a.cu:2cc428e9de32c439:causal_n4096": 3.27e9,
-    # fa_bwd at head dim 64: bwd_main 0.997 GB, bwd_preprocess 0.073 GB, bwd_dq_convert 0.069 GB
-    "fa_bwd_sm103a.cu:2cc428e9de32c439:causal_d64_n4096": 1.139e9,
-    # split forward on splitkv_n32768: 25.4 MB read + 0.2-0.5 MB write (partials stay in L2)
-    "fa_fwd_sm103a.cu:13f6438b56253de0:splitkv_n32768": 2.59e7,
-    # fa_bwd_masked, three kernels
-    "fa_bwd_sm103a.cu:2cc428e9de32c439:local_n16384": 0.996e9,
-    "fa_bwd_sm103a.cu:2cc428e9de32c439:varlen_n8192": 25.1e9,
-    # fa_bwd_dropout, three kernels
-    "fa_bwd_sm103a.cu:2cc428e9de32c439:dropout_n4096": 3.79e9,
-    # fa_bwd on gqa_n8192: bwd_main 0.645 + 0.279 GB, bwd_preprocess 0.206 GB, bwd_dq_convert
-    # 0.160 GB; on long_n32768: bwd_main 7.658 + 3.892 GB, bwd_preprocess 0.475 GB,
-    # bwd_dq_convert 0.354 GB
-    "fa_bwd_sm103a.cu:2cc428e9de32c439:gqa_n8192": 1.290e9,
-    "fa_bwd_sm103a.cu:2cc428e9de32c439:long_n32768": 12.38e9,
+    # fa_bwd, three kernels per launch (bwd_preprocess + bwd_main + bwd_dq_convert, read + write):
+    # causal_n4096 0.206 + 0.641 + 0.160 GB; causal_d64_n4096 0.073 + 0.291 + 0.070 GB;
+    # gqa_n8192 0.206 + 0.906 + 0.161 GB; long_n32768 0.476 + 1.345 + 0.355 GB
+    "fa_bwd_sm103a.cu:53515684288a829d:causal_n4096": 1.007e9,
+    "fa_bwd_sm103a.cu:53515684288a829d:causal_d64_n4096": 0.433e9,
+    "fa_bwd_sm103a.cu:53515684288a829d:gqa_n8192": 1.273e9,
+    "fa_bwd_sm103a.cu:53515684288a829d:long_n32768": 2.175e9,
+    # fa_bwd_masked, three kernels: local_n16384 0.206 + 0.630 + 0.160 GB; varlen_n8192
+    # 1.014 + 1.901 + 0.766 GB
+    "fa_bwd_sm103a.cu:53515684288a829d:local_n16384": 0.996e9,
+    "fa_bwd_sm103a.cu:53515684288a829d:varlen_n8192": 3.681e9,
+    # fa_bwd_dropout, three kernels: 0.206 + 0.634 + 0.160 GB
+    "fa_bwd_sm103a.cu:53515684288a829d:dropout_n4096": 1.001e9,
+    # split forward on splitkv_n32768: 25.3 MB read + 0.2 MB write (partials stay in L2)
+    "fa_fwd_sm103a.cu:b18fda5356d2798b:splitkv_n32768": 2.55e7,
     # forward at head dim 64 on fwd_d64: 25.2 MB read (Q, K, V), O written back from L2 later
-    "fa_fwd_sm103a.cu:13f6438b56253de0:fwd_d64": 2.52e7,
-    # key/value-outer forward
-    "fa_fwd_kvouter_sm103a.cu:cf980aee93773e67:kvouter_n4096": 4.14e9,
+    "fa_fwd_sm103a.cu:b18fda5356d2798b:fwd_d64": 2.52e7,
+    # key/value-outer forward: 2.374 GB read + 1.765 GB write
+    "fa_fwd_kvouter_sm103a.cu:e1fd8857363ec7a5:kvouter_n4096": 4.139e9,
     # fp32 tensor-core backward: split rows 0.343 GB, split transposes 0.239 GB, dq pass
-    # 0.328 GB, dkv pass 0.403 GB
-    "fa_bwd_tf32x3_sm103a.cu:920f747c9ad578a2:fp32tc_n4096": 1.314e9,
+    # 0.328 GB, dkv pass 0.404 GB
+    "fa_bwd_tf32x3_sm103a.cu:e7a2a8701d4616b6:fp32tc_n4096": 1.314e9,
 }
 
 
@@ -777,6 +772,28 @@ def main():
         torch.cuda.synchronize()
         simt_bwd_ms = b_s.elapsed_time(b_e)
 
+    # the deterministic backward (dQ reductions in a fixed order) on the same inputs, timed like
+    # fa_bwd in the steps above, for its cost against fa_bwd
+    det_bwd_ms = None
+    if (w.backward and not (masked or w.dropout or w.tensor_fp32 or split)
+            and not args.no_extras):
+        wdet = torch.empty(fa.fa_bwd_deterministic_workspace_bytes(B, Hq, N, d), dtype=torch.uint8,
+                           device=dev)
+        det_args = (q, k, v, O, do, LSE, dQ, dK, dV, w.causal, w.scale, wdet)
+        for _ in range(3):
+            fa.fa_bwd_deterministic(*det_args)
+        d_s = torch.cuda.Event(enable_timing=True)
+        d_e = torch.cuda.Event(enable_timing=True)
+        d_s.record(stream)
+        for _ in range(args.steps):
+            fa.fa_bwd_deterministic(*det_args)
+        d_e.record(stream)
+        torch.cuda.synchronize()
+        if fa.fa_get_device_status() != fa.FA_OK:
+            raise RuntimeError("device status after the deterministic backward")
+        det_bwd_ms = d_s.elapsed_time(d_e) / args.steps
+        del wdet
+
     # ---------------------------------------------------------------- end to end (host buffers)
     # Every step copies its inputs from pinned host memory, runs the path through the public
     # entry points and copies its outputs back to pinned host memory.  The copies run on their
@@ -916,6 +933,11 @@ def main():
                     "mufu_ex2": ex2_ceiling(exps, flops_bwd, second_ms,
                                             (clocks or {}).get("sm_mhz"), num_sms),
                     "bwd_ms": second_ms, "sources": bwd_key}
+        if det_bwd_ms is not None:
+            roofline["deterministic_bwd"] = {
+                "kernel": "fa_bwd_deterministic (dQ reductions in a fixed order)",
+                "ms": det_bwd_ms, "achieved": flops_bwd / (det_bwd_ms * 1e-3) / 1e12,
+                "time_vs_fa_bwd": det_bwd_ms / second_ms}
     else:
         roofline = {"bound": "tensor",
                     "kernel": ("fa_fwd_kvouter" if w.kv_outer else

@@ -213,6 +213,17 @@ size_t fa_bwd_workspace_bytes(int B, int Hq, int N, int d) {
     return fa::align256(r * sizeof(float)) + r * static_cast<size_t>(d) * sizeof(float);
 }
 
+size_t fa_bwd_deterministic_workspace_bytes(int B, int Hq, int N, int d) {
+    const size_t base = fa_bwd_workspace_bytes(B, Hq, N, d);
+    if (base == 0 || base == SIZE_MAX) return base;
+    // four turn counters per 64-row query tile, then the abort word (padded to 16 bytes)
+    const size_t tiles = static_cast<size_t>(B) * Hq * ((static_cast<size_t>(N) + 63) / 64);
+    if (tiles > (SIZE_MAX - 16) / 16) return SIZE_MAX;
+    const size_t extra = tiles * 16 + 16;
+    if (base > SIZE_MAX - extra) return SIZE_MAX;
+    return base + extra;
+}
+
 fa_status fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int Hq,
                  int Hkv, int N, int d, int causal, float scale, cudaStream_t stream) {
     fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
@@ -589,6 +600,49 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
     if (e == cudaSuccess)
         e = fa::launch_bwd_main_bf16(p, tq, tk, tv, tdo, tdk, tdv, tdq, LSE, Dvec, dQacc, di->status,
                                      stream);
+    if (e == cudaSuccess) e = fa::launch_bwd_dq_convert_bf16(p, dQacc, dQ, stream);
+    return fa::from_cuda(e);
+}
+
+fa_status fa_bwd_deterministic(const void *Q, const void *K, const void *V, const void *O,
+                               const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                               int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                               void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    fa_status st = fa::check_sizes(B, Hq, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!fa::aligned16(Q) || !fa::aligned16(K) || !fa::aligned16(V) || !fa::aligned16(O) ||
+        !fa::aligned16(dO) || !fa::aligned16(LSE) || !fa::aligned16(dQ) || !fa::aligned16(dK) ||
+        !fa::aligned16(dV))
+        return FA_ERR_MISALIGNED;
+    if (!fa::aligned16(workspace) ||
+        workspace_bytes < fa_bwd_deterministic_workspace_bytes(B, Hq, N, d))
+        return FA_ERR_WORKSPACE;
+    fa::DeviceInfo *di = nullptr;
+    if ((st = fa::current_device(&di, true)) != FA_OK) return st;
+    const Problem p{B, Hq, Hkv, N, d, causal ? 1 : 0, scale};
+    const size_t rows = static_cast<size_t>(B) * Hq * N;
+    const size_t base = fa_bwd_workspace_bytes(B, Hq, N, d);
+    float *Dvec = static_cast<float *>(workspace);
+    float *dQacc = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                             fa::align256(rows * sizeof(float)));
+    // the counters follow the accumulator directly (base is a multiple of 16 for d = 64, 128), so
+    // K2 clears both in one pass
+    unsigned *dq_sem = reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + base);
+    const size_t sem_bytes = fa_bwd_deterministic_workspace_bytes(B, Hq, N, d) - base;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
+    if (!fa::encode_bf16(&tq, Q, d, N, 1LL * B * Hq, 64) ||
+        !fa::encode_bf16(&tk, K, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tv, V, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tdo, dO, d, N, 1LL * B * Hq, 64) ||
+        !fa::encode_bf16(&tdk, dK, d, N, 1LL * B * Hkv, 128) ||
+        !fa::encode_bf16(&tdv, dV, d, N, 1LL * B * Hkv, 128))
+        return FA_ERR_CUDA;
+    if (!fa::encode_dq(&tdq, dQacc, d, N, 1LL * B * Hq)) return FA_ERR_CUDA;
+    cudaError_t e = fa::launch_bwd_preprocess_bf16(p, O, dO, Dvec, dQacc, stream, sem_bytes);
+    if (e == cudaSuccess)
+        e = fa::launch_bwd_main_deterministic_bf16(p, tq, tk, tv, tdo, tdk, tdv, tdq, LSE, Dvec,
+                                                   dQacc, dq_sem, di->status, stream);
     if (e == cudaSuccess) e = fa::launch_bwd_dq_convert_bf16(p, dQacc, dQ, stream);
     return fa::from_cuda(e);
 }

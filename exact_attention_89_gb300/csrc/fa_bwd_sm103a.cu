@@ -28,7 +28,8 @@
 // Roles (384 threads): warps 0-3 softmax-gradient (and the dK / dV epilogue), warps 4-7 dQ drain
 // (at head dim 64 also the dV half of the epilogue), warp 8 TMA, warp 9 the S^T / dP^T MMAs and
 // warp 10 the dQ^T / dV / dK MMAs (one elected lane each), warp 11 idle (it completes the third
-// warpgroup for the register split).
+// warpgroup for the register split) except in the deterministic variant, where it passes the dQ
+// turns.
 // TMEM (512 columns): dK [0,128), dV [128,256), buffer b at 256 + 128 b:
 //   [+0,+64) S^T -> P^T [+0,+32) and dS^T [+32,+64);  [+64,+128) dP^T -> dQ^T.
 #include <algorithm>
@@ -48,6 +49,8 @@ constexpr int NUM_THREADS = 384;   // three warpgroups
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;       // TMEM allocator; issues S^T and dP^T
 constexpr int WARP_MMA2 = 10;     // issues dQ^T, dV and dK
+constexpr int WARP_PASS = 11;     // deterministic variant: passes the dQ turns
+constexpr int NSENT = 4;          // steps the drain warps may run ahead of the turn passer
 // Register split: softmax-gradient warpgroup grows; dQ drain and TMA/MMA warpgroups shrink.
 constexpr uint32_t REGS_GRAD = 256, REGS_DRAIN = 88, REGS_OTHER = 80;
 constexpr int REGS_NEEDED = 128 * (REGS_GRAD + REGS_DRAIN + REGS_OTHER);
@@ -83,6 +86,10 @@ struct Layout {
     static constexpr int KM_BAR_OFF = KEEP_OFF + 2 * BKV * 8;
     static constexpr int XCH_OFF = KM_BAR_OFF + 4 * 8;            // [BKV] quad exchange words
     static constexpr int BYTES_DROP = XCH_OFF + BKV * 8 + 1024;
+    // Deterministic variant: sent_full[NSENT] / sent_empty[NSENT], the drain warps' hand-over of
+    // finished steps to the turn passer.
+    static constexpr int SENT_OFF = ABORT_OFF + 16;
+    static constexpr int BYTES_DET = SENT_OFF + 2 * NSENT * 8 + 1024;
 };
 
 constexpr uint32_t T_DK = 0, T_DV = 128, T_BUF = 256;
@@ -104,6 +111,57 @@ __device__ __forceinline__ void bulk_wait_read() {
 
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- ordered dQ reductions
+// The deterministic variant adds the contributions of the key blocks to each 64-row query tile
+// of dQ in one fixed order: descending key block.  A counter per query row tile in the workspace,
+// zeroed by K2, says how many key blocks have added their part.  The drain warps of key block jb
+// wait for their turn (the number of contributing key blocks above jb), add, and hand the step
+// to the turn passer (warp 11), which moves the step's counter on with a release reduction: the
+// drain warps' reductions, which it acquired through the hand-over barrier, are ordered before
+// it, and the wait for them to reach L2 stays off the drain warps' loop.  CTAs of one head are launched in the same descending order,
+// so a CTA only ever waits for CTAs launched before it.  All waits are bounded: a wait that runs
+// out records FA_ERR_DEVICE_TIMEOUT and sets the call's abort word (after the counters), which
+// ends every other CTA's waits at once.
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Warp-collective: true once counter `tile` of dq_sem equals `turn`; false after an abort (this
+// CTA's or the call's, the word after the `tiles` counters) or a timeout.
+__device__ __forceinline__ bool dq_turn_wait(unsigned *dq_sem, size_t tile, size_t tiles, unsigned turn,
+                                             volatile int *abort_flag, unsigned *status) {
+    int ok = 1;
+    const unsigned *sem = dq_sem + tile * 4;
+    if ((threadIdx.x & 31) == 0 && ld_acquire_gpu(sem) != turn) {
+        unsigned *call_abort = dq_sem + tiles * 4;
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(sem) != turn) {
+            if (*abort_flag || ld_relaxed_gpu(call_abort)) {
+                *abort_flag = 1;
+                ok = 0;
+                break;
+            }
+            if (globaltimer_ns() - t0 > FA_WAIT_NS) {
+                *abort_flag = 1;
+                atomicExch(call_abort, 1u);
+                record_status(status, FA_ERR_DEVICE_TIMEOUT);
+                ok = 0;
+                break;
+            }
+            __nanosleep(64);
+        }
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 template <int W>
@@ -154,7 +212,9 @@ __device__ __forceinline__ int first_q_tile(int jb) {
 // words one step ahead into shared memory: one Philox call gives the decisions of the four keys
 // of a quad at one query, so each lane of a quad calls it for a quarter of the queries and the
 // quad exchanges its four 64-bit results through shared memory (shuffles measured 4x slower).
-template <int D, int DR, bool CAUSAL, bool MASK, bool DROP>
+// DET = true: the deterministic variant (ordered dQ reductions, above); dq_sem holds B * Hq *
+// ceil(N / 64) * 4 counters followed by the call's abort word.
+template <int D, int DR, bool CAUSAL, bool MASK, bool DROP, bool DET>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -163,8 +223,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const float *__restrict__ LSE, const float *__restrict__ Dvec,
                     float *__restrict__ dQacc, int Hq, int Hkv, int N, int BHkv, int HC,
                     float scale, float scale_log2, const MaskArgs mk, const DropoutArgs drop,
-                    unsigned *status) {
+                    unsigned *dq_sem, unsigned *status) {
     static_assert(!(MASK && DROP), "one variant at a time");
+    static_assert(!(DET && (MASK || DROP)), "the deterministic variant has no mask or dropout");
     // Laid out for d = 128.  With a real head dim DR = 64 only the first 64-column chunk of Q,
     // dO and V is loaded and S^T, dP^T (K dim), dV and dK (N) run over DR; dQ^T keeps M = 128
     // (the MMA's row count), its upper rows coming from K's second chunk, which the 64-wide
@@ -173,7 +234,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     static_assert(DR == 64 || DR == 128, "real head dim 64 or 128");
     // At head dim 64 dQ leaves through bulk tensor reductions (see the drain warps); at 128 the
     // per-element reductions measured faster (a staged 64 x 128 tile: 0.944 ms against 0.917).
-    constexpr bool DQ_TMA = DR == 64;
+    // The deterministic variant uses the per-element reductions at both head dims, so that
+    // passing a turn only has to order plain global reductions.
+    constexpr bool DQ_TMA = DR == 64 && !DET;
     // The dK / dV epilogue: split between the gradient warps (dK) and the drain warps (dV) where
     // the drain warps' per-step work is the short staged reduction (DR = 64); at DR = 128 the
     // drain warps are still busy with the last step's per-element reductions then.
@@ -199,6 +262,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t *keep_words = reinterpret_cast<uint64_t *>(smem + L::KEEP_OFF);
     uint64_t *km_full = reinterpret_cast<uint64_t *>(smem + L::KM_BAR_OFF);
     uint64_t *km_empty = km_full + 2;
+    uint64_t *sent_full = reinterpret_cast<uint64_t *>(smem + L::SENT_OFF);   // [NSENT]
+    uint64_t *sent_empty = sent_full + NSENT;                                // [NSENT]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = Hq / Hkv;
@@ -208,12 +273,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     (void)rows_total;
     // Work item: (key block jb, batch * KV head).  KV heads go in chunks of HC (about one wave),
     // so the Q / dO / dQ accumulator rows of the heads in flight stay in L2; inside a chunk the
-    // small jb (most query tiles under causal masking) go first.
+    // small jb (most query tiles under causal masking) go first, except in the deterministic
+    // variant, whose dQ reduction order (descending jb) the launch order has to follow.
     const int chunk = blockIdx.x / (HC * nkb);
     const int in_chunk = blockIdx.x - chunk * HC * nkb;
     const int hc = min(HC, BHkv - chunk * HC);
     const int bkv = chunk * HC + in_chunk % hc;          // b * Hkv + hk
-    const int jb = in_chunk / hc;
+    const int jb = DET ? nkb - 1 - in_chunk / hc : in_chunk / hc;
     const int b = bkv / Hkv, hk = bkv % Hkv;
     const int nq = (N + BQ - 1) / BQ;
     const int i0 = first_q_tile<CAUSAL>(jb);
@@ -291,6 +357,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (DROP) {
             uint64_t *kb = reinterpret_cast<uint64_t *>(smem + L::KM_BAR_OFF);
             for (int k = 0; k < 4; ++k) mbar_init(&kb[k], 128);
+        }
+        if (DET) {
+            for (int k = 0; k < NSENT; ++k) {
+                mbar_init(&sent_full[k], 128);
+                mbar_init(&sent_empty[k], 1);
+            }
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -432,6 +504,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // Nothing either issued may still be running when TMEM is released.
             mma_commit(mma_done);
             mbar_drain(mma_done, 0);
+        }
+      } else if (DET && warp == WARP_PASS) {
+        // ------------------------------------------------------------------ dQ turn passer
+        // Takes every step the drain warps have handed over (at least one), moves those steps'
+        // counters on and frees their hand-over slots.
+        if (lane == 0) {
+            int s = 0;
+            while (s < T) {
+                if (!mbar_wait(&sent_full[s % NSENT], (s / NSENT) & 1, abort_flag, status)) break;
+                int e = s + 1;
+                while (e < T && e - s < NSENT && mbar_try_wait(&sent_full[e % NSENT], (e / NSENT) & 1))
+                    ++e;
+                for (int t = s; t < e; ++t) {
+                    int g, i;
+                    step_tile(t, g, i);
+                    unsigned *sem = dq_sem + (static_cast<size_t>(b * Hq + hk * G + g) * nq + i) * 4;
+                    // a release: the drain warps' reductions, acquired through sent_full, are
+                    // ordered before the counter moves (cheaper here than a fence and a relaxed add)
+                    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(sem) : "memory");
+                    mbar_arrive(&sent_empty[t % NSENT]);
+                }
+                s = e;
+            }
+            if (*abort_flag) atomicExch(dq_sem + static_cast<size_t>(BHkv) * G * nq * 4, 1u);
         }
       }
         tc_fence_before();
@@ -697,20 +793,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int bhq = b * Hq + hk * G + g;
                 const int q0 = i * BQ;
                 const int bsel = s & 1;
+                // (DR = 64, deterministic variant: warps 6-7 hold K's zero-filled half of dQ^T)
+                if constexpr (DET) {
+                    // a free hand-over slot (the passer at most NSENT steps behind), then this tile's
+                    // turn: key blocks jb + 1 .. jtop add to it before this one; both waited for
+                    // before the tile is read from TMEM, while the tensor core forms it
+                    if (s >= NSENT &&
+                        !__all_sync(0xffffffffu, mbar_wait(&sent_empty[s % NSENT], ((s / NSENT) - 1) & 1,
+                                                           abort_flag, status)))
+                        break;
+                    const int jtop = CAUSAL ? min(nkb - 1, (i * BQ) / BKV) : nkb - 1;
+                    if (dcol < DR &&
+                        !dq_turn_wait(dq_sem, static_cast<size_t>(bhq) * nq + i,
+                                      static_cast<size_t>(BHkv) * G * nq,
+                                      static_cast<unsigned>(jtop - jb), abort_flag, status))
+                        break;
+                }
                 if (!__all_sync(0xffffffffu, mbar_wait(&dq_full[bsel], (s >> 1) & 1, abort_flag, status))) break;
                 tc_fence_after();
                 uint32_t a[64];
                 tmem_ld_x64(tmem + lane_off + T_BUF + bsel * 128 + B_DQT, a);
                 tc_fence_before();
                 mbar_arrive(&dq_empty[bsel]);
-                const long long row0 = static_cast<long long>(bhq) * N + q0;   // first row of the tile
-                float *dst = dQacc + static_cast<size_t>(row0) * DR + dcol;
-                const int nvalid = min(BQ, qend - q0);   // rows of this tile inside the sequence
+                if (dcol < DR) {
+                    const long long row0 = static_cast<long long>(bhq) * N + q0;   // first row of the tile
+                    float *dst = dQacc + static_cast<size_t>(row0) * DR + dcol;
+                    const int nvalid = min(BQ, qend - q0);   // rows of this tile inside the sequence
 #pragma unroll
-                for (int c = 0; c < BQ; ++c)
-                    if (c < nvalid && in_bounds(row0 + c, rows_total, status))
-                        atomicAdd(dst + static_cast<size_t>(c) * DR, __uint_as_float(a[c]) * scale);
+                    for (int c = 0; c < BQ; ++c)
+                        if (c < nvalid && in_bounds(row0 + c, rows_total, status))
+                            atomicAdd(dst + static_cast<size_t>(c) * DR, __uint_as_float(a[c]) * scale);
+                }
+                // hand the step to the turn passer; each lane's arrival releases its own
+                // reductions to it
+                if constexpr (DET) mbar_arrive(&sent_full[s % NSENT]);
             }
+            if (DET && *abort_flag) atomicExch(dq_sem + static_cast<size_t>(BHkv) * G * nq * 4, 1u);
         }
         if constexpr (SPLIT_EPI) {
             // epilogue, dV half: dV rows -> bf16 -> smem over V (its first DR / 64 chunks; at
@@ -804,9 +922,9 @@ static int grid_for(long long work, int per_block, int num_sms) {
 }  // namespace bwd
 
 cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const void *dO, float *D,
-                                       float *dQacc, cudaStream_t stream) {
+                                       float *dQacc, cudaStream_t stream, size_t zero_tail_bytes) {
     const long long rows = static_cast<long long>(p.B) * p.Hq * p.N;
-    const long long acc4 = rows * p.d / 4;
+    const long long acc4 = rows * p.d / 4 + static_cast<long long>(zero_tail_bytes / 16);
     const int sms = num_sms();
     const int grid = bwd::grid_for(rows * (p.d / 8), 256, sms);
     bwd::bwd_preprocess_kernel<<<grid, 256, 0, stream>>>(
@@ -816,12 +934,12 @@ cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const vo
 }
 
 namespace bwd {
-template <bool MASK, bool DROP>
+template <bool MASK, bool DROP, bool DET = false>
 cudaError_t launch_main(const Problem &p, const CUtensorMap &tmQ, const CUtensorMap &tmK,
                         const CUtensorMap &tmV, const CUtensorMap &tmdO, const CUtensorMap &tmdK,
                         const CUtensorMap &tmdV, const CUtensorMap &tmdQ, const float *LSE,
                         const float *D, float *dQacc, const MaskArgs &mk, const DropoutArgs &dr,
-                        unsigned *status, cudaStream_t stream) {
+                        unsigned *dq_sem, unsigned *status, cudaStream_t stream) {
     if (p.d != 128 && p.d != 64) return cudaErrorInvalidValue;
     const int BHkv = p.B * p.Hkv;
     const long long nkb = (p.N + BKV - 1) / BKV;
@@ -830,25 +948,31 @@ cudaError_t launch_main(const Problem &p, const CUtensorMap &tmQ, const CUtensor
     // key blocks run (B2 H32 N4096: 16 heads, 2% faster and a fraction of the DRAM traffic), and
     // the last chunk is as full as the others (a lone last head left a long tail: +27% at
     // B1 Hkv8 N8192).
+    // Under a tile mask the key blocks' step counts follow the mask and can differ by far more
+    // than under causal masking (a sink block seen by every query next to window blocks seen by a
+    // few), so all KV heads form one chunk and every head's longest blocks start first (chunks of
+    // 4 heads left the last chunk's sink blocks as a tail: +55% at B1 H16 N16384 window + sink).
     int HC = 1;
     for (int h = 1; h <= BHkv; ++h)
         if (BHkv % h == 0 && static_cast<long long>(h) * nkb <= 4LL * num_sms()) HC = h;
+    if (MASK && mk.block_mask) HC = BHkv;
     const long long grid = nkb * BHkv;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (MASK && static_cast<long long>(p.Hq / p.Hkv) * ((p.N + BQ - 1) / BQ) > MAX_MASK_STEPS)
         return cudaErrorInvalidConfiguration;
-    const int smem = MASK ? Layout<128>::BYTES_MASK : DROP ? Layout<128>::BYTES_DROP : Layout<128>::BYTES;
+    const int smem = MASK ? Layout<128>::BYTES_MASK : DROP ? Layout<128>::BYTES_DROP
+                     : DET ? Layout<128>::BYTES_DET : Layout<128>::BYTES;
     const float scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634);
     using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                           CUtensorMap, const float *, const float *, float *, int, int, int, int, int,
-                          float, float, MaskArgs, DropoutArgs, unsigned *);
+                          float, float, MaskArgs, DropoutArgs, unsigned *, unsigned *);
     Kern kern;
     if (p.d == 128)
-        kern = p.causal ? bwd_main_kernel<128, 128, true, MASK, DROP>
-                        : bwd_main_kernel<128, 128, false, MASK, DROP>;
+        kern = p.causal ? bwd_main_kernel<128, 128, true, MASK, DROP, DET>
+                        : bwd_main_kernel<128, 128, false, MASK, DROP, DET>;
     else
-        kern = p.causal ? bwd_main_kernel<128, 64, true, MASK, DROP>
-                        : bwd_main_kernel<128, 64, false, MASK, DROP>;
+        kern = p.causal ? bwd_main_kernel<128, 64, true, MASK, DROP, DET>
+                        : bwd_main_kernel<128, 64, false, MASK, DROP, DET>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // the in-kernel register split needs at least REGS_NEEDED registers at launch
@@ -857,7 +981,7 @@ cudaError_t launch_main(const Problem &p, const CUtensorMap &tmQ, const CUtensor
     if (attr.numRegs * NUM_THREADS < REGS_NEEDED) return cudaErrorInvalidConfiguration;
     kern<<<static_cast<unsigned>(grid), NUM_THREADS, smem, stream>>>(
         tmQ, tmK, tmV, tmdO, tmdK, tmdV, tmdQ, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, HC, p.scale,
-        scale_log2, mk, dr, status);
+        scale_log2, mk, dr, dq_sem, status);
     return cudaGetLastError();
 }
 }  // namespace bwd
@@ -868,7 +992,19 @@ cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const
                                  const CUtensorMap &tmdQ, const float *LSE, const float *D,
                                  float *dQacc, unsigned *status, cudaStream_t stream) {
     return bwd::launch_main<false, false>(p, tmQ, tmK, tmV, tmdO, tmdK, tmdV, tmdQ, LSE, D, dQacc,
-                                          MaskArgs{}, DropoutArgs{}, status, stream);
+                                          MaskArgs{}, DropoutArgs{}, nullptr, status, stream);
+}
+
+cudaError_t launch_bwd_main_deterministic_bf16(const Problem &p, const CUtensorMap &tmQ,
+                                               const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                               const CUtensorMap &tmdO, const CUtensorMap &tmdK,
+                                               const CUtensorMap &tmdV, const CUtensorMap &tmdQ,
+                                               const float *LSE, const float *D, float *dQacc,
+                                               unsigned *dq_sem, unsigned *status,
+                                               cudaStream_t stream) {
+    return bwd::launch_main<false, false, true>(p, tmQ, tmK, tmV, tmdO, tmdK, tmdV, tmdQ, LSE, D,
+                                                dQacc, MaskArgs{}, DropoutArgs{}, dq_sem, status,
+                                                stream);
 }
 
 cudaError_t launch_bwd_main_masked_bf16(const Problem &p, const CUtensorMap &tmQ,
@@ -878,7 +1014,7 @@ cudaError_t launch_bwd_main_masked_bf16(const Problem &p, const CUtensorMap &tmQ
                                         const float *LSE, const float *D, float *dQacc,
                                         const MaskArgs &mk, unsigned *status, cudaStream_t stream) {
     return bwd::launch_main<true, false>(p, tmQ, tmK, tmV, tmdO, tmdK, tmdV, tmdQ, LSE, D, dQacc, mk,
-                                         DropoutArgs{}, status, stream);
+                                         DropoutArgs{}, nullptr, status, stream);
 }
 
 cudaError_t launch_bwd_main_dropout_bf16(const Problem &p, const CUtensorMap &tmQ,
@@ -888,7 +1024,7 @@ cudaError_t launch_bwd_main_dropout_bf16(const Problem &p, const CUtensorMap &tm
                                          const float *LSE, const float *D, float *dQacc,
                                          const DropoutArgs &dr, unsigned *status, cudaStream_t stream) {
     return bwd::launch_main<false, true>(p, tmQ, tmK, tmV, tmdO, tmdK, tmdV, tmdQ, LSE, D, dQacc,
-                                         MaskArgs{}, dr, status, stream);
+                                         MaskArgs{}, dr, nullptr, status, stream);
 }
 
 cudaError_t launch_bwd_dq_convert_bf16(const Problem &p, const float *dQacc, void *dQ,

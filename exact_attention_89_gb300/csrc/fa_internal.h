@@ -97,9 +97,11 @@ cudaError_t launch_tf32x3_bwd(const Problem &p, const CUtensorMap *maps, const f
                               float *dQ, float *dK, float *dV, float *Dvec, unsigned *status,
                               cudaStream_t stream);
 
-// K2: D = rowsum(dO * O) in fp32 and zeroing of the fp32 dQ accumulator.
+// K2: D = rowsum(dO * O) in fp32 and zeroing of the fp32 dQ accumulator, plus zero_tail_bytes
+// (a multiple of 16) right after it (the deterministic variant's counters).
 cudaError_t launch_bwd_preprocess_bf16(const Problem &p, const void *O, const void *dO, float *D,
-                                       float *dQacc, cudaStream_t stream);
+                                       float *dQacc, cudaStream_t stream,
+                                       size_t zero_tail_bytes = 0);
 
 // K3: bf16 backward main loop on tcgen05.  tmQ / tmdO use a [64, 64, 1] box; tmK, tmV, tmdK,
 // tmdV a [64, 128, 1] box.  Accumulates scale * dS K into dQacc with fp32 reductions: per
@@ -111,6 +113,16 @@ cudaError_t launch_bwd_main_bf16(const Problem &p, const CUtensorMap &tmQ, const
                                  const CUtensorMap &tmdQ, const float *LSE, const float *D,
                                  float *dQacc, unsigned *status,
                                  cudaStream_t stream);
+
+// K3 with the dQ reductions in a fixed order (bitwise reproducible dQ): dq_sem holds
+// B * Hq * ceil(N / 64) * 4 zeroed turn counters and one zeroed abort word after them.
+cudaError_t launch_bwd_main_deterministic_bf16(const Problem &p, const CUtensorMap &tmQ,
+                                               const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                               const CUtensorMap &tmdO, const CUtensorMap &tmdK,
+                                               const CUtensorMap &tmdV, const CUtensorMap &tmdQ,
+                                               const float *LSE, const float *D, float *dQacc,
+                                               unsigned *dq_sem, unsigned *status,
+                                               cudaStream_t stream);
 
 // K3 under a general mask.  Needs (Hq / Hkv) * ceil(N / 64) <= MASK_BWD_MAX_STEPS (the CTA's
 // step list lives in shared memory).

@@ -9,9 +9,11 @@ Low-level functions (same names and argument order as ``include/flashattn.h``):
     fa_get_device_status, fa_status_string, fa_bwd_noalloc, fa_fwd_split, fa_merge,
     fa_fwd_masked, fa_bwd_masked, fa_fwd_dropout, fa_bwd_dropout, fa_dropout_mask,
     fa_fwd_kvouter, fa_fwd_kvouter_workspace_bytes, fa_fwd_fp32_tc, fa_fwd_fp32_tc_workspace_bytes,
-    fa_bwd_fp32_tc, fa_bwd_fp32_tc_workspace_bytes
+    fa_bwd_fp32_tc, fa_bwd_fp32_tc_workspace_bytes, fa_bwd_deterministic,
+    fa_bwd_deterministic_workspace_bytes
 Convenience wrappers that allocate outputs with torch:
-    attention_forward, attention_backward, attention_forward_split
+    attention_forward, attention_backward (deterministic=True: fa_bwd_deterministic),
+    attention_forward_split
 """
 from __future__ import annotations
 
@@ -39,7 +41,8 @@ EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_fp32", "fa_bwd
             "fa_merge", "fa_fwd_masked", "fa_bwd_masked", "fa_fwd_dropout", "fa_bwd_dropout",
             "fa_dropout_mask", "fa_fwd_kvouter", "fa_fwd_kvouter_workspace_bytes",
             "fa_fwd_fp32_tc", "fa_fwd_fp32_tc_workspace_bytes", "fa_bwd_fp32_tc",
-            "fa_bwd_fp32_tc_workspace_bytes")
+            "fa_bwd_fp32_tc_workspace_bytes", "fa_bwd_deterministic",
+            "fa_bwd_deterministic_workspace_bytes")
 
 # Side of the square tiles of a block mask (FA_MASK_BLOCK).
 MASK_BLOCK = 128
@@ -87,6 +90,10 @@ def lib() -> ctypes.CDLL:
             L.fa_status_string.restype = ctypes.c_char_p
             L.fa_bwd_noalloc.argtypes = [vp] * 9 + dims + [vp]
             L.fa_bwd_noalloc.restype = i
+            L.fa_bwd_deterministic.argtypes = [vp] * 9 + dims + [vp, sz, vp]
+            L.fa_bwd_deterministic.restype = i
+            L.fa_bwd_deterministic_workspace_bytes.argtypes = [i, i, i, i]
+            L.fa_bwd_deterministic_workspace_bytes.restype = sz
             L.fa_fwd_split.argtypes = [vp] * 5 + dims + [i, vp]
             L.fa_fwd_split.restype = i
             L.fa_merge.argtypes = [vp, vp, i, ctypes.c_longlong, i, vp, i, vp, vp]
@@ -166,6 +173,23 @@ def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, causal: bool, scale: float, workspac
                       _ptr(dK), _ptr(dV), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
                       _ptr(workspace), wbytes, _stream(stream))
     return _check(st, "fa_bwd", check)
+
+
+def fa_bwd_deterministic_workspace_bytes(B: int, Hq: int, N: int, d: int) -> int:
+    return int(lib().fa_bwd_deterministic_workspace_bytes(B, Hq, N, d))
+
+
+def fa_bwd_deterministic(Q, K, V, O, dO, LSE, dQ, dK, dV, causal: bool, scale: float, workspace,
+                         stream=None, check: bool = True) -> int:
+    """fa_bwd with the dQ reductions in a fixed order (bitwise reproducible dQ); the workspace
+    holds fa_bwd_deterministic_workspace_bytes bytes."""
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().fa_bwd_deterministic(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE),
+                                    _ptr(dQ), _ptr(dK), _ptr(dV), B, Hq, Hkv, N, d,
+                                    int(bool(causal)), float(scale), _ptr(workspace), wbytes,
+                                    _stream(stream))
+    return _check(st, "fa_bwd_deterministic", check)
 
 
 def fa_bwd_noalloc(Q, K, V, O, dO, LSE, dQ, dK, dV, causal: bool, scale: float, stream=None,
@@ -457,15 +481,21 @@ def attention_backward_fp32_tc(Q, K, V, O, dO, LSE, causal: bool, scale: float |
 
 
 def attention_backward(Q, K, V, O, dO, LSE, causal: bool, scale: float | None = None,
-                       workspace=None, stream=None):
-    """Allocates dQ, dK, dV (and the workspace unless given) and runs the backward."""
+                       workspace=None, stream=None, deterministic: bool = False):
+    """Allocates dQ, dK, dV (and the workspace unless given) and runs the backward
+    (deterministic: the bf16 backward with the dQ reductions in a fixed order)."""
     if scale is None:
         scale = 1.0 / math.sqrt(Q.shape[-1])
     B, Hq, N, d = Q.shape
+    if deterministic and Q.dtype == torch.float32:
+        raise ValueError("the deterministic backward is the bf16 one; the fp32 backward "
+                         "(fa_bwd_fp32) is reproducible as it is")
     if workspace is None:
-        workspace = torch.empty(fa_bwd_workspace_bytes(B, Hq, N, d), dtype=torch.uint8,
-                                device=Q.device)
+        size = (fa_bwd_deterministic_workspace_bytes if deterministic else
+                fa_bwd_workspace_bytes)(B, Hq, N, d)
+        workspace = torch.empty(size, dtype=torch.uint8, device=Q.device)
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
-    f = fa_bwd_fp32 if Q.dtype == torch.float32 else fa_bwd
+    f = (fa_bwd_fp32 if Q.dtype == torch.float32 else
+         fa_bwd_deterministic if deterministic else fa_bwd)
     f(Q, K, V, O, dO, LSE, dQ, dK, dV, causal, scale, workspace, stream)
     return dQ, dK, dV

@@ -215,8 +215,8 @@ size_t fa_bwd_workspace_bytes(int B, int Hq, int N, int d);
  *   Q, K, V, O, dO: bf16 inputs as in fa_fwd (O is the forward output; D is formed from it).
  *   LSE: the fp32 LSE fa_fwd wrote for these inputs.
  *   dQ [B,Hq,N,d], dK [B,Hkv,N,d], dV [B,Hkv,N,d]: bf16 outputs (dK, dV summed over the group).
- *   d must be 64 or 128 (d = 64 runs the d = 128 tiling on zero-padded operands, so it costs
- *   the FLOPs of d = 128).
+ *   d must be 64 or 128 (at d = 64 the dQ^T product keeps the 128-row tiling over a zero-filled
+ *   half of K; the other products run over the 64 real columns).
  *   workspace: caller-owned device scratch of at least fa_bwd_workspace_bytes(B,Hq,N,d) bytes,
  *   16-byte aligned; its contents on entry do not matter and are clobbered.
  *   Calls that share one workspace must not overlap on the GPU.
@@ -225,6 +225,34 @@ fa_status fa_bwd(const void *Q, const void *K, const void *V, const void *O, con
                  const float *LSE, void *dQ, void *dK, void *dV,
                  int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                  void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd_deterministic needs: fa_bwd_workspace_bytes(B,Hq,N,d), then
+ * 16 bytes per 64-row query tile of every (batch, query head) for the turn counters, then 16
+ * bytes for an abort word.  Returns 0 for invalid sizes and SIZE_MAX on overflow.
+ */
+size_t fa_bwd_deterministic_workspace_bytes(int B, int Hq, int N, int d);
+
+/*
+ * fa_bwd with a dQ that is bitwise the same on every call with the same inputs (same GPU model
+ * and library build).  Gradients by recompute as in the "Flash Attention backward" section of
+ * the mzeromiko blog ("Attention's hidden recurrence"); fa_bwd adds the key blocks' shares of
+ * dQ into its fp32 accumulator in whatever order the CTAs reach it, so its dQ can differ in the
+ * last bits from call to call.  Here the shares of each 64-row query tile are added in one fixed
+ * order (descending key block), each CTA waiting on a counter in the workspace for its turn;
+ * dK and dV are computed as in fa_bwd (they need no cross-CTA sum and are reproducible there
+ * too).  The results agree with fa_bwd's to the rounding of the fp32 sums.
+ *   Arguments, layouts, results and errors are those of fa_bwd, except that the workspace must
+ *   hold fa_bwd_deterministic_workspace_bytes(B,Hq,N,d) bytes.  Slower than fa_bwd: the CTAs of
+ *   a head are launched in the reduction order (the longest last), a CTA can wait for its turn,
+ *   and at d = 64 dQ goes out through per-element reductions instead of bulk tile reductions.
+ *   Every wait for a turn is bounded; one that runs out reports FA_ERR_DEVICE_TIMEOUT through
+ *   fa_get_device_status and ends the other CTAs' waits at once (dQ is then not valid).
+ */
+fa_status fa_bwd_deterministic(const void *Q, const void *K, const void *V, const void *O,
+                               const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                               int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                               void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Size of the fixed device scratch that fa_bwd_noalloc uses: 64 MiB.

@@ -56,17 +56,30 @@ def test_workspace_bytes(built_lib):
     assert st == built_lib.FA_ERR_WORKSPACE
 
 
+def test_deterministic_workspace_bytes(built_lib):
+    f, g = built_lib.fa_bwd_deterministic_workspace_bytes, built_lib.fa_bwd_workspace_bytes
+    # the fa_bwd workspace, then 16 bytes of turn counters per 64-row query tile, then the abort
+    # word padded to 16 bytes
+    for B, Hq, N, d in [(2, 32, 4096, 128), (1, 1, 1, 64), (3, 5, 1000, 64), (1, 16, 32768, 128)]:
+        assert f(B, Hq, N, d) == g(B, Hq, N, d) + B * Hq * ((N + 63) // 64) * 16 + 16
+    assert f(0, 1, 1, 1) == 0 and f(1, 1, -1, 64) == 0
+    big = 2 ** 31 - 1
+    assert f(big, big, big, 128) == 2 ** 64 - 1
+    assert f(big, big, 1, 1) == 2 ** 64 - 1
+
+
 def fwd(L, Q=A, K=A, V=A, O=A, LSE=A, B=1, Hq=2, Hkv=1, N=64, d=128, causal=1, scale=0.1, fp32=False):
     fn = L.fa_fwd_fp32 if fp32 else L.fa_fwd
     return fn(Q, K, V, O, LSE, B, Hq, Hkv, N, d, causal, scale, None)
 
 
 def bwd(L, ptrs=None, B=1, Hq=2, Hkv=1, N=64, d=128, causal=1, scale=0.1, ws=A, wbytes=None,
-        fp32=False):
+        fp32=False, det=False):
     ptrs = ptrs or [A] * 9
     if wbytes is None:
-        wbytes = L.fa_bwd_workspace_bytes(B, Hq, N, d)
-    fn = L.fa_bwd_fp32 if fp32 else L.fa_bwd
+        wbytes = (L.fa_bwd_deterministic_workspace_bytes if det else
+                  L.fa_bwd_workspace_bytes)(B, Hq, N, d)
+    fn = L.fa_bwd_fp32 if fp32 else L.fa_bwd_deterministic if det else L.fa_bwd
     return fn(*ptrs, B, Hq, Hkv, N, d, causal, scale, ws, wbytes, None)
 
 
@@ -109,6 +122,25 @@ def test_backward_rejects_invalid_arguments(built_lib, fp32):
     assert bwd(L, wbytes=need - 1, fp32=fp32) == E.FA_ERR_WORKSPACE
     assert bwd(L, ws=None, fp32=fp32) == E.FA_ERR_WORKSPACE
     assert bwd(L, ws=MIS, fp32=fp32) == E.FA_ERR_WORKSPACE
+
+
+def test_deterministic_backward_rejects_invalid_arguments(built_lib):
+    L = built_lib.lib()
+    E = built_lib
+    assert bwd(L, B=0, det=True) == E.FA_ERR_INVALID_ARG
+    assert bwd(L, Hq=4, Hkv=3, det=True) == E.FA_ERR_INVALID_ARG
+    assert bwd(L, scale=math.nan, det=True) == E.FA_ERR_INVALID_ARG
+    assert bwd(L, d=96, det=True) == E.FA_ERR_UNSUPPORTED
+    for k in range(9):
+        ptrs = [A] * 9
+        ptrs[k] = MIS
+        assert bwd(L, ptrs, det=True) == E.FA_ERR_MISALIGNED
+    need = L.fa_bwd_deterministic_workspace_bytes(1, 2, 64, 128)
+    # fa_bwd's workspace size is not enough: the counters need their own bytes
+    assert bwd(L, wbytes=L.fa_bwd_workspace_bytes(1, 2, 64, 128), det=True) == E.FA_ERR_WORKSPACE
+    assert bwd(L, wbytes=need - 1, det=True) == E.FA_ERR_WORKSPACE
+    assert bwd(L, ws=None, det=True) == E.FA_ERR_WORKSPACE
+    assert bwd(L, ws=MIS, det=True) == E.FA_ERR_WORKSPACE
 
 
 def test_split_forward_rejects_invalid_arguments(built_lib):
