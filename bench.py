@@ -575,6 +575,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="only warm-up and timed steps (no clock load, e2e or cpu baseline); "
                          "for profiler runs")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager calls instead of replays of the step captured in a CUDA graph")
     ap.add_argument("--oracle-table", default=None,
                     help="with --impl reference: time the oracle's forward and backward per "
                          "workload ('all' or a comma-separated list) instead of the bench line")
@@ -690,6 +692,18 @@ def main():
     if st != fa.FA_OK:
         raise RuntimeError("device status after warm-up: " + fa.fa_status_string(st))
 
+    # One step captured in a CUDA graph: the timed steps replay it, with no host-side launch path
+    # between the kernels of a step or between steps (the entry points allocate nothing and never
+    # synchronise after their first call).  --no-graph or --no-extras time eager calls instead.
+    graph = None
+    if not (args.no_graph or args.no_extras):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+
     # ---------------------------------------------------------------- device-timed region
     bus = None
     try:
@@ -726,16 +740,32 @@ def main():
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
+    # the same K steps as replays of the captured graph: the step time `value` reports
+    graph_total_ms = None
+    if graph is not None:
+        barrier()
+        torch.cuda.synchronize()
+        g_s = torch.cuda.Event(enable_timing=True)
+        g_e = torch.cuda.Event(enable_timing=True)
+        g_s.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        g_e.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        graph_total_ms = g_s.elapsed_time(g_e)
     if not args.no_extras:
         load_for(0.6)
     clocks = sampler.stop()
     st = fa.fa_get_device_status()
     if st != fa.FA_OK:
         raise RuntimeError("device status after timed region: " + fa.fa_status_string(st))
-    total_ms = t_start.elapsed_time(t_end)
+    # eager steps: their per-launch events give the split of a step between its kernels
+    eager_total_ms = max_over_ranks(t_start.elapsed_time(t_end), ws, dev)
     first_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / args.steps
     second_ms = sum(b.elapsed_time(c) for _, b, c in ev) / args.steps
-    total_ms = max_over_ranks(total_ms, ws, dev)
+    total_ms = (max_over_ranks(graph_total_ms, ws, dev) if graph_total_ms is not None
+                else eager_total_ms)
 
     # FLOPs: the formula 4 B Hq N^2 d (/2 causal, x2.5 backward), or under a general mask
     # 4 d per allowed (query, key) pair
@@ -1005,6 +1035,12 @@ def main():
                 "fwd_bwd_frac_of_nominal_peak": (value / ws / NOMINAL_BF16_TFLOPS
                                                  if w.backward else None),
                 "other_workloads": others,
+                # how the K timed steps ran, and the same steps as eager calls
+                "timed_as": ("replays of one step captured in a CUDA graph" if graph is not None
+                             else "eager calls"),
+                "eager": {"ms_per_step": eager_total_ms / args.steps,
+                          "value": whole_job_tflops(ws, flops_step, args.steps, eager_total_ms),
+                          "unit": "TFLOP/s"},
                 # (not measured under --no-extras: null rather than NaN, which is not JSON)
                 "e2e": {"value": None if math.isnan(e2e_ms) else e2e_value, "unit": "TFLOP/s",
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
