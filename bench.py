@@ -742,18 +742,19 @@ def main():
     barrier()
     # the same K steps as replays of the captured graph: the step time `value` reports
     graph_total_ms = None
+    step_times = sorted(e0.elapsed_time(e2) for e0, _, e2 in ev)   # the replays' below, if any
     if graph is not None:
         barrier()
         torch.cuda.synchronize()
-        g_s = torch.cuda.Event(enable_timing=True)
-        g_e = torch.cuda.Event(enable_timing=True)
-        g_s.record(stream)
-        for _ in range(args.steps):
+        g_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        g_ev[0].record(stream)
+        for i in range(args.steps):
             graph.replay()
-        g_e.record(stream)
+            g_ev[i + 1].record(stream)
         torch.cuda.synchronize()
         barrier()
-        graph_total_ms = g_s.elapsed_time(g_e)
+        graph_total_ms = g_ev[0].elapsed_time(g_ev[-1])
+        step_times = sorted(a.elapsed_time(b) for a, b in zip(g_ev[:-1], g_ev[1:]))
     if not args.no_extras:
         load_for(0.6)
     clocks = sampler.stop()
@@ -1017,6 +1018,9 @@ def main():
                 "value": value,
                 "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+                # per-step spread of the timed steps (this rank): median and fastest
+                "ms_per_step_median": step_times[len(step_times) // 2],
+                "ms_per_step_min": step_times[0],
                 "scaling": "weak", "vs_baseline": None,
                 "dtype": "f32" if w.tensor_fp32 else "bf16", "data": "synthetic",
                 "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
