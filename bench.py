@@ -59,10 +59,10 @@ NCU_TRAFFIC = {
     "fa_bwd_sm103a.cu:53515684288a829d:varlen_n8192": 3.681e9,
     # fa_bwd_dropout, three kernels: 0.206 + 0.634 + 0.160 GB
     "fa_bwd_sm103a.cu:53515684288a829d:dropout_n4096": 1.001e9,
-    # split forward on splitkv_n32768: 25.3 MB read + 0.2 MB write (partials stay in L2)
-    "fa_fwd_sm103a.cu:b18fda5356d2798b:splitkv_n32768": 2.55e7,
+    # split forward on splitkv_n32768: 25.4 MB read + 0.3 MB write (partials stay in L2)
+    "fa_fwd_sm103a.cu:e4f59c3f62dbbcd0:splitkv_n32768": 2.57e7,
     # forward at head dim 64 on fwd_d64: 25.2 MB read (Q, K, V), O written back from L2 later
-    "fa_fwd_sm103a.cu:b18fda5356d2798b:fwd_d64": 2.52e7,
+    "fa_fwd_sm103a.cu:e4f59c3f62dbbcd0:fwd_d64": 2.52e7,
     # key/value-outer forward: 2.374 GB read + 1.765 GB write
     "fa_fwd_kvouter_sm103a.cu:e1fd8857363ec7a5:kvouter_n4096": 4.139e9,
     # fp32 tensor-core backward: split rows 0.343 GB, split transposes 0.239 GB, dq pass

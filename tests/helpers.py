@@ -54,6 +54,22 @@ BF16_O_MEAN_ABS = 1e-3
 BF16_LSE_MAX_ABS = 1e-3
 BF16_GRAD_REL_FRO = 2e-2
 
+# bf16 unit roundoff (8-bit significand, round to nearest even): |bf16(x) - x| <= 2^-8 |x|.
+BF16_U = 2.0 ** -8
+
+
+def bf16_forward_allowed(o_ref, oabs_ref):
+    """Per-element bound on |O - O_ref| for the bf16 forward: BF16_O_MAX_ABS, or where larger the
+    worst case of the arithmetic the method prescribes, whatever the kernel.  P is rounded to bf16
+    (each weight within u of itself) before P V, while the normaliser sums the unrounded weights,
+    so before the output rounding O is within E = u (sum_j P_j |V_j| + |O_ref|); the bf16 output
+    then adds at most u |O_ref + E|.  o_ref is the exact O, oabs_ref the same attention applied to
+    |V| (sum_j P_j |V_j|).  Where |O_ref| >= 4 half a bf16 ulp alone (0.0156) exceeds 1e-2, so the
+    stated bound cannot hold for every bf16 output there."""
+    o_ref = np.abs(_np(o_ref))
+    e = BF16_U * (_np(oabs_ref) + o_ref)
+    return np.maximum(BF16_O_MAX_ABS, e + BF16_U * (o_ref + e))
+
 
 def sample_rows(B, H, N, n, seed):
     """Flat row indices (b*H + h)*N + i: first / last rows of every tile edge plus random ones."""

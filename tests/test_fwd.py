@@ -1,9 +1,12 @@
 """bf16 forward on tcgen05 (fa_fwd) against the fp64 oracle on the same seeded inputs.
 
 Tolerances: O max abs <= 1e-2 and mean abs <= 1e-3; LSE max abs <= 1e-3.
-Small shapes and the full-size workloads up to N = 8192 are compared over every element; the
-N = 32768 workload over every row of four whole KV groups drawn by seed plus rows sampled over
-all heads (its oracle computes one row at a time)."""
+Small shapes and every full-size workload are compared over every element.  On the N = 32768
+workload (queries scaled by 4, so rows put nearly all their weight on a few keys and |O| reaches
+4 and more) a few elements cannot be within 1e-2 of the exact value in the arithmetic the method
+prescribes (P rounded to bf16, a bf16 output: half a bf16 ulp alone is 0.0156 for |O| >= 4);
+there each element is held to the worst case of that arithmetic instead (helpers.
+bf16_forward_allowed), and the test prints how many elements exceed 1e-2."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +14,7 @@ import torch
 import helpers
 from exact_attention_89_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
 from helpers import (BF16_LSE_MAX_ABS, BF16_O_MAX_ABS, BF16_O_MEAN_ABS, ErrorTally,
-                     chosen_groups, f64, group_slice, max_abs, mean_abs, sample_rows)
+                     bf16_forward_allowed, f64, group_slice, max_abs, mean_abs)
 
 pytestmark = pytest.mark.gpu
 
@@ -81,7 +84,7 @@ def test_forward_fwd_d64_workload(flash, oracle_mod):
 # Workloads whose every element the oracle checks (a few heads per oracle call), and the one
 # too long for that: its whole-group check covers KV groups drawn by seed.
 EVERY_ELEMENT = ["causal_n4096", "gqa_n8192", "causal_d64_n4096"]
-WHOLE_GROUPS = {"long_n32768": 4}
+WHOLE_GROUPS = ["long_n32768"]
 
 
 @pytest.mark.parametrize("name", EVERY_ELEMENT)
@@ -107,29 +110,42 @@ def test_forward_full_size_every_element(flash, oracle_mod, name):
             and tl.max_abs <= BF16_LSE_MAX_ABS), (name, to.max_abs, to.mean_abs, tl.max_abs)
 
 
-@pytest.mark.parametrize("name", sorted(WHOLE_GROUPS))
+@pytest.mark.parametrize("name", WHOLE_GROUPS)
 def test_forward_full_size_whole_groups(flash, oracle_mod, name):
-    """The longest workload: every row of KV groups drawn by seed (groups are independent, so
-    this is exact for those heads), plus rows sampled over all heads."""
+    """The longest workload, every element, one KV group per oracle call (the oracle computes it
+    row by row).  Each element within 1e-2, or within the worst case of the prescribed bf16
+    arithmetic where that is larger (the oracle's attention applied to |V| gives the weighted
+    |V| the bound needs)."""
     w = WORKLOADS[name]
     Q, K, V, _ = workload_inputs(w)
     O, LSE = gpu_forward(flash, Q, K, V, w.causal, w.scale)
     G = w.Hq // w.Hkv
     to, tl = ErrorTally(), ErrorTally()
-    groups = chosen_groups(w.B * w.Hkv, WHOLE_GROUPS[name], w.seed)
-    for bk in groups:
+    over, beyond, worst_ratio = 0, 0, 0.0
+    for bk in range(w.B * w.Hkv):
         b, hk = divmod(bk, w.Hkv)
         q, k, v, _ = group_slice(Q, K, V, None, b, hk)
         rows = np.arange(G * w.N, dtype=np.int64)
-        Oo, Lo = oracle_mod.forward_rows(f64(q), f64(k), f64(v), w.causal, w.scale, rows)
-        to.add(O[b, hk * G:(hk + 1) * G].reshape(-1, w.d), Oo, label="group %d" % bk)
+        q64, k64, v64 = f64(q), f64(k), f64(v)
+        Oo, Lo = oracle_mod.forward_rows(q64, k64, v64, w.causal, w.scale, rows)
+        Oa, _ = oracle_mod.forward_rows(q64, k64, np.abs(v64), w.causal, w.scale, rows)
+        got = O[b, hk * G:(hk + 1) * G].reshape(-1, w.d)
+        err = np.abs(f64(got) - Oo)
+        allowed = bf16_forward_allowed(Oo, Oa)
+        over += int((err > BF16_O_MAX_ABS).sum())
+        beyond += int((err > allowed).sum())
+        worst_ratio = max(worst_ratio, float((err / allowed).max()))
+        to.add(got, Oo, label="group %d" % bk)
         tl.add(LSE[b, hk * G:(hk + 1) * G].reshape(-1), Lo, label="group %d" % bk)
-    rows = sample_rows(w.B, w.Hq, w.N, 96, seed=w.seed)
-    Or, Lr = oracle_mod.forward_rows(f64(Q), f64(K), f64(V), w.causal, w.scale, rows)
-    to.add(O.reshape(-1, w.d)[rows], Or)
-    tl.add(LSE.reshape(-1)[rows], Lr)
-    print("[parity] %s forward, groups %s + %d sampled rows: O max abs %.3e mean abs %.3e, "
-          "LSE max abs %.3e; worst O element %s" % (name, groups, len(rows), to.max_abs, to.mean_abs,
-                                                    tl.max_abs, to.worst))
-    assert (to.max_abs <= BF16_O_MAX_ABS and to.mean_abs <= BF16_O_MEAN_ABS
-            and tl.max_abs <= BF16_LSE_MAX_ABS), (name, to.max_abs, to.mean_abs, tl.max_abs)
+    print("[parity] %s forward, every element of all %d KV groups: O max abs %.3e mean abs %.3e, "
+          "LSE max abs %.3e; worst O element %s; %d elements above %.0e, %d above the bound of "
+          "the prescribed arithmetic (largest error / bound %.3f)"
+          % (name, w.B * w.Hkv, to.max_abs, to.mean_abs, tl.max_abs, to.worst, over,
+             BF16_O_MAX_ABS, beyond, worst_ratio))
+    assert beyond == 0, (name, beyond, worst_ratio)
+    # The bound is a worst case, loose where it applies; as a guard against a regression hiding
+    # under it, elements above 1e-2 must stay rare (a kernel-faithful model of the current
+    # arithmetic puts 13 to 15 of the 537 M elements there).
+    assert over <= 1e-6 * O.numel(), (name, over)
+    assert to.mean_abs <= BF16_O_MEAN_ABS and tl.max_abs <= BF16_LSE_MAX_ABS, (
+        name, to.mean_abs, tl.max_abs)
