@@ -25,11 +25,12 @@
 // the tensor core's work on the other.  Inside a buffer, P^T and dS^T (bf16) are both written over
 // the S^T half, which frees the dP^T half for the dQ^T product of the same step.
 //
-// Roles (384 threads): warps 0-3 softmax-gradient (and the dK / dV epilogue), warps 4-7 dQ drain
-// (at head dim 64 also the dV half of the epilogue), warp 8 TMA, warp 9 the S^T / dP^T MMAs and
-// warp 10 the dQ^T / dV / dK MMAs (one elected lane each), warp 11 idle (it completes the third
-// warpgroup for the register split) except in the deterministic variant, where it passes the dQ
-// turns.
+// Roles (512 threads at head dim 128, 384 at 64): warps 0-3 softmax-gradient (and the dK / dV
+// epilogue), warps 4-7 dQ drain (query columns 0-31 of each dQ^T tile; at head dim 64 all 64 and
+// the dV half of the epilogue), warps 12-15 (head dim 128) the second dQ drain warpgroup
+// (columns 32-63), warp 8 TMA, warp 9 the S^T / dP^T MMAs and warp 10 the dQ^T / dV / dK MMAs
+// (one elected lane each), warp 11 idle (it completes the third warpgroup for the register split)
+// except in the deterministic variant, where it passes the dQ turns.
 // TMEM (512 columns): dK [0,128), dV [128,256), buffer b at 256 + 128 b:
 //   [+0,+64) S^T -> P^T [+0,+32) and dS^T [+32,+64);  [+64,+128) dP^T -> dQ^T.
 #include <algorithm>
@@ -45,7 +46,7 @@ namespace bwd {
 constexpr int BKV = 128;          // keys per CTA (= TMEM lanes)
 constexpr int BQ = 64;            // query rows per step
 constexpr int NSQ = 3;            // Q / dO ring stages
-constexpr int NUM_THREADS = 384;   // three warpgroups
+constexpr int NUM_THREADS = 384;   // three warpgroups (four with a second drain warpgroup)
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;       // TMEM allocator; issues S^T and dP^T
 constexpr int WARP_MMA2 = 10;     // issues dQ^T, dV and dK
@@ -53,7 +54,18 @@ constexpr int WARP_PASS = 11;     // deterministic variant: passes the dQ turns
 constexpr int NSENT = 4;          // steps the drain warps may run ahead of the turn passer
 // Register split: softmax-gradient warpgroup grows; dQ drain and TMA/MMA warpgroups shrink.
 constexpr uint32_t REGS_GRAD = 256, REGS_DRAIN = 88, REGS_OTHER = 80;
-constexpr int REGS_NEEDED = 128 * (REGS_GRAD + REGS_DRAIN + REGS_OTHER);
+// Head dim 128: a second dQ drain warpgroup (warps 12-15) takes query columns 32-63 of each dQ^T
+// tile, the first one columns 0-31, so each drain warp issues half of a step's per-element
+// reductions (and, with dropout, half of its keep decisions) and reads its TMEM buffer out
+// sooner.  (At head dim 64 dQ leaves as one bulk reduction per step.)
+template <int DR>
+struct Roles {
+    static constexpr bool DRAIN2 = DR == 128;
+    static constexpr int THREADS = DRAIN2 ? 512 : NUM_THREADS;
+    static constexpr int DRAIN_THREADS = DRAIN2 ? 256 : 128;
+    // registers the split needs at launch: 65536 with the second drain warpgroup
+    static constexpr int REGS_NEEDED = 128 * (REGS_GRAD + REGS_OTHER) + DRAIN_THREADS * REGS_DRAIN;
+};
 constexpr float LOG2E = 1.4426950408889634f;
 // Steps (query head of the group x query tile) a masked CTA can list in shared memory.
 constexpr int MAX_MASK_STEPS = MASK_BWD_MAX_STEPS;
@@ -84,8 +96,8 @@ struct Layout {
     // by the dQ drain warps one step ahead, and their km_full[2] / km_empty[2] barriers.
     static constexpr int KEEP_OFF = ABORT_OFF + 16;
     static constexpr int KM_BAR_OFF = KEEP_OFF + 2 * BKV * 8;
-    static constexpr int XCH_OFF = KM_BAR_OFF + 4 * 8;            // [BKV] quad exchange words
-    static constexpr int BYTES_DROP = XCH_OFF + BKV * 8 + 1024;
+    static constexpr int XCH_OFF = KM_BAR_OFF + 4 * 8;   // [2 drain warpgroups][BKV] quad exchange
+    static constexpr int BYTES_DROP = XCH_OFF + 2 * BKV * 8 + 1024;
     // Deterministic variant: sent_full[NSENT] / sent_empty[NSENT], the drain warps' hand-over of
     // finished steps to the turn passer.
     static constexpr int SENT_OFF = ABORT_OFF + 16;
@@ -215,7 +227,7 @@ __device__ __forceinline__ int first_q_tile(int jb) {
 // DET = true: the deterministic variant (ordered dQ reductions, above); dq_sem holds B * Hq *
 // ceil(N / 64) * 4 counters followed by the call's abort word.
 template <int D, int DR, bool CAUSAL, bool MASK, bool DROP, bool DET>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
@@ -241,6 +253,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // the drain warps' per-step work is the short staged reduction (DR = 64); at DR = 128 the
     // drain warps are still busy with the last step's per-element reductions then.
     constexpr bool SPLIT_EPI = DQ_TMA;
+    using R = Roles<DR>;
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -348,7 +361,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&s_full[k], 1);
             mbar_init(&p_full[k], 128);
             mbar_init(&dq_full[k], 1);
-            mbar_init(&dq_empty[k], 128);
+            mbar_init(&dq_empty[k], R::DRAIN_THREADS);
         }
         mbar_init(acc_full, 1);
         mbar_init(mma_done, 2);            // one commit from each issuer
@@ -356,11 +369,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(&kvd[1], 1);
         if (DROP) {
             uint64_t *kb = reinterpret_cast<uint64_t *>(smem + L::KM_BAR_OFF);
-            for (int k = 0; k < 4; ++k) mbar_init(&kb[k], 128);
+            for (int k = 0; k < 4; ++k) mbar_init(&kb[k], k < 2 ? R::DRAIN_THREADS : 128);   // full, empty
         }
         if (DET) {
             for (int k = 0; k < NSENT; ++k) {
-                mbar_init(&sent_full[k], 128);
+                mbar_init(&sent_full[k], R::DRAIN_THREADS);
                 mbar_init(&sent_empty[k], 1);
             }
         }
@@ -390,7 +403,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     // Each role branch starts with its register budget and ends with its own copy of the final
     // barrier, so no code is shared between budgets.
-    if (warp >= 8) {
+    if (warp >= 8 && warp < 12) {
         regs_dec<REGS_OTHER>();
       if (warp == WARP_TMA) {
         // ------------------------------------------------------------------ TMA producer
@@ -673,9 +686,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, status));
         if (ok) {
             tc_fence_after();
-            stage_acc_rows<DR, DR>(tmem + lane_off + T_DK, scale, smem + L::K_OFF, krow, MASK && T == 0);
+            // (one TMEM load per accumulator row where the launch's 168 registers per thread
+            // allow it; 64 columns at a time in the 512-thread launch, compiled for 128)
+            constexpr int W = R::DRAIN2 ? 64 : DR;
+            stage_acc_rows<W, DR>(tmem + lane_off + T_DK, scale, smem + L::K_OFF, krow, MASK && T == 0);
             if constexpr (!SPLIT_EPI)
-                stage_acc_rows<DR, DR>(tmem + lane_off + T_DV, 1.f, smem + L::V_OFF, krow, MASK && T == 0);
+                stage_acc_rows<W, DR>(tmem + lane_off + T_DV, 1.f, smem + L::V_OFF, krow, MASK && T == 0);
         }
         fence_proxy_async_smem();
         named_barrier_sync(1, 128);
@@ -692,7 +708,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         regs_dec<REGS_DRAIN>();
         // ------------------------------------------------------------------ dQ drain warps
-        const int wq = warp - 4;
+        const int wq = warp & 3;
+        // with two drain warpgroups: which half of a step's 64 query columns this warp reduces
+        const int half = R::DRAIN2 && warp >= 12;
         const int dcol = wq * 32 + lane;            // column of dQ = TMEM lane of dQ^T
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         // Dropout: keep words of step s for key row dcol of this block (the same lane <-> key
@@ -704,10 +722,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int q0 = i * BQ;
             const int qd = lane & 3;                // this lane's key within its quad
             const uint32_t mkey = static_cast<uint32_t>(jb * BKV + dcol) >> 2;
-            // bit 4t + k of `mine`: query q0 + 4t + qd keeps key 4 mkey + k
+            // bit 4t + k of `mine`: query q0 + 4t + qd keeps key 4 mkey + k (t over this drain
+            // warpgroup's half of the queries with two of them)
+            constexpr int NT = R::DRAIN2 ? BQ / 8 : BQ / 4;
             uint64_t mine = 0ull;
 #pragma unroll
-            for (int t = 0; t < BQ / 4; ++t) {
+            for (int t = half * NT; t < (half + 1) * NT; ++t) {
                 const uint4 w = dropout_words(drop, mkey, static_cast<uint32_t>(q0 + 4 * t + qd),
                                               static_cast<uint32_t>(bhq));
                 mine |= (static_cast<uint64_t>(w.x < drop.thresh) << (4 * t)) |
@@ -715,7 +735,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         (static_cast<uint64_t>(w.z < drop.thresh) << (4 * t + 2)) |
                         (static_cast<uint64_t>(w.w < drop.thresh) << (4 * t + 3));
             }
-            uint64_t *xch = reinterpret_cast<uint64_t *>(smem + L::XCH_OFF);
+            uint64_t *xch = reinterpret_cast<uint64_t *>(smem + L::XCH_OFF) + half * BKV;
             xch[dcol] = mine;
             __syncwarp();
             // from quad lane src, the bits of this lane's key (positions 4t + qd) are queries 4t + src
@@ -724,7 +744,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int src = 0; src < 4; ++src)
                 keep |= ((xch[(dcol & ~3) + src] >> qd) & 0x1111111111111111ull) << src;
             __syncwarp();                           // the exchange words are rewritten next call
-            keep_words[(s & 1) * BKV + dcol] = keep;
+            if constexpr (R::DRAIN2)         // this warpgroup's 32 queries: one half of the word
+                reinterpret_cast<uint32_t *>(keep_words + (s & 1) * BKV + dcol)[half] =
+                    static_cast<uint32_t>(keep >> (32 * half));
+            else
+                keep_words[(s & 1) * BKV + dcol] = keep;
             mbar_arrive(&km_full[s & 1]);
         };
         if (DROP && T > 0) make_keep(0);
@@ -811,16 +835,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (!__all_sync(0xffffffffu, mbar_wait(&dq_full[bsel], (s >> 1) & 1, abort_flag, status))) break;
                 tc_fence_after();
-                uint32_t a[64];
-                tmem_ld_x64(tmem + lane_off + T_BUF + bsel * 128 + B_DQT, a);
+                constexpr int NC = R::DRAIN2 ? BQ / 2 : BQ;   // query columns per drain warp
+                const int c0 = half * NC;
+                uint32_t a[NC];
+                if constexpr (NC == 32) tmem_ld_x32(tmem + lane_off + T_BUF + bsel * 128 + B_DQT + c0, a);
+                else tmem_ld_x64(tmem + lane_off + T_BUF + bsel * 128 + B_DQT, a);
                 tc_fence_before();
                 mbar_arrive(&dq_empty[bsel]);
                 if (dcol < DR) {
-                    const long long row0 = static_cast<long long>(bhq) * N + q0;   // first row of the tile
+                    const long long row0 = static_cast<long long>(bhq) * N + q0 + c0;   // first row
                     float *dst = dQacc + static_cast<size_t>(row0) * DR + dcol;
-                    const int nvalid = min(BQ, qend - q0);   // rows of this tile inside the sequence
+                    const int nvalid = min(NC, qend - q0 - c0);   // of these rows inside the sequence
 #pragma unroll
-                    for (int c = 0; c < BQ; ++c)
+                    for (int c = 0; c < NC; ++c)
                         if (c < nvalid && in_bounds(row0 + c, rows_total, status))
                             atomicAdd(dst + static_cast<size_t>(c) * DR, __uint_as_float(a[c]) * scale);
                 }
@@ -973,13 +1000,15 @@ cudaError_t launch_main(const Problem &p, const CUtensorMap &tmQ, const CUtensor
     else
         kern = p.causal ? bwd_main_kernel<128, 64, true, MASK, DROP, DET>
                         : bwd_main_kernel<128, 64, false, MASK, DROP, DET>;
+    const int threads = p.d == 128 ? Roles<128>::THREADS : Roles<64>::THREADS;
+    const int regs_needed = p.d == 128 ? Roles<128>::REGS_NEEDED : Roles<64>::REGS_NEEDED;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    // the in-kernel register split needs at least REGS_NEEDED registers at launch
+    // the in-kernel register split needs at least this many registers at launch
     cudaFuncAttributes attr{};
     if ((e = cudaFuncGetAttributes(&attr, kern)) != cudaSuccess) return e;
-    if (attr.numRegs * NUM_THREADS < REGS_NEEDED) return cudaErrorInvalidConfiguration;
-    kern<<<static_cast<unsigned>(grid), NUM_THREADS, smem, stream>>>(
+    if (attr.numRegs * threads < regs_needed) return cudaErrorInvalidConfiguration;
+    kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(
         tmQ, tmK, tmV, tmdO, tmdK, tmdV, tmdQ, LSE, D, dQacc, p.Hq, p.Hkv, p.N, BHkv, HC, p.scale,
         scale_log2, mk, dr, dq_sem, status);
     return cudaGetLastError();
