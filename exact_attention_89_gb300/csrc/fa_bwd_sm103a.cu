@@ -25,12 +25,14 @@
 // the tensor core's work on the other.  Inside a buffer, P^T and dS^T (bf16) are both written over
 // the S^T half, which frees the dP^T half for the dQ^T product of the same step.
 //
-// Roles (512 threads at head dim 128, 384 at 64): warps 0-3 softmax-gradient (and the dK / dV
-// epilogue), warps 4-7 dQ drain (query columns 0-31 of each dQ^T tile; at head dim 64 all 64 and
-// the dV half of the epilogue), warps 12-15 (head dim 128) the second dQ drain warpgroup
-// (columns 32-63), warp 8 TMA, warp 9 the S^T / dP^T MMAs and warp 10 the dQ^T / dV / dK MMAs
-// (one elected lane each), warp 11 idle (it completes the third warpgroup for the register split)
-// except in the deterministic variant, where it passes the dQ turns.
+// Roles (640 threads at head dim 128, 384 at 64): warps 0-3 softmax-gradient (queries 0-31 of each
+// step at head dim 128, and the dK epilogue; at 64 all queries and dK), warps 16-19 (head dim 128)
+// the second softmax-gradient warpgroup (queries 32-63, and the dV epilogue), warps 4-7 dQ drain
+// (query columns 0-31 of each dQ^T tile; at head dim 64 all 64 and the dV epilogue), warps 12-15
+// (head dim 128) the second dQ drain warpgroup (columns 32-63), warp 8 TMA, warp 9 the S^T / dP^T
+// MMAs and warp 10 the dQ^T / dV / dK MMAs (one elected lane each), warp 11 idle (it completes
+// the third warpgroup for the register split) except in the deterministic variant, where it
+// passes the dQ turns.
 // TMEM (512 columns): dK [0,128), dV [128,256), buffer b at 256 + 128 b:
 //   [+0,+64) S^T -> P^T [+0,+32) and dS^T [+32,+64);  [+64,+128) dP^T -> dQ^T.
 #include <algorithm>
@@ -53,18 +55,23 @@ constexpr int WARP_MMA2 = 10;     // issues dQ^T, dV and dK
 constexpr int WARP_PASS = 11;     // deterministic variant: passes the dQ turns
 constexpr int NSENT = 4;          // steps the drain warps may run ahead of the turn passer
 // Register split: softmax-gradient warpgroup grows; dQ drain and TMA/MMA warpgroups shrink.
-constexpr uint32_t REGS_GRAD = 256, REGS_DRAIN = 88, REGS_OTHER = 80;
-// Head dim 128: a second dQ drain warpgroup (warps 12-15) takes query columns 32-63 of each dQ^T
-// tile, the first one columns 0-31, so each drain warp issues half of a step's per-element
-// reductions (and, with dropout, half of its keep decisions) and reads its TMEM buffer out
-// sooner.  (At head dim 64 dQ leaves as one bulk reduction per step.)
+// Head dim 128 (WIDE): two softmax-gradient warpgroups (warps 0-3 and 16-19) take query columns
+// 0-31 and 32-63 of each step, and two dQ drain warpgroups (warps 4-7 and 12-15) the same columns
+// of each dQ^T tile, so a step's element-wise work and its per-element reductions (and, with
+// dropout, its keep decisions) are each split over two warps per scheduler.  (At head dim 64 dQ
+// leaves as one bulk reduction per step and one warpgroup of each kind is used.)
 template <int DR>
 struct Roles {
-    static constexpr bool DRAIN2 = DR == 128;
-    static constexpr int THREADS = DRAIN2 ? 512 : NUM_THREADS;
-    static constexpr int DRAIN_THREADS = DRAIN2 ? 256 : 128;
-    // registers the split needs at launch: 65536 with the second drain warpgroup
-    static constexpr int REGS_NEEDED = 128 * (REGS_GRAD + REGS_OTHER) + DRAIN_THREADS * REGS_DRAIN;
+    static constexpr bool WIDE = DR == 128;
+    static constexpr int THREADS = WIDE ? 640 : NUM_THREADS;
+    static constexpr int GRAD_THREADS = WIDE ? 256 : 128;
+    static constexpr int DRAIN_THREADS = WIDE ? 256 : 128;
+    static constexpr uint32_t REGS_GRAD = WIDE ? 152 : 256;
+    static constexpr uint32_t REGS_DRAIN = WIDE ? 48 : 88;
+    static constexpr uint32_t REGS_OTHER = 80;
+    // registers the split needs at launch (the 640-thread launch has 96 per thread)
+    static constexpr int REGS_NEEDED =
+        GRAD_THREADS * REGS_GRAD + DRAIN_THREADS * REGS_DRAIN + 128 * REGS_OTHER;
 };
 constexpr float LOG2E = 1.4426950408889634f;
 // Steps (query head of the group x query tile) a masked CTA can list in shared memory.
@@ -254,6 +261,16 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
     // drain warps are still busy with the last step's per-element reductions then.
     constexpr bool SPLIT_EPI = DQ_TMA;
     using R = Roles<DR>;
+    // TMEM columns (within a buffer) of P^T and dS^T for the 16-query chunk kk: one warpgroup
+    // writes P^T over S^T's first 32 columns and dS^T over the next 32; two write theirs over
+    // their own half of S^T (queries 32 h .. 32 h + 31: P^T at 32 h, dS^T at 32 h + 16), so
+    // neither overwrites S^T columns the other has not read yet.
+    auto pt_col = [](int kk) -> uint32_t {
+        return R::WIDE ? (kk >> 1) * 32 + (kk & 1) * 8 : B_PT + kk * 8;
+    };
+    auto dst_col = [](int kk) -> uint32_t {
+        return R::WIDE ? (kk >> 1) * 32 + 16 + (kk & 1) * 8 : B_DST + kk * 8;
+    };
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -359,7 +376,7 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(&s_full[k], 1);
-            mbar_init(&p_full[k], 128);
+            mbar_init(&p_full[k], R::GRAD_THREADS);
             mbar_init(&dq_full[k], 1);
             mbar_init(&dq_empty[k], R::DRAIN_THREADS);
         }
@@ -369,7 +386,8 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
         mbar_init(&kvd[1], 1);
         if (DROP) {
             uint64_t *kb = reinterpret_cast<uint64_t *>(smem + L::KM_BAR_OFF);
-            for (int k = 0; k < 4; ++k) mbar_init(&kb[k], k < 2 ? R::DRAIN_THREADS : 128);   // full, empty
+            for (int k = 0; k < 4; ++k)                               // full, empty
+                mbar_init(&kb[k], k < 2 ? R::DRAIN_THREADS : R::GRAD_THREADS);
         }
         if (DET) {
             for (int k = 0; k < NSENT; ++k) {
@@ -404,7 +422,7 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
     // Each role branch starts with its register budget and ends with its own copy of the final
     // barrier, so no code is shared between budgets.
     if (warp >= 8 && warp < 12) {
-        regs_dec<REGS_OTHER>();
+        regs_dec<R::REGS_OTHER>();
       if (warp == WARP_TMA) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -500,14 +518,16 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
                     mma_commit(&dq_full[bsel]);
                     const uint64_t dqm = sdesc_add(dq_mn, ring_off(s));
                     const uint64_t dom = sdesc_add(dqm, L::Q_BYTES);
-                    // dV += P^T dO ; dK += dS^T Q   (B operands MN-major: d contiguous)
+                    // dV += P^T dO ; dK += dS^T Q   (B operands MN-major: d contiguous).  The TMEM
+                    // columns of P^T / dS^T for queries 16 kk .. 16 kk + 15: with two gradient
+                    // warpgroups each half of the queries has its own 32 columns (P^T, then dS^T).
 #pragma unroll
                     for (int kk = 0; kk < BQ / 16; ++kk)
-                        mma_ts(tmem + T_DV, buf + B_PT + kk * 8, sdesc_add(dom, kk * 2048), IDESC_KV,
+                        mma_ts(tmem + T_DV, buf + pt_col(kk), sdesc_add(dom, kk * 2048), IDESC_KV,
                                (s > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                     for (int kk = 0; kk < BQ / 16; ++kk)
-                        mma_ts(tmem + T_DK, buf + B_DST + kk * 8, sdesc_add(dqm, kk * 2048), IDESC_KV,
+                        mma_ts(tmem + T_DK, buf + dst_col(kk), sdesc_add(dqm, kk * 2048), IDESC_KV,
                                (s > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(&kvd[bsel]);
                     mma_commit(&q_empty[s % NSQ]);
@@ -550,12 +570,16 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             tc_fence_after();
             tmem_dealloc(tmem, 512);
         }
-    } else if (warp < 4) {
-        regs_inc<REGS_GRAD>();
+    } else if (warp < 4 || warp >= 16) {
+        regs_inc<R::REGS_GRAD>();
         // ------------------------------------------------------------------ P^T / dS^T warps
-        const int krow = warp * 32 + lane;          // key row within the block = TMEM lane
+        const int krow = (warp & 3) * 32 + lane;    // key row within the block = TMEM lane
         const int key = jb * BKV + krow;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        // queries of each step this warp handles: NQ from qoff (two warpgroups: halves)
+        constexpr int NQ = R::WIDE ? BQ / 2 : BQ;
+        const int gh = warp >= 16;
+        const int qoff = gh * NQ;
         const uint64_t c2 = f2_pack(scale_log2, scale_log2);
         bool ok = true;
         // Statistics of step s's query tile: thread t < 64 holds LSE_t * log2 e, t >= 64 holds
@@ -577,7 +601,8 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             }
             return (q < qend) ? Dvec[static_cast<size_t>(bhq) * N + q] : 0.f;
         };
-        float v_next = load_stat(0);
+        // (with two warpgroups the first one loads the statistics for both)
+        float v_next = gh == 0 ? load_stat(0) : 0.f;
         for (int s = 0; s < T; ++s) {
             int g, i;
             step_tile(s, g, i);
@@ -586,11 +611,12 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             const uint32_t buf = tmem + lane_off + T_BUF + bsel * 128;
             float *sbuf = stat + bsel * 2 * BQ;
             const float v = v_next;
-            v_next = load_stat(s + 1);
+            if (gh == 0) v_next = load_stat(s + 1);
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[bsel], (s >> 1) & 1, abort_flag, status));
-            sbuf[krow] = v;
-            // executed by all four warps every step (even after a failed wait) so the counts match
-            named_barrier_sync(1, 128);
+            if (gh == 0) sbuf[krow] = v;
+            // executed by all gradient warps every step (even after a failed wait) so the counts
+            // match
+            named_barrier_sync(1, R::GRAD_THREADS);
             uint64_t keep_s = ~0ull;
             if constexpr (DROP) {
                 if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&km_full[bsel], (s >> 1) & 1, abort_flag, status));
@@ -601,16 +627,18 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             }
             if (ok) {
                 tc_fence_after();
-                // P^T in place over the S^T registers, then dS^T with dP^T streamed in halves
-                uint32_t sr[64];
-                tmem_ld_x64(buf + B_ST, sr);
+                // P^T in place over the S^T registers, then dS^T with dP^T streamed in 32-query
+                // pieces (this warp's queries qoff .. qoff + NQ - 1 of the step)
+                uint32_t sr[NQ];
+                if constexpr (NQ == 32) tmem_ld_x32(buf + B_ST + qoff, sr);
+                else tmem_ld_x64(buf + B_ST, sr);
                 const bool need_mask = (CAUSAL && q0 < jb * BKV + BKV) || (q0 + BQ > qend) ||
                                        (jb * BKV + BKV > kend);
-                const float4 *l4 = reinterpret_cast<const float4 *>(sbuf);
-                const float4 *d4 = reinterpret_cast<const float4 *>(sbuf + BQ);
-                float pf[64];
+                const float4 *l4 = reinterpret_cast<const float4 *>(sbuf + qoff);
+                const float4 *d4 = reinterpret_cast<const float4 *>(sbuf + BQ + qoff);
+                float pf[NQ];
 #pragma unroll
-                for (int c = 0; c < BQ; c += 4) {
+                for (int c = 0; c < NQ; c += 4) {
                     const float4 lse = l4[c >> 2];
                     const float2 pa = f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
                                                        c2, f2_pack(-lse.x, -lse.y)));
@@ -623,17 +651,17 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
                 }
                 if (need_mask) {
 #pragma unroll
-                    for (int c = 0; c < BQ; ++c) {
-                        const int q = q0 + c;
+                    for (int c = 0; c < NQ; ++c) {
+                        const int q = q0 + qoff + c;
                         if ((CAUSAL && key > q) || q >= qend || key >= kend) pf[c] = 0.f;
                     }
                 }
-                uint32_t pp[32], dd[32];
+                uint32_t pp[NQ / 2], dd[NQ / 2];
                 uint64_t keep = ~0ull;                  // bit c: query q0 + c keeps this key
-                if constexpr (DROP) keep = keep_s;
+                if constexpr (DROP) keep = keep_s >> qoff;
                 auto kept = [&](int c) -> bool { return !DROP || ((keep >> c) & 1ull); };
 #pragma unroll
-                for (int c = 0; c < BQ; c += 2) {
+                for (int c = 0; c < NQ; c += 2) {
                     if constexpr (DROP)
                         pp[c >> 1] = pack_bf16x2(kept(c) ? pf[c] * drop.rscale : 0.f,
                                                  kept(c + 1) ? pf[c + 1] * drop.rscale : 0.f);
@@ -641,9 +669,9 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
                         pp[c >> 1] = pack_bf16x2(pf[c], pf[c + 1]);
                 }
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < NQ / 32; ++h) {
                     uint32_t dr[32];
-                    tmem_ld_x32(buf + B_DPT + 32 * h, dr);
+                    tmem_ld_x32(buf + B_DPT + qoff + 32 * h, dr);
                     if constexpr (DROP) {
                         // dP of a dropped pair does not reach P; a kept one is scaled by 1/(1-p)
 #pragma unroll
@@ -665,14 +693,20 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
                         dd[((32 * h + c) >> 1) + 1] = pack_bf16x2(db.x, db.y);
                     }
                 }
-                tmem_st_x32(buf + B_PT, pp);
-                tmem_st_x32(buf + B_DST, dd);
-                // dS^T row -> smem buffer (128B-swizzled, MN-major B operand of the dQ^T product)
+                if constexpr (NQ == 32) {
+                    tmem_st_x16(buf + pt_col(2 * gh), pp);
+                    tmem_st_x16(buf + dst_col(2 * gh), dd);
+                } else {
+                    tmem_st_x32(buf + B_PT, pp);
+                    tmem_st_x32(buf + B_DST, dd);
+                }
+                // dS^T row -> smem buffer (128B-swizzled, MN-major B operand of the dQ^T product):
+                // this warp's 16-byte chunks qoff / 8 ..
                 uint8_t *ds_row = smem + L::DS_OFF + bsel * L::DS_BYTES + krow * 128;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < NQ / 8; ++u) {
                     uint4 w4 = make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
-                    *reinterpret_cast<uint4 *>(ds_row + ((u ^ (krow & 7)) << 4)) = w4;
+                    *reinterpret_cast<uint4 *>(ds_row + (((u + qoff / 8) ^ (krow & 7)) << 4)) = w4;
                 }
                 tmem_wait_st();
                 fence_proxy_async_smem();
@@ -686,31 +720,37 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, status));
         if (ok) {
             tc_fence_after();
-            // (one TMEM load per accumulator row where the launch's 168 registers per thread
-            // allow it; 64 columns at a time in the 512-thread launch, compiled for 128)
-            constexpr int W = R::DRAIN2 ? 64 : DR;
-            stage_acc_rows<W, DR>(tmem + lane_off + T_DK, scale, smem + L::K_OFF, krow, MASK && T == 0);
-            if constexpr (!SPLIT_EPI)
-                stage_acc_rows<W, DR>(tmem + lane_off + T_DV, 1.f, smem + L::V_OFF, krow, MASK && T == 0);
+            // two gradient warpgroups: the first stages dK, the second dV (64 columns per TMEM
+            // load in their register budget)
+            if constexpr (R::WIDE) {
+                if (gh == 0)
+                    stage_acc_rows<64, DR>(tmem + lane_off + T_DK, scale, smem + L::K_OFF, krow, MASK && T == 0);
+                else
+                    stage_acc_rows<64, DR>(tmem + lane_off + T_DV, 1.f, smem + L::V_OFF, krow, MASK && T == 0);
+            } else {
+                stage_acc_rows<DR, DR>(tmem + lane_off + T_DK, scale, smem + L::K_OFF, krow, MASK && T == 0);
+                if constexpr (!SPLIT_EPI)
+                    stage_acc_rows<DR, DR>(tmem + lane_off + T_DV, 1.f, smem + L::V_OFF, krow, MASK && T == 0);
+            }
         }
         fence_proxy_async_smem();
-        named_barrier_sync(1, 128);
+        named_barrier_sync(R::WIDE ? 4 + gh : 1, 128);
         if (ok && krow == 0 && !*abort_flag) {
+            const bool st_dk = !R::WIDE || gh == 0, st_dv = !SPLIT_EPI && (!R::WIDE || gh == 1);
             for (int ch = 0; ch < DR / 64; ++ch) {
-                tma_store_3d(&tmdK, smem + L::K_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
-                if constexpr (!SPLIT_EPI)
-                    tma_store_3d(&tmdV, smem + L::V_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
+                if (st_dk) tma_store_3d(&tmdK, smem + L::K_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
+                if (st_dv) tma_store_3d(&tmdV, smem + L::V_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
             }
             tma_store_commit_and_wait_read();
         }
         tc_fence_before();
         __syncthreads();
     } else {
-        regs_dec<REGS_DRAIN>();
+        regs_dec<R::REGS_DRAIN>();
         // ------------------------------------------------------------------ dQ drain warps
         const int wq = warp & 3;
         // with two drain warpgroups: which half of a step's 64 query columns this warp reduces
-        const int half = R::DRAIN2 && warp >= 12;
+        const int half = R::WIDE && warp >= 12;
         const int dcol = wq * 32 + lane;            // column of dQ = TMEM lane of dQ^T
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         // Dropout: keep words of step s for key row dcol of this block (the same lane <-> key
@@ -724,7 +764,7 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             const uint32_t mkey = static_cast<uint32_t>(jb * BKV + dcol) >> 2;
             // bit 4t + k of `mine`: query q0 + 4t + qd keeps key 4 mkey + k (t over this drain
             // warpgroup's half of the queries with two of them)
-            constexpr int NT = R::DRAIN2 ? BQ / 8 : BQ / 4;
+            constexpr int NT = R::WIDE ? BQ / 8 : BQ / 4;
             uint64_t mine = 0ull;
 #pragma unroll
             for (int t = half * NT; t < (half + 1) * NT; ++t) {
@@ -744,7 +784,7 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             for (int src = 0; src < 4; ++src)
                 keep |= ((xch[(dcol & ~3) + src] >> qd) & 0x1111111111111111ull) << src;
             __syncwarp();                           // the exchange words are rewritten next call
-            if constexpr (R::DRAIN2)         // this warpgroup's 32 queries: one half of the word
+            if constexpr (R::WIDE)         // this warpgroup's 32 queries: one half of the word
                 reinterpret_cast<uint32_t *>(keep_words + (s & 1) * BKV + dcol)[half] =
                     static_cast<uint32_t>(keep >> (32 * half));
             else
@@ -835,7 +875,7 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
                 }
                 if (!__all_sync(0xffffffffu, mbar_wait(&dq_full[bsel], (s >> 1) & 1, abort_flag, status))) break;
                 tc_fence_after();
-                constexpr int NC = R::DRAIN2 ? BQ / 2 : BQ;   // query columns per drain warp
+                constexpr int NC = R::WIDE ? BQ / 2 : BQ;   // query columns per drain warp
                 const int c0 = half * NC;
                 uint32_t a[NC];
                 if constexpr (NC == 32) tmem_ld_x32(tmem + lane_off + T_BUF + bsel * 128 + B_DQT + c0, a);
