@@ -62,12 +62,16 @@ constexpr int NSENT = 4;          // steps the drain warps may run ahead of the 
 // leaves as one bulk reduction per step and one warpgroup of each kind is used.)
 template <int DR>
 struct Roles {
-    static constexpr bool WIDE = DR == 128;
-    static constexpr int THREADS = WIDE ? 640 : NUM_THREADS;
-    static constexpr int GRAD_THREADS = WIDE ? 256 : 128;
-    static constexpr int DRAIN_THREADS = WIDE ? 256 : 128;
-    static constexpr uint32_t REGS_GRAD = WIDE ? 152 : 256;
-    static constexpr uint32_t REGS_DRAIN = WIDE ? 48 : 88;
+    // (two gradient warpgroups at head dim 64 too: 0.691 against 0.695 ms, and the deterministic
+    // variant 5% slower there, its one drain warpgroup then setting the pace)
+    static constexpr bool GRAD2 = DR == 128;       // two softmax-gradient warpgroups
+    static constexpr bool DRAIN2 = DR == 128;      // two dQ drain warpgroups
+    static constexpr int GRAD1_WARP = 16;          // first warp of the second gradient one
+    static constexpr int THREADS = DR == 128 ? 640 : NUM_THREADS;
+    static constexpr int GRAD_THREADS = GRAD2 ? 256 : 128;
+    static constexpr int DRAIN_THREADS = DRAIN2 ? 256 : 128;
+    static constexpr uint32_t REGS_GRAD = GRAD2 ? 152 : 256;
+    static constexpr uint32_t REGS_DRAIN = DRAIN2 ? 48 : 88;
     static constexpr uint32_t REGS_OTHER = 80;
     // registers the split needs at launch (the 640-thread launch has 96 per thread)
     static constexpr int REGS_NEEDED =
@@ -266,10 +270,10 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
     // their own half of S^T (queries 32 h .. 32 h + 31: P^T at 32 h, dS^T at 32 h + 16), so
     // neither overwrites S^T columns the other has not read yet.
     auto pt_col = [](int kk) -> uint32_t {
-        return R::WIDE ? (kk >> 1) * 32 + (kk & 1) * 8 : B_PT + kk * 8;
+        return R::GRAD2 ? (kk >> 1) * 32 + (kk & 1) * 8 : B_PT + kk * 8;
     };
     auto dst_col = [](int kk) -> uint32_t {
-        return R::WIDE ? (kk >> 1) * 32 + 16 + (kk & 1) * 8 : B_DST + kk * 8;
+        return R::GRAD2 ? (kk >> 1) * 32 + 16 + (kk & 1) * 8 : B_DST + kk * 8;
     };
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -570,15 +574,15 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             tc_fence_after();
             tmem_dealloc(tmem, 512);
         }
-    } else if (warp < 4 || warp >= 16) {
+    } else if (warp < 4 || (R::GRAD2 && warp >= R::GRAD1_WARP)) {
         regs_inc<R::REGS_GRAD>();
         // ------------------------------------------------------------------ P^T / dS^T warps
         const int krow = (warp & 3) * 32 + lane;    // key row within the block = TMEM lane
         const int key = jb * BKV + krow;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         // queries of each step this warp handles: NQ from qoff (two warpgroups: halves)
-        constexpr int NQ = R::WIDE ? BQ / 2 : BQ;
-        const int gh = warp >= 16;
+        constexpr int NQ = R::GRAD2 ? BQ / 2 : BQ;
+        const int gh = R::GRAD2 && warp >= R::GRAD1_WARP;
         const int qoff = gh * NQ;
         const uint64_t c2 = f2_pack(scale_log2, scale_log2);
         bool ok = true;
@@ -722,10 +726,10 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             tc_fence_after();
             // two gradient warpgroups: the first stages dK, the second dV (64 columns per TMEM
             // load in their register budget)
-            if constexpr (R::WIDE) {
+            if constexpr (R::GRAD2) {
                 if (gh == 0)
                     stage_acc_rows<64, DR>(tmem + lane_off + T_DK, scale, smem + L::K_OFF, krow, MASK && T == 0);
-                else
+                else if (!SPLIT_EPI)
                     stage_acc_rows<64, DR>(tmem + lane_off + T_DV, 1.f, smem + L::V_OFF, krow, MASK && T == 0);
             } else {
                 stage_acc_rows<DR, DR>(tmem + lane_off + T_DK, scale, smem + L::K_OFF, krow, MASK && T == 0);
@@ -734,9 +738,9 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             }
         }
         fence_proxy_async_smem();
-        named_barrier_sync(R::WIDE ? 4 + gh : 1, 128);
+        named_barrier_sync(R::GRAD2 ? 4 + gh : 1, 128);
         if (ok && krow == 0 && !*abort_flag) {
-            const bool st_dk = !R::WIDE || gh == 0, st_dv = !SPLIT_EPI && (!R::WIDE || gh == 1);
+            const bool st_dk = !R::GRAD2 || gh == 0, st_dv = !SPLIT_EPI && (!R::GRAD2 || gh == 1);
             for (int ch = 0; ch < DR / 64; ++ch) {
                 if (st_dk) tma_store_3d(&tmdK, smem + L::K_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
                 if (st_dv) tma_store_3d(&tmdV, smem + L::V_OFF + ch * L::KV_CHUNK, ch * 64, jb * BKV, bkv);
@@ -750,7 +754,7 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
         // ------------------------------------------------------------------ dQ drain warps
         const int wq = warp & 3;
         // with two drain warpgroups: which half of a step's 64 query columns this warp reduces
-        const int half = R::WIDE && warp >= 12;
+        const int half = R::DRAIN2 && warp >= 12;
         const int dcol = wq * 32 + lane;            // column of dQ = TMEM lane of dQ^T
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         // Dropout: keep words of step s for key row dcol of this block (the same lane <-> key
@@ -764,7 +768,7 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             const uint32_t mkey = static_cast<uint32_t>(jb * BKV + dcol) >> 2;
             // bit 4t + k of `mine`: query q0 + 4t + qd keeps key 4 mkey + k (t over this drain
             // warpgroup's half of the queries with two of them)
-            constexpr int NT = R::WIDE ? BQ / 8 : BQ / 4;
+            constexpr int NT = R::DRAIN2 ? BQ / 8 : BQ / 4;
             uint64_t mine = 0ull;
 #pragma unroll
             for (int t = half * NT; t < (half + 1) * NT; ++t) {
@@ -784,7 +788,7 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             for (int src = 0; src < 4; ++src)
                 keep |= ((xch[(dcol & ~3) + src] >> qd) & 0x1111111111111111ull) << src;
             __syncwarp();                           // the exchange words are rewritten next call
-            if constexpr (R::WIDE)         // this warpgroup's 32 queries: one half of the word
+            if constexpr (R::DRAIN2)         // this warpgroup's 32 queries: one half of the word
                 reinterpret_cast<uint32_t *>(keep_words + (s & 1) * BKV + dcol)[half] =
                     static_cast<uint32_t>(keep >> (32 * half));
             else
@@ -875,7 +879,7 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
                 }
                 if (!__all_sync(0xffffffffu, mbar_wait(&dq_full[bsel], (s >> 1) & 1, abort_flag, status))) break;
                 tc_fence_after();
-                constexpr int NC = R::WIDE ? BQ / 2 : BQ;   // query columns per drain warp
+                constexpr int NC = R::DRAIN2 ? BQ / 2 : BQ;   // query columns per drain warp
                 const int c0 = half * NC;
                 uint32_t a[NC];
                 if constexpr (NC == 32) tmem_ld_x32(tmem + lane_off + T_BUF + bsel * 128 + B_DQT + c0, a);
