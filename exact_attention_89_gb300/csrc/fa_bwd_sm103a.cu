@@ -30,11 +30,13 @@
 // the second softmax-gradient warpgroup (queries 32-63, and the dV epilogue), warps 4-7 dQ drain
 // (query columns 0-31 of each dQ^T tile; at head dim 64 all 64 and the dV epilogue), warps 12-15
 // (head dim 128) the second dQ drain warpgroup (columns 32-63), warp 8 TMA, warp 9 the S^T / dP^T
-// MMAs and warp 10 the dQ^T / dV / dK MMAs (one elected lane each), warp 11 idle (it completes
-// the third warpgroup for the register split) except in the deterministic variant, where it
-// passes the dQ turns.
+// MMAs and warp 10 the dQ^T / dV / dK MMAs (one elected lane each).  Warp 11 completes the third
+// warpgroup for the register split; at head dim 128 it issues the dP^T MMAs (warp 9 then only
+// S^T), and in the deterministic variant it passes the dQ turns instead.
 // TMEM (512 columns): dK [0,128), dV [128,256), buffer b at 256 + 128 b:
-//   [+0,+64) S^T -> P^T [+0,+32) and dS^T [+32,+64);  [+64,+128) dP^T -> dQ^T.
+//   [+0,+64) S^T -> P^T [+0,+32) and dS^T [+32,+64) (two gradient warpgroups: P^T [+0,+16) and
+//   dS^T [+16,+32) for queries 0-31, [+32,+48) and [+48,+64) for 32-63);
+//   [+64,+128) dP^T -> dQ^T.
 #include <algorithm>
 #include <cmath>
 
@@ -265,6 +267,11 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
     // drain warps are still busy with the last step's per-element reductions then.
     constexpr bool SPLIT_EPI = DQ_TMA;
     using R = Roles<DR>;
+    // Head dim 128 outside the deterministic variant (whose warp 11 passes the dQ turns): S^T and
+    // dP^T are issued by two threads (warps 9 and 11), each as soon as its own TMEM columns are
+    // free (S^T after dV / dK of the step two before, dP^T after the drain's read of its dQ^T):
+    // 2-3% faster than one thread issuing both.
+    constexpr bool SPLIT_A = DR == 128 && !DET;
     // TMEM columns (within a buffer) of P^T and dS^T for the 16-query chunk kk: one warpgroup
     // writes P^T over S^T's first 32 columns and dS^T over the next 32; two write theirs over
     // their own half of S^T (queries 32 h .. 32 h + 31: P^T at 32 h, dS^T at 32 h + 16), so
@@ -379,13 +386,13 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             mbar_init(&q_empty[s], 1);
         }
         for (int k = 0; k < 2; ++k) {
-            mbar_init(&s_full[k], 1);
+            mbar_init(&s_full[k], SPLIT_A ? 2 : 1);
             mbar_init(&p_full[k], R::GRAD_THREADS);
             mbar_init(&dq_full[k], 1);
             mbar_init(&dq_empty[k], R::DRAIN_THREADS);
         }
         mbar_init(acc_full, 1);
-        mbar_init(mma_done, 2);            // one commit from each issuer
+        mbar_init(mma_done, SPLIT_A ? 3 : 2);            // one commit from each issuer
         mbar_init(&kvd[0], 1);
         mbar_init(&kvd[1], 1);
         if (DROP) {
@@ -458,11 +465,12 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
                 if (T > 0) mbar_drain(kv_full, 0);
             }
         }
-    } else if (warp == WARP_MMA || warp == WARP_MMA2) {
+    } else if (warp == WARP_MMA || warp == WARP_MMA2 || (SPLIT_A && warp == WARP_PASS)) {
         // ------------------------------------------------------------------ MMA issuers
-        // Two threads issue: one the S^T / dP^T products of step s + 1 as soon as their buffer
-        // is free, the other this step's dQ^T, dV and dK as soon as the gradient warps are done,
-        // so neither stream queues behind the other in one thread.  The reuse of a buffer that
+        // Two threads issue (three with SPLIT_A): one the S^T / dP^T products of step s + 1 as
+        // soon as their buffer is free (with SPLIT_A one thread each), the other this step's
+        // dQ^T, dV and dK as soon as the gradient warps are done, so neither stream queues
+        // behind the other in one thread.  The reuse of a buffer that
         // one in-order stream would order by itself is ordered by barriers: S^T(s+2) waits for
         // dV / dK(s) (kvd, P^T and dS^T are their operands) and for the drain's read of dQ^T(s).
         if (lane == 0) {
@@ -478,32 +486,37 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             const uint64_t dds = sdesc_sw128(smem_u32(smem + L::DS_OFF), L::DS_BYTES, 1024);   // dS^T
             auto ring_off = [&](int s) { return static_cast<uint32_t>((s % NSQ) * 2 * L::Q_BYTES); };
             bool ok = T > 0;
-            if (warp == WARP_MMA) {
+            if (warp != WARP_MMA2) {
+                const bool do_s = !SPLIT_A || warp == WARP_MMA, do_dp = !SPLIT_A || warp == WARP_PASS;
                 // S^T(s) and dP^T(s) into buffer s & 1
                 ok = ok && mbar_wait(kv_full, 0, abort_flag, status);
                 for (int s = 0; s < T && ok; ++s) {
                     const int bsel = s & 1;
                     if (!mbar_wait(&q_full[s % NSQ], (s / NSQ) & 1, abort_flag, status)) break;
-                    if (s >= 2 && (!mbar_wait(&kvd[bsel], ((s - 2) >> 1) & 1, abort_flag, status) ||
-                                   !mbar_wait(&dq_empty[bsel], ((s - 2) >> 1) & 1, abort_flag, status)))
+                    if (s >= 2 && ((do_s && !mbar_wait(&kvd[bsel], ((s - 2) >> 1) & 1, abort_flag, status)) ||
+                                   (do_dp && !mbar_wait(&dq_empty[bsel], ((s - 2) >> 1) & 1, abort_flag, status))))
                         break;
                     tc_fence_after();
                     const uint64_t dq = sdesc_add(dq_k, ring_off(s));
                     const uint64_t ddo = sdesc_add(dq, L::Q_BYTES);
                     const uint32_t buf = tmem + T_BUF + bsel * 128;
+                    if (do_s) {
 #pragma unroll
-                    for (int kk = 0; kk < DR / 16; ++kk) {
-                        const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
-                        const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
-                        mma_ss(buf + B_ST, sdesc_add(dk_k, oa), sdesc_add(dq, ob), IDESC_SP, kk > 0);
+                        for (int kk = 0; kk < DR / 16; ++kk) {
+                            const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
+                            const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
+                            mma_ss(buf + B_ST, sdesc_add(dk_k, oa), sdesc_add(dq, ob), IDESC_SP, kk > 0);
+                        }
                     }
+                    if (do_dp) {
 #pragma unroll
-                    for (int kk = 0; kk < DR / 16; ++kk) {
-                        const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
-                        const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
-                        mma_ss(buf + B_DPT, sdesc_add(dv_k, oa), sdesc_add(ddo, ob), IDESC_SP, kk > 0);
+                        for (int kk = 0; kk < DR / 16; ++kk) {
+                            const uint32_t oa = (kk >> 2) * L::KV_CHUNK + (kk & 3) * 32;
+                            const uint32_t ob = (kk >> 2) * L::Q_CHUNK + (kk & 3) * 32;
+                            mma_ss(buf + B_DPT, sdesc_add(dv_k, oa), sdesc_add(ddo, ob), IDESC_SP, kk > 0);
+                        }
                     }
-                    mma_commit(&s_full[bsel]);
+                    mma_commit(&s_full[bsel]);     // (one commit from each S^T / dP^T issuer)
                 }
             } else {
                 for (int s = 0; s < T && ok; ++s) {
