@@ -72,8 +72,8 @@ struct Roles {
     static constexpr int THREADS = DR == 128 ? 640 : NUM_THREADS;
     static constexpr int GRAD_THREADS = GRAD2 ? 256 : 128;
     static constexpr int DRAIN_THREADS = DRAIN2 ? 256 : 128;
-    static constexpr uint32_t REGS_GRAD = GRAD2 ? 152 : 256;
-    static constexpr uint32_t REGS_DRAIN = DRAIN2 ? 48 : 88;
+    static constexpr uint32_t REGS_GRAD = GRAD2 ? 144 : 256;
+    static constexpr uint32_t REGS_DRAIN = DRAIN2 ? 56 : 88;
     static constexpr uint32_t REGS_OTHER = 80;
     // registers the split needs at launch (the 640-thread launch has 96 per thread)
     static constexpr int REGS_NEEDED =
@@ -599,18 +599,21 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
         const int qoff = gh * NQ;
         const uint64_t c2 = f2_pack(scale_log2, scale_log2);
         bool ok = true;
-        // Statistics of step s's query tile: thread t < 64 holds LSE_t * log2 e, t >= 64 holds
-        // D_{t-64}.  They are loaded one step ahead so the global-load latency overlaps a whole
-        // step instead of sitting between the MMAs and this step's work.
+        // Statistics of this warpgroup's NQ queries of step s: thread t < NQ holds
+        // LSE_{qoff+t} * log2 e, NQ <= t < 2 NQ holds D_{qoff+t-NQ} (slot sidx of the step's stat
+        // buffer; with two warpgroups each fills and reads only its own half, so they never
+        // wait for each other).  They are loaded one step ahead so the global-load latency
+        // overlaps a whole step instead of sitting between the MMAs and this step's work.
+        const int sidx = krow < NQ ? qoff + krow : (krow < 2 * NQ ? BQ + qoff + krow - NQ : -1);
         auto load_stat = [&](int s) -> float {
-            if (s >= T) return 0.f;
+            if (s >= T || sidx < 0) return 0.f;
             int g, i;
             step_tile(s, g, i);
             const int bhq = b * Hq + hk * G + g;
-            const int q = i * BQ + (krow & (BQ - 1));
+            const int q = i * BQ + qoff + krow % NQ;
             if (q < qend && !in_bounds(static_cast<long long>(bhq) * N + q, rows_total, status))
                 return 0.f;                                  // (debug builds: reported)
-            if (krow < BQ) {
+            if (krow < NQ) {
                 if (q >= qend) return INFINITY;
                 const float lse = LSE[static_cast<size_t>(bhq) * N + q];
                 // a row with no allowed key (LSE = -inf) gets P = 0 from +inf
@@ -618,8 +621,7 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             }
             return (q < qend) ? Dvec[static_cast<size_t>(bhq) * N + q] : 0.f;
         };
-        // (with two warpgroups the first one loads the statistics for both)
-        float v_next = gh == 0 ? load_stat(0) : 0.f;
+        float v_next = load_stat(0);
         for (int s = 0; s < T; ++s) {
             int g, i;
             step_tile(s, g, i);
@@ -628,12 +630,12 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
             const uint32_t buf = tmem + lane_off + T_BUF + bsel * 128;
             float *sbuf = stat + bsel * 2 * BQ;
             const float v = v_next;
-            if (gh == 0) v_next = load_stat(s + 1);
+            v_next = load_stat(s + 1);
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[bsel], (s >> 1) & 1, abort_flag, status));
-            if (gh == 0) sbuf[krow] = v;
-            // executed by all gradient warps every step (even after a failed wait) so the counts
-            // match
-            named_barrier_sync(1, R::GRAD_THREADS);
+            if (sidx >= 0) sbuf[sidx] = v;
+            // executed by all warps of the warpgroup every step (even after a failed wait) so the
+            // counts match
+            named_barrier_sync(gh ? 6 : 1, 128);
             uint64_t keep_s = ~0ull;
             if constexpr (DROP) {
                 if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&km_full[bsel], (s >> 1) & 1, abort_flag, status));
