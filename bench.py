@@ -49,25 +49,25 @@ NCU_TRAFFIC = {
     # fa_bwd, three kernels per launch (bwd_preprocess + bwd_main + bwd_dq_convert, read + write):
     # causal_n4096 0.206 + 0.644 + 0.160 GB; causal_d64_n4096 0.073 + 0.291 + 0.070 GB;
     # gqa_n8192 0.206 + 0.860 + 0.161 GB; long_n32768 0.475 + 1.343 + 0.354 GB
-    "fa_bwd_sm103a.cu:82cb528fe6c8cef9:causal_n4096": 1.010e9,
-    "fa_bwd_sm103a.cu:82cb528fe6c8cef9:causal_d64_n4096": 0.433e9,
-    "fa_bwd_sm103a.cu:82cb528fe6c8cef9:gqa_n8192": 1.227e9,
-    "fa_bwd_sm103a.cu:82cb528fe6c8cef9:long_n32768": 2.172e9,
+    "fa_bwd_sm103a.cu:3a963a54061f80b1:causal_n4096": 1.010e9,
+    "fa_bwd_sm103a.cu:3a963a54061f80b1:causal_d64_n4096": 0.433e9,
+    "fa_bwd_sm103a.cu:3a963a54061f80b1:gqa_n8192": 1.227e9,
+    "fa_bwd_sm103a.cu:3a963a54061f80b1:long_n32768": 2.172e9,
     # fa_bwd_masked, three kernels: local_n16384 0.206 + 0.630 + 0.160 GB; varlen_n8192
     # 1.014 + 1.899 + 0.765 GB
-    "fa_bwd_sm103a.cu:82cb528fe6c8cef9:local_n16384": 0.996e9,
-    "fa_bwd_sm103a.cu:82cb528fe6c8cef9:varlen_n8192": 3.678e9,
+    "fa_bwd_sm103a.cu:3a963a54061f80b1:local_n16384": 0.996e9,
+    "fa_bwd_sm103a.cu:3a963a54061f80b1:varlen_n8192": 3.678e9,
     # fa_bwd_dropout, three kernels: 0.206 + 0.640 + 0.160 GB
-    "fa_bwd_sm103a.cu:82cb528fe6c8cef9:dropout_n4096": 1.006e9,
+    "fa_bwd_sm103a.cu:3a963a54061f80b1:dropout_n4096": 1.006e9,
     # split forward on splitkv_n32768: 25.4 MB read + 0.3 MB write (partials stay in L2)
-    "fa_fwd_sm103a.cu:e4f59c3f62dbbcd0:splitkv_n32768": 2.57e7,
+    "fa_fwd_sm103a.cu:4cb1c4303c86d174:splitkv_n32768": 2.57e7,
     # forward at head dim 64 on fwd_d64: 25.2 MB read (Q, K, V), O written back from L2 later
-    "fa_fwd_sm103a.cu:e4f59c3f62dbbcd0:fwd_d64": 2.52e7,
+    "fa_fwd_sm103a.cu:4cb1c4303c86d174:fwd_d64": 2.52e7,
     # key/value-outer forward: 2.374 GB read + 1.765 GB write
-    "fa_fwd_kvouter_sm103a.cu:e1fd8857363ec7a5:kvouter_n4096": 4.139e9,
+    "fa_fwd_kvouter_sm103a.cu:8eb13f6609ed98d2:kvouter_n4096": 4.139e9,
     # fp32 tensor-core backward: split rows 0.343 GB, split transposes 0.239 GB, dq pass
     # 0.328 GB, dkv pass 0.404 GB
-    "fa_bwd_tf32x3_sm103a.cu:e7a2a8701d4616b6:fp32tc_n4096": 1.314e9,
+    "fa_bwd_tf32x3_sm103a.cu:560f2a16a488a0a8:fp32tc_n4096": 1.314e9,
 }
 
 
@@ -106,16 +106,25 @@ def allowed_pairs(w, q_len, k_len, block_mask, B=None, heads=None) -> float:
     return total
 
 
+def _code_only(src: str) -> str:
+    """C++ source without comments, blank lines and trailing blanks: an edit of a comment leaves
+    the kernel, and so its key, unchanged."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_sources_hash(kernel_file: str) -> str:
-    """Key prefix for NCU_TRAFFIC: the kernel's source file and the device headers it uses."""
+    """Key prefix for NCU_TRAFFIC: the code of the kernel's source file and of the device headers
+    it uses (comments excluded)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_89_gb300", "csrc")
     with open(os.path.join(csrc, kernel_file)) as f:
         own = re.findall(r'^#include "(\w+\.cuh)"', f.read(), re.M)
     extra = [fn for fn in own if fn not in ("fa_ptx.cuh", "fa_philox.cuh")]
     for fn in [kernel_file, "fa_ptx.cuh", "fa_philox.cuh"] + extra:
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(fn.encode() + f.read())
+        with open(os.path.join(csrc, fn)) as f:
+            h.update(fn.encode() + _code_only(f.read()).encode())
     return "%s:%s" % (kernel_file, h.hexdigest()[:16])
 
 

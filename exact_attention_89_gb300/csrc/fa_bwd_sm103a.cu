@@ -52,12 +52,14 @@ constexpr int BQ = 64;            // query rows per step
 constexpr int NSQ = 3;            // Q / dO ring stages
 constexpr int NUM_THREADS = 384;   // three warpgroups (four with a second drain warpgroup)
 constexpr int WARP_TMA = 8;
-constexpr int WARP_MMA = 9;       // TMEM allocator; issues S^T and dP^T
+constexpr int WARP_MMA = 9;       // TMEM allocator; issues S^T (and dP^T unless warp 11 does)
 constexpr int WARP_MMA2 = 10;     // issues dQ^T, dV and dK
-constexpr int WARP_PASS = 11;     // deterministic variant: passes the dQ turns
+constexpr int WARP_PASS = 11;     // head dim 128: issues dP^T; deterministic variant: passes the dQ turns
 constexpr int NSENT = 4;          // steps the drain warps may run ahead of the turn passer
-// Register split: softmax-gradient warpgroup grows; dQ drain and TMA/MMA warpgroups shrink.
-// Head dim 128 (WIDE): two softmax-gradient warpgroups (warps 0-3 and 16-19) take query columns
+// Register split: the softmax-gradient warpgroups grow; dQ drain and TMA/MMA warpgroups shrink
+// (head dim 128: 144 / 56 / 80 of the 96 per thread a 640-thread launch has; 64: 256 / 88 / 80
+// of 168 at 384 threads).
+// Head dim 128: two softmax-gradient warpgroups (warps 0-3 and 16-19) take query columns
 // 0-31 and 32-63 of each step, and two dQ drain warpgroups (warps 4-7 and 12-15) the same columns
 // of each dQ^T tile, so a step's element-wise work and its per-element reductions (and, with
 // dropout, its keep decisions) are each split over two warps per scheduler.  (At head dim 64 dQ
