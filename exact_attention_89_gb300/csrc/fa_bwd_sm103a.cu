@@ -25,12 +25,13 @@
 // the tensor core's work on the other.  Inside a buffer, P^T and dS^T (bf16) are both written over
 // the S^T half, which frees the dP^T half for the dQ^T product of the same step.
 //
-// Roles (640 threads at head dim 128, 384 at 64): warps 0-3 softmax-gradient (queries 0-31 of each
-// step at head dim 128, and the dK epilogue; at 64 all queries and dK), warps 16-19 (head dim 128)
-// the second softmax-gradient warpgroup (queries 32-63, and the dV epilogue), warps 4-7 dQ drain
-// (query columns 0-31 of each dQ^T tile; at head dim 64 all 64 and the dV epilogue), warps 12-15
-// (head dim 128) the second dQ drain warpgroup (columns 32-63), warp 8 TMA, warp 9 the S^T / dP^T
-// MMAs and warp 10 the dQ^T / dV / dK MMAs (one elected lane each).  Warp 11 completes the third
+// Roles (640 threads, or 512 at head dim 64 outside the deterministic variant): warps 0-3
+// softmax-gradient (queries 0-31 of each step, and the dK epilogue), warps 16-19 (12-15 at 512
+// threads) the second softmax-gradient warpgroup (queries 32-63, and the dV epilogue unless the
+// drain warps take it), warps 4-7 dQ drain (query columns 0-31 of each dQ^T tile; at 512 threads
+// all 64, added as one bulk reduction, and the dV epilogue), warps 12-15 (640 threads) the second
+// dQ drain warpgroup (columns 32-63), warp 8 TMA, warp 9 the S^T / dP^T MMAs and warp 10 the
+// dQ^T / dV / dK MMAs (one elected lane each).  Warp 11 completes the third
 // warpgroup for the register split; at head dim 128 it issues the dP^T MMAs (warp 9 then only
 // S^T), and in the deterministic variant it passes the dQ turns instead.
 // TMEM (512 columns): dK [0,128), dV [128,256), buffer b at 256 + 128 b:
@@ -50,28 +51,28 @@ namespace bwd {
 constexpr int BKV = 128;          // keys per CTA (= TMEM lanes)
 constexpr int BQ = 64;            // query rows per step
 constexpr int NSQ = 3;            // Q / dO ring stages
-constexpr int NUM_THREADS = 384;   // three warpgroups (four with a second drain warpgroup)
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;       // TMEM allocator; issues S^T (and dP^T unless warp 11 does)
 constexpr int WARP_MMA2 = 10;     // issues dQ^T, dV and dK
 constexpr int WARP_PASS = 11;     // head dim 128: issues dP^T; deterministic variant: passes the dQ turns
 constexpr int NSENT = 4;          // steps the drain warps may run ahead of the turn passer
 // Register split: the softmax-gradient warpgroups grow; dQ drain and TMA/MMA warpgroups shrink
-// (head dim 128: 144 / 56 / 80 of the 96 per thread a 640-thread launch has; 64: 256 / 88 / 80
-// of 168 at 384 threads).
-// Head dim 128: two softmax-gradient warpgroups (warps 0-3 and 16-19) take query columns
-// 0-31 and 32-63 of each step, and two dQ drain warpgroups (warps 4-7 and 12-15) the same columns
-// of each dQ^T tile, so a step's element-wise work and its per-element reductions (and, with
-// dropout, its keep decisions) are each split over two warps per scheduler.  (At head dim 64 dQ
-// leaves as one bulk reduction per step and one warpgroup of each kind is used.)
-template <int DR>
+// (640 threads: 144 / 56 / 80 of the 96 per thread the launch has; 512 threads: 144 / 88 / 80 of
+// 128).
+// Two softmax-gradient warpgroups (warps 0-3 and 16-19, or 12-15 with one drain warpgroup) take
+// query columns 0-31 and 32-63 of each step.  Where dQ leaves through per-element reductions
+// (head dim 128, and the deterministic variant at 64) two dQ drain warpgroups (warps 4-7 and
+// 12-15) take the same columns of each dQ^T tile, so a step's element-wise work and its
+// per-element reductions (and, with dropout, its keep decisions) are each split over two warps
+// per scheduler; at head dim 64 otherwise dQ leaves as one bulk reduction per step from one drain
+// warpgroup.  (Head dim 64: two gradient warpgroups 0.695 -> 0.633 ms; the deterministic variant
+// 1.107 -> 0.933 ms with two of each kind, 1.147 with one drain warpgroup.)
+template <int DR, bool DET>
 struct Roles {
-    // (two gradient warpgroups at head dim 64 too: 0.691 against 0.695 ms, and the deterministic
-    // variant 5% slower there, its one drain warpgroup then setting the pace)
-    static constexpr bool GRAD2 = DR == 128;       // two softmax-gradient warpgroups
-    static constexpr bool DRAIN2 = DR == 128;      // two dQ drain warpgroups
-    static constexpr int GRAD1_WARP = 16;          // first warp of the second gradient one
-    static constexpr int THREADS = DR == 128 ? 640 : NUM_THREADS;
+    static constexpr bool GRAD2 = true;                   // two softmax-gradient warpgroups
+    static constexpr bool DRAIN2 = DR == 128 || DET;      // two dQ drain warpgroups
+    static constexpr int GRAD1_WARP = DRAIN2 ? 16 : 12;   // first warp of the second gradient one
+    static constexpr int THREADS = DRAIN2 ? 640 : 512;
     static constexpr int GRAD_THREADS = GRAD2 ? 256 : 128;
     static constexpr int DRAIN_THREADS = DRAIN2 ? 256 : 128;
     static constexpr uint32_t REGS_GRAD = GRAD2 ? 144 : 256;
@@ -242,7 +243,7 @@ __device__ __forceinline__ int first_q_tile(int jb) {
 // DET = true: the deterministic variant (ordered dQ reductions, above); dq_sem holds B * Hq *
 // ceil(N / 64) * 4 counters followed by the call's abort word.
 template <int D, int DR, bool CAUSAL, bool MASK, bool DROP, bool DET>
-__global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
+__global__ void __launch_bounds__((Roles<DR, DET>::THREADS), 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__((Roles<DR>::THREADS), 1)
     // the drain warps' per-step work is the short staged reduction (DR = 64); at DR = 128 the
     // drain warps are still busy with the last step's per-element reductions then.
     constexpr bool SPLIT_EPI = DQ_TMA;
-    using R = Roles<DR>;
+    using R = Roles<DR, DET>;
     // Head dim 128 outside the deterministic variant (whose warp 11 passes the dQ turns): S^T and
     // dP^T are issued by two threads (warps 9 and 11), each as soon as its own TMEM columns are
     // free (S^T after dV / dK of the step two before, dP^T after the drain's read of its dQ^T):
@@ -1061,8 +1062,8 @@ cudaError_t launch_main(const Problem &p, const CUtensorMap &tmQ, const CUtensor
     else
         kern = p.causal ? bwd_main_kernel<128, 64, true, MASK, DROP, DET>
                         : bwd_main_kernel<128, 64, false, MASK, DROP, DET>;
-    const int threads = p.d == 128 ? Roles<128>::THREADS : Roles<64>::THREADS;
-    const int regs_needed = p.d == 128 ? Roles<128>::REGS_NEEDED : Roles<64>::REGS_NEEDED;
+    const int threads = p.d == 128 ? Roles<128, DET>::THREADS : Roles<64, DET>::THREADS;
+    const int regs_needed = p.d == 128 ? Roles<128, DET>::REGS_NEEDED : Roles<64, DET>::REGS_NEEDED;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // the in-kernel register split needs at least this many registers at launch
