@@ -32,8 +32,8 @@
 // all 64, added as one bulk reduction, and the dV epilogue), warps 12-15 (640 threads) the second
 // dQ drain warpgroup (columns 32-63), warp 8 TMA, warp 9 the S^T / dP^T MMAs and warp 10 the
 // dQ^T / dV / dK MMAs (one elected lane each).  Warp 11 completes the third
-// warpgroup for the register split; at head dim 128 it issues the dP^T MMAs (warp 9 then only
-// S^T), and in the deterministic variant it passes the dQ turns instead.
+// warpgroup for the register split; it issues the dP^T MMAs (warp 9 then only S^T), and in the
+// deterministic variant it passes the dQ turns instead.
 // TMEM (512 columns): dK [0,128), dV [128,256), buffer b at 256 + 128 b:
 //   [+0,+64) S^T -> P^T [+0,+32) and dS^T [+32,+64) (two gradient warpgroups: P^T [+0,+16) and
 //   dS^T [+16,+32) for queries 0-31, [+32,+48) and [+48,+64) for 32-63);
@@ -54,7 +54,7 @@ constexpr int NSQ = 3;            // Q / dO ring stages
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;       // TMEM allocator; issues S^T (and dP^T unless warp 11 does)
 constexpr int WARP_MMA2 = 10;     // issues dQ^T, dV and dK
-constexpr int WARP_PASS = 11;     // head dim 128: issues dP^T; deterministic variant: passes the dQ turns
+constexpr int WARP_PASS = 11;     // issues dP^T; deterministic variant: passes the dQ turns
 constexpr int NSENT = 4;          // steps the drain warps may run ahead of the turn passer
 // Register split: the softmax-gradient warpgroups grow; dQ drain and TMA/MMA warpgroups shrink
 // (640 threads: 144 / 56 / 80 of the 96 per thread the launch has; 512 threads: 144 / 88 / 80 of
@@ -270,11 +270,11 @@ __global__ void __launch_bounds__((Roles<DR, DET>::THREADS), 1)
     // drain warps are still busy with the last step's per-element reductions then.
     constexpr bool SPLIT_EPI = DQ_TMA;
     using R = Roles<DR, DET>;
-    // Head dim 128 outside the deterministic variant (whose warp 11 passes the dQ turns): S^T and
-    // dP^T are issued by two threads (warps 9 and 11), each as soon as its own TMEM columns are
-    // free (S^T after dV / dK of the step two before, dP^T after the drain's read of its dQ^T):
-    // 2-3% faster than one thread issuing both.
-    constexpr bool SPLIT_A = DR == 128 && !DET;
+    // Outside the deterministic variant (whose warp 11 passes the dQ turns): S^T and dP^T are
+    // issued by two threads (warps 9 and 11), each as soon as its own TMEM columns are free (S^T
+    // after dV / dK of the step two before, dP^T after the drain's read of its dQ^T): 2-3% faster
+    // than one thread issuing both at either head dim.
+    constexpr bool SPLIT_A = !DET;
     // TMEM columns (within a buffer) of P^T and dS^T for the 16-query chunk kk: one warpgroup
     // writes P^T over S^T's first 32 columns and dS^T over the next 32; two write theirs over
     // their own half of S^T (queries 32 h .. 32 h + 31: P^T at 32 h, dS^T at 32 h + 16), so
