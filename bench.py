@@ -48,17 +48,17 @@ MUFU_EX2_PER_CLK_PER_SM = 32.0
 NCU_TRAFFIC = {
     # fa_bwd, three kernels per launch (bwd_preprocess + bwd_main + bwd_dq_convert, read + write):
     # causal_n4096 0.206 + 0.644 + 0.160 GB; causal_d64_n4096 0.073 + 0.291 + 0.070 GB;
-    # gqa_n8192 0.206 + 0.860 + 0.161 GB; long_n32768 0.475 + 1.343 + 0.354 GB
-    "fa_bwd_sm103a.cu:3a963a54061f80b1:causal_n4096": 1.010e9,
-    "fa_bwd_sm103a.cu:3a963a54061f80b1:causal_d64_n4096": 0.433e9,
-    "fa_bwd_sm103a.cu:3a963a54061f80b1:gqa_n8192": 1.227e9,
-    "fa_bwd_sm103a.cu:3a963a54061f80b1:long_n32768": 2.172e9,
+    # gqa_n8192 0.207 + 0.880 + 0.161 GB; long_n32768 0.476 + 1.344 + 0.355 GB
+    "fa_bwd_sm103a.cu:bda22c19073291fe:causal_n4096": 1.010e9,
+    "fa_bwd_sm103a.cu:bda22c19073291fe:causal_d64_n4096": 0.433e9,
+    "fa_bwd_sm103a.cu:bda22c19073291fe:gqa_n8192": 1.247e9,
+    "fa_bwd_sm103a.cu:bda22c19073291fe:long_n32768": 2.174e9,
     # fa_bwd_masked, three kernels: local_n16384 0.206 + 0.630 + 0.160 GB; varlen_n8192
-    # 1.014 + 1.899 + 0.765 GB
-    "fa_bwd_sm103a.cu:3a963a54061f80b1:local_n16384": 0.996e9,
-    "fa_bwd_sm103a.cu:3a963a54061f80b1:varlen_n8192": 3.678e9,
-    # fa_bwd_dropout, three kernels: 0.206 + 0.640 + 0.160 GB
-    "fa_bwd_sm103a.cu:3a963a54061f80b1:dropout_n4096": 1.006e9,
+    # 1.014 + 1.900 + 0.766 GB
+    "fa_bwd_sm103a.cu:bda22c19073291fe:local_n16384": 0.997e9,
+    "fa_bwd_sm103a.cu:bda22c19073291fe:varlen_n8192": 3.680e9,
+    # fa_bwd_dropout, three kernels: 0.206 + 0.640 + 0.161 GB
+    "fa_bwd_sm103a.cu:bda22c19073291fe:dropout_n4096": 1.007e9,
     # split forward on splitkv_n32768: 25.4 MB read + 0.3 MB write (partials stay in L2)
     "fa_fwd_sm103a.cu:4cb1c4303c86d174:splitkv_n32768": 2.57e7,
     # forward at head dim 64 on fwd_d64: 25.2 MB read (Q, K, V), O written back from L2 later
