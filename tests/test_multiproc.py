@@ -85,3 +85,16 @@ def test_split_key_ranges_partition_the_keys():
                 assert k0 % 128 == 0 or k0 == N
                 pos = max(pos, k1)
             assert pos == N
+
+
+def test_traffic_key_ignores_comments_only():
+    """The ncu traffic table is keyed by the kernels' code without comments: a comment edit keeps
+    the key (the captured kernel is unchanged), any edit of the code changes it."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    src = 'int f(int a) { // add one\n    return a + 1; /* the result */\n}\n'
+    assert bench._code_only(src) == bench._code_only(src.replace('add one', 'increment'))
+    assert bench._code_only(src) == bench._code_only(src.replace('/* the result */', '') + '\n\n')
+    assert bench._code_only(src) != bench._code_only(src.replace('a + 1', 'a + 2'))
+    assert bench._code_only('x = 1; /* a\nb */ y = 2;') == 'x = 1;  y = 2;'
